@@ -1,0 +1,75 @@
+"""Dense brute-force attention for tiny inputs (numpy float64) -- a pin for the
+oracle, written with a different structure: K/V are first de-paged into dense
+per-request arrays with fancy indexing, an explicit [q_len x seq_len] boolean
+mask is built, and softmax(scale * Q K^T masked) V is taken as whole-matrix
+operations.  Conversions to float64 go through torch dtypes (bfloat16,
+float8_e4m3fn), not through the oracle's own bit-level decoders.
+
+Semantics (page "[vLLM] FlashAttention": cache shape, GQA ratio,
+varlen metadata; page "RBLN Attention modes": naive attention, causal mask,
+sliding window): row i of request r sits at position ctx + i with
+ctx = seq_len - query_len.
+"""
+import numpy as np
+import torch
+
+
+def to_f64_q(q):
+    return q.detach().cpu().to(torch.float32).to(torch.float64).numpy()
+
+
+def to_f64_kv(kv, kv_dtype, kv_scale):
+    kv = kv.detach().cpu()
+    if kv_dtype == 0:
+        if kv.dtype != torch.bfloat16:
+            kv = kv.view(torch.bfloat16)
+        return kv.to(torch.float32).to(torch.float64).numpy()
+    x = kv.view(torch.float8_e4m3fn).to(torch.float32).to(torch.float64).numpy()
+    x = x.copy()
+    x[0] *= float(kv_scale[0])
+    x[1] *= float(kv_scale[1])
+    return x
+
+
+def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
+                    num_heads, num_kv_heads, head_size, block_size, window=0,
+                    causal=1, kv_dtype=0, kv_scale=(1.0, 1.0)):
+    """Returns (out [T, H, d], lse [T, H]) in float64; rows of tokens outside
+    every request stay NaN."""
+    Q = to_f64_q(q)
+    KV = to_f64_kv(kv_cache, kv_dtype, kv_scale)
+    bt = np.asarray(block_table.cpu() if torch.is_tensor(block_table) else block_table)
+    sl = np.asarray(seq_lens.cpu() if torch.is_tensor(seq_lens) else seq_lens)
+    qsl = np.asarray(query_start_loc.cpu() if torch.is_tensor(query_start_loc)
+                     else query_start_loc)
+    T = Q.shape[0]
+    G = num_heads // num_kv_heads
+    out = np.full((T, num_heads, head_size), np.nan)
+    lse = np.full((T, num_heads), np.nan)
+    bs = block_size
+    for r in range(len(sl)):
+        t0, t1 = int(qsl[r]), int(qsl[r + 1])
+        ql, s = t1 - t0, int(sl[r])
+        if ql == 0:
+            continue
+        nb = (s + bs - 1) // bs
+        blocks = bt[r, :nb]
+        K = KV[0][blocks].reshape(nb * bs, num_kv_heads, head_size)[:s]
+        V = KV[1][blocks].reshape(nb * bs, num_kv_heads, head_size)[:s]
+        pos = (s - ql) + np.arange(ql)[:, None]
+        key = np.arange(s)[None, :]
+        mask = np.ones((ql, s), dtype=bool)
+        if causal:
+            mask &= key <= pos
+        if window > 0:
+            mask &= (pos - key) < window
+        for h in range(num_heads):
+            g = h // G
+            S = float(np.float32(scale)) * (Q[t0:t1, h, :] @ K[:, g, :].T)
+            S = np.where(mask, S, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            W = np.exp(S - m)
+            den = W.sum(axis=1, keepdims=True)
+            out[t0:t1, h, :] = (W @ V[:, g, :]) / den
+            lse[t0:t1, h] = (m + np.log(den))[:, 0]
+    return out, lse
