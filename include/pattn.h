@@ -1,0 +1,169 @@
+/*
+ * pattn.h -- C ABI of the GB300 (sm_103a) paged variable-length attention
+ * library, libpattn.so.
+ *
+ * One call computes exact softmax attention for a batch of requests that
+ * mixes prefills, chunked prefills and single-token decodes, over a paged KV
+ * cache.  The operation is defined on these pages:
+ *   - "[vLLM] FlashAttention", FlashAttentionBackend.get_kv_cache_shape:
+ *     the cache is (2, num_blocks, block_size, num_kv_heads, head_size), index
+ *     0 of the first dimension is K and 1 is V, and block_size must be a
+ *     multiple of 16;
+ *   - same page, FlashAttentionImpl.__init__: num_queries_per_kv =
+ *     num_heads / num_kv_heads query heads share one KV head (GQA);
+ *   - same page, FlashAttentionMetadata: query_start_loc, seq_lens,
+ *     block_table, max_query_len, max_seq_len let one call serve requests of
+ *     different lengths;
+ *   - "[vLLM] other attention backends", TritonAttentionMetadata:
+ *     seq_len = context_len + query_len, so query row i of a request sits at
+ *     position context_len + i;
+ *   - "RBLN Attention modes", overview / Full Attention / SWA: scores over the
+ *     valid tokens, softmax, product with V; causal masking; a sliding window;
+ *     per-partition results merged with online softmax;
+ *   - "[vLLM] FlashAttention", "why this design" item 4: tiled online softmax
+ *     is exact attention, not an approximation.
+ *
+ * For request r: q_len = query_start_loc[r+1] - query_start_loc[r],
+ * s = seq_lens[r], ctx = s - q_len.  Row i (position p = ctx + i) of head h
+ * reads KV head g = h / (num_heads / num_kv_heads).  Key k < s lives in
+ * physical block block_table[r * max_blocks_per_seq + k / block_size], slot
+ * k % block_size.  Key k is visible iff (causal == 0 or k <= p) and
+ * (window <= 0 or p - k < window).  out = softmax(scale * q . K^T over the
+ * visible keys) . V.  A request with q_len == 1 is a decode (the page
+ * "[vLLM] Lightning & Linear Attention", prefill/decode split with
+ * threshold 1); any other q_len > 0 is a prefill; q_len == 0 produces nothing.
+ *
+ * Conventions for every entry point
+ *   - Device pointers are marked [device]; everything else is host memory.
+ *   - The caller owns every buffer.  The library allocates no memory, keeps
+ *     no state between calls and may be called from several host threads.
+ *   - Work is enqueued on ext->stream and the call returns without waiting.
+ *   - Errors are returned, never thrown, and no call aborts the process.
+ */
+#ifndef PATTN_H
+#define PATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PATTN_OK = 0,
+  PATTN_ERR_INVALID_ARGUMENT = 1,   /* NULL pointer, bad size, bad scale     */
+  PATTN_ERR_UNSUPPORTED = 2,        /* valid but not built (head_size, ...)  */
+  PATTN_ERR_WORKSPACE_TOO_SMALL = 3,
+  PATTN_ERR_CUDA = 4,               /* a CUDA runtime call failed            */
+  PATTN_ERR_BAD_METADATA = 5,       /* device-detected: see read_device_status */
+  PATTN_ERR_DEVICE_TIMEOUT = 6      /* device-detected: a bounded wait expired */
+} pattn_status_t;
+
+typedef enum {
+  PATTN_KV_BF16 = 0,      /* K and V stored as bf16                          */
+  PATTN_KV_FP8_E4M3 = 1   /* K and V stored as e4m3 bytes, one fp32 scale each */
+} pattn_kv_dtype_t;
+
+/*
+ * Host-side sizes and resources of one call.  Everything a device-pointer API
+ * cannot learn without a device-to-host copy is passed here, so no call ever
+ * synchronises.  The FlashAttentionMetadata fields (num_actual_tokens,
+ * max_query_len, max_seq_len) have the same meaning.
+ */
+typedef struct {
+  size_t struct_size;     /* sizeof(pattn_ext_t)                              */
+  int num_seqs;           /* B: requests in the batch                         */
+  int num_tokens;         /* T: rows of q and out (>= query_start_loc[B])     */
+  int max_blocks_per_seq; /* row stride of block_table                        */
+  int num_blocks;         /* physical blocks in kv_cache                      */
+  int max_query_len;      /* >= every q_len in the batch                      */
+  int max_seq_len;        /* >= every seq_len in the batch                    */
+  int num_splits;         /* decode KV partitions: 0 = library chooses,
+                             1..PATTN_MAX_SPLITS forces the count             */
+  void* workspace;        /* [device] scratch of >= workspace_bytes, 256-B aligned */
+  size_t workspace_bytes;
+  void* stream;           /* cudaStream_t; NULL = the legacy default stream   */
+} pattn_ext_t;
+
+#define PATTN_MAX_SPLITS 64
+
+/*
+ * pattn_varlen_fwd -- the forward pass.
+ *
+ *   q               [device] bf16 [num_tokens, num_heads, head_size], contiguous
+ *   kv_cache        [device] [2, num_blocks, block_size, num_kv_heads, head_size],
+ *                   contiguous, bf16 or e4m3 bytes per kv_dtype; 16-B aligned
+ *   block_table     [device] int32 [num_seqs, max_blocks_per_seq]; entries past
+ *                   ceil(seq_len / block_size) are never read
+ *   seq_lens        [device] int32 [num_seqs]
+ *   query_start_loc [device] int32 [num_seqs + 1], non-decreasing prefix sum
+ *   out             [device] bf16 [num_tokens, num_heads, head_size]; rows of
+ *                   tokens outside [query_start_loc[0], query_start_loc[B]) are
+ *                   left untouched
+ *   scale           multiplies q . k; finite and >= 0
+ *   num_heads, num_kv_heads   num_heads % num_kv_heads == 0 and
+ *                   num_heads / num_kv_heads <= 16
+ *   head_size       64 or 128
+ *   block_size      a multiple of 16 (the ValueError of get_kv_cache_shape)
+ *   window          <= 0: no window; > 0: keys with p - k < window are visible
+ *   causal          1: k <= p; 0: every key < seq_len (then window must be <= 0)
+ *   kv_dtype        a pattn_kv_dtype_t
+ *   kv_scale        host float[2] {k_scale, v_scale}; required for e4m3, ignored
+ *                   for bf16 (may be NULL)
+ *   ext             host sizes, workspace and stream (see pattn_ext_t)
+ *
+ * Returns PATTN_OK once the work is enqueued.  Host-side checks return
+ * INVALID_ARGUMENT / UNSUPPORTED / WORKSPACE_TOO_SMALL before any CUDA call;
+ * a failed launch returns PATTN_ERR_CUDA.  Metadata the host cannot see
+ * (q_len > seq_len, a block id outside [0, num_blocks), seq_len above
+ * max_blocks_per_seq * block_size or max_seq_len) is detected on the device:
+ * the offending ids are clamped so no access leaves the buffers, the rows of
+ * that request are unspecified but finite, and a status word in the
+ * workspace records it for pattn_read_device_status.
+ */
+pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, void* out, float scale,
+                                int num_heads, int num_kv_heads, int head_size,
+                                int block_size, int window, int causal, int kv_dtype,
+                                const float* kv_scale, const pattn_ext_t* ext);
+
+/*
+ * Workspace bytes pattn_varlen_fwd needs for these sizes (reads num_seqs,
+ * num_tokens, max_query_len, max_seq_len and num_splits from ext; ignores its
+ * workspace and stream).  Returns 0 if the arguments are invalid.
+ */
+size_t pattn_workspace_bytes(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
+                             int head_size, int block_size);
+
+/*
+ * The decode KV partition count pattn_varlen_fwd will use for these sizes
+ * (ext->num_splits if set, else the library's choice).  Partitions are runs of
+ * ceil(n / splits) whole KV blocks over the n blocks a decode row can see,
+ * merged by log-sum-exp ("RBLN Attention modes", flash attention; the Triton
+ * backend's 16 parallel softmax segments).
+ */
+int pattn_decode_splits(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
+                        int block_size, int window);
+
+/*
+ * Reads and clears the device status word of ext->workspace.  Synchronises
+ * ext->stream.  Returns PATTN_OK, PATTN_ERR_BAD_METADATA or
+ * PATTN_ERR_DEVICE_TIMEOUT for the calls since the last read (each
+ * pattn_varlen_fwd call first clears the word on its stream), or
+ * PATTN_ERR_CUDA if the copy fails.
+ */
+pattn_status_t pattn_read_device_status(const pattn_ext_t* ext);
+
+/* A static, human-readable name for a status code. */
+const char* pattn_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int pattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PATTN_H */

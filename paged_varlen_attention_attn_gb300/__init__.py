@@ -1,0 +1,182 @@
+"""Python binding of libpattn -- paged variable-length attention for GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpattn.so`` (built by ``_build.build()``).  There is no CPU or
+PyTorch fallback; if the library is missing, ``load()`` raises.
+
+The names follow the C ABI in ``include/pattn.h``:
+``pattn_varlen_fwd``, ``pattn_workspace_bytes``, ``pattn_decode_splits``,
+``pattn_read_device_status``, ``pattn_status_string``, ``pattn_version``.
+``forward(...)`` is a convenience wrapper for torch tensors that fills the
+extension struct from the tensors' shapes and allocates the workspace with
+torch (plumbing; the library itself allocates nothing).
+"""
+import ctypes
+import os
+
+from . import _build
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+MAX_SPLITS = 64
+
+STATUS = {0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARGUMENT", 2: "PATTN_ERR_UNSUPPORTED",
+          3: "PATTN_ERR_WORKSPACE_TOO_SMALL", 4: "PATTN_ERR_CUDA",
+          5: "PATTN_ERR_BAD_METADATA", 6: "PATTN_ERR_DEVICE_TIMEOUT"}
+
+EXPORTS = ("pattn_varlen_fwd", "pattn_workspace_bytes", "pattn_decode_splits",
+           "pattn_read_device_status", "pattn_status_string", "pattn_version")
+
+
+class PattnError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+class Ext(ctypes.Structure):
+    """pattn_ext_t"""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("num_seqs", ctypes.c_int),
+                ("num_tokens", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("max_query_len", ctypes.c_int),
+                ("max_seq_len", ctypes.c_int), ("num_splits", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("stream", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library_path():
+    return _build.LIB
+
+
+def load(path=None):
+    """Open libpattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise PattnError(4, f"{p} is missing; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.pattn_varlen_fwd.restype = i
+    lib.pattn_varlen_fwd.argtypes = [vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp,
+                                     ctypes.POINTER(Ext)]
+    lib.pattn_workspace_bytes.restype = ctypes.c_size_t
+    lib.pattn_workspace_bytes.argtypes = [ctypes.POINTER(Ext), i, i, i, i]
+    lib.pattn_decode_splits.restype = i
+    lib.pattn_decode_splits.argtypes = [ctypes.POINTER(Ext), i, i, i, i]
+    lib.pattn_read_device_status.restype = i
+    lib.pattn_read_device_status.argtypes = [ctypes.POINTER(Ext)]
+    lib.pattn_status_string.restype = ctypes.c_char_p
+    lib.pattn_status_string.argtypes = [i]
+    lib.pattn_version.restype = i
+    lib.pattn_version.argtypes = []
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_len,
+             max_seq_len, num_splits=0, workspace=0, workspace_bytes=0, stream=0):
+    e = Ext()
+    e.struct_size = ctypes.sizeof(Ext)
+    e.num_seqs, e.num_tokens = int(num_seqs), int(num_tokens)
+    e.max_blocks_per_seq, e.num_blocks = int(max_blocks_per_seq), int(num_blocks)
+    e.max_query_len, e.max_seq_len = int(max_query_len), int(max_seq_len)
+    e.num_splits = int(num_splits)
+    e.workspace = int(workspace) or None
+    e.workspace_bytes = int(workspace_bytes)
+    e.stream = int(stream) or None
+    return e
+
+
+def pattn_varlen_fwd(q, kv_cache, block_table, seq_lens, query_start_loc, out, scale,
+                     num_heads, num_kv_heads, head_size, block_size, window, causal,
+                     kv_dtype, kv_scale, ext, lib=None):
+    """Raw call with integer device pointers; returns the status code."""
+    lib = lib or load()
+    ks = None
+    if kv_scale is not None:
+        ks = (ctypes.c_float * 2)(float(kv_scale[0]), float(kv_scale[1]))
+    return lib.pattn_varlen_fwd(q, kv_cache, block_table, seq_lens, query_start_loc, out,
+                                float(scale), int(num_heads), int(num_kv_heads),
+                                int(head_size), int(block_size), int(window), int(causal),
+                                int(kv_dtype), ks, ctypes.byref(ext))
+
+
+def pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size, lib=None):
+    return (lib or load()).pattn_workspace_bytes(ctypes.byref(ext), num_heads, num_kv_heads,
+                                                 head_size, block_size)
+
+
+def pattn_decode_splits(ext, num_heads, num_kv_heads, block_size, window, lib=None):
+    return (lib or load()).pattn_decode_splits(ctypes.byref(ext), num_heads, num_kv_heads,
+                                               block_size, window)
+
+
+def pattn_read_device_status(ext, lib=None):
+    return (lib or load()).pattn_read_device_status(ctypes.byref(ext))
+
+
+def pattn_status_string(status, lib=None):
+    return (lib or load()).pattn_status_string(int(status)).decode()
+
+
+def pattn_version(lib=None):
+    return (lib or load()).pattn_version()
+
+
+class Workspace:
+    """A torch-allocated device workspace, grown on demand (plumbing only)."""
+
+    def __init__(self):
+        self.buf = None
+
+    def get(self, nbytes, device):
+        import torch
+        nbytes = max(256, int(nbytes))
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != torch.device(device):
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = Workspace()
+
+
+def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_heads,
+            num_kv_heads, head_size, block_size, window=0, causal=1, kv_dtype=KV_BF16,
+            kv_scale=None, max_query_len, max_seq_len, num_splits=0, out=None,
+            workspace=None, stream=None, check=True):
+    """pattn_varlen_fwd on torch tensors (all on one CUDA device).
+
+    max_query_len / max_seq_len are host ints (as in FlashAttentionMetadata):
+    the library never reads device memory on the host.  Returns ``out``.
+    """
+    import torch
+    dev = q.device
+    T = q.shape[0]
+    if out is None:
+        out = torch.empty((T, num_heads, head_size), dtype=torch.bfloat16, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    ext = make_ext(num_seqs=seq_lens.shape[0], num_tokens=T,
+                   max_blocks_per_seq=block_table.shape[1], num_blocks=kv_cache.shape[1],
+                   max_query_len=max_query_len, max_seq_len=max_seq_len,
+                   num_splits=num_splits, stream=stream.cuda_stream)
+    need = pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size)
+    if need == 0:
+        raise PattnError(1, "pattn_workspace_bytes")
+    ws = (workspace or _default_ws).get(need, dev)
+    ext.workspace = ws.data_ptr()
+    ext.workspace_bytes = ws.numel()
+    st = pattn_varlen_fwd(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
+                          seq_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(),
+                          scale, num_heads, num_kv_heads, head_size, block_size, window,
+                          causal, kv_dtype, kv_scale, ext)
+    if check and st != 0:
+        raise PattnError(st, "pattn_varlen_fwd")
+    forward.last_ext = ext
+    return out

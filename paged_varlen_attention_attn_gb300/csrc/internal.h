@@ -1,0 +1,55 @@
+// internal.h -- host/device interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pattn {
+
+// Prefill tiles are BLOCK_M query rows of one head.
+constexpr int BLOCK_M = 128;
+// Key tile of the prefill kernel.
+constexpr int BLOCK_N = 128;
+
+// Header at the start of the workspace (one 256-byte line).
+struct WsHeader {
+  unsigned status;        // PATTN_DEV_* bits
+  int num_prefill_tiles;  // written by the plan kernel
+  int pad[62];
+};
+
+struct Problem {
+  const void* q;
+  const void* kv;
+  const int* block_table;
+  const int* seq_lens;
+  const int* qsl;
+  void* out;
+  float scale;
+  int H, Hkv, G, D, bs, window, causal, kv_dtype;
+  float k_scale, v_scale;
+  int B, T, mbps, NB, max_q, max_s, splits;
+  // workspace views
+  WsHeader* hdr;
+  int2* tiles;       // (request, q-tile) pairs sorted by cost, descending
+  int max_tiles;     // capacity of tiles[]
+  float* o_part;     // [B][H][splits][D]  (splits > 1)
+  float* lse_part;   // [B][H][splits]     (log2 domain)
+  cudaStream_t stream;
+};
+
+// Workspace layout for a problem (offsets in bytes, 256-byte aligned).
+struct WsLayout {
+  size_t tiles_off, o_part_off, lse_off, total;
+  int max_tiles;
+};
+WsLayout workspace_layout(int B, int T, int H, int D, int max_q, int splits);
+
+// Kernel launchers; each returns the launch's cudaError_t.
+cudaError_t launch_plan(const Problem& p);
+cudaError_t launch_decode(const Problem& p);
+cudaError_t launch_combine(const Problem& p);
+cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
+
+}  // namespace pattn

@@ -61,12 +61,14 @@ def shuffle_blocks(case, seed):
     nb = case.kv_cache.shape[1]
     perm = torch.randperm(nb, generator=g)            # new position of block b
     kv = torch.empty_like(case.kv_cache)
-    kv[:, perm] = case.kv_cache
-    bt = case.block_table.clone()
+    kv[:, perm.to(kv.device)] = case.kv_cache
+    bt = case.block_table.cpu().clone()
+    sl = case.seq_lens.cpu()
     for r in range(bt.shape[0]):
-        s = int(case.seq_lens[r])
+        s = int(sl[r])
         n = (s + case.spec.block_size - 1) // case.spec.block_size
         bt[r, :n] = perm[bt[r, :n].long()].to(torch.int32)
-    return W.Case(spec=case.spec, q=case.q, kv_cache=kv, block_table=bt,
+    return W.Case(spec=case.spec, q=case.q, kv_cache=kv,
+                  block_table=bt.to(case.block_table.device),
                   seq_lens=case.seq_lens, query_start_loc=case.query_start_loc,
                   scale=case.scale, kv_scale=case.kv_scale)

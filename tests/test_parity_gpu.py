@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs.  Tolerances: bf16 KV max-abs 2e-2 and mean-abs 2e-3;
+e4m3 KV max-abs 6e-2.  Small cases compare every row; the full-size workloads
+compare sampled rows (the oracle recomputes each one from the definition)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_varlen_attention_attn_gb300 as pa
+import workloads as W
+from cases import shuffle_blocks, small_spec
+from gpu_util import (assert_close, check_case, oracle_all, oracle_sampled, run_gpu,
+                      valid_rows)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_varlen_attention_attn_gb300 import _build
+    _build.build()
+    pa.load()
+
+
+def make(spec):
+    return W.make_case(spec, device=DEV)
+
+
+# ------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_small(G, D):
+    Hkv = 2
+    spec = small_spec(300 + G * 7 + D, H=G * Hkv, Hkv=Hkv, d=D, bs=16, n_req=5, max_s=300,
+                      kinds=("decode",))
+    check_case(make(spec))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 16, 64])
+def test_decode_forced_splits(splits):
+    spec = small_spec(400 + splits, H=8, Hkv=2, d=128, bs=16, n_req=6, max_s=700,
+                      kinds=("decode",))
+    check_case(make(spec), num_splits=splits)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 256])
+@pytest.mark.parametrize("window", [0, 1, 7, 100])
+def test_decode_block_sizes_and_windows(bs, window):
+    spec = small_spec(500 + bs + window, H=8, Hkv=2, d=128, bs=bs, n_req=5, max_s=600,
+                      window=window, kinds=("decode",))
+    check_case(make(spec))
+
+
+@pytest.mark.parametrize("splits", [1, 16])
+def test_decode_fp8(splits):
+    spec = small_spec(600 + splits, H=16, Hkv=2, d=128, bs=64, n_req=4, max_s=2000,
+                      kv_dtype=W.KV_FP8_E4M3, kinds=("decode",))
+    check_case(make(spec), num_splits=splits)
+
+
+def test_decode_noncausal():
+    spec = small_spec(610, H=8, Hkv=2, d=64, bs=16, n_req=4, max_s=300, causal=0,
+                      kinds=("decode",))
+    check_case(make(spec))
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [16, 64, 128, 256])
+def test_prefill_small(D, bs):
+    spec = small_spec(700 + D + bs, H=4, Hkv=2, d=D, bs=bs, n_req=3, max_s=400,
+                      kinds=("prefill",))
+    check_case(make(spec))
+
+
+@pytest.mark.parametrize("window", [1, 5, 128, 200])
+def test_prefill_window(window):
+    spec = small_spec(800 + window, H=4, Hkv=1, d=128, bs=16, n_req=3, max_s=600,
+                      window=window, kinds=("prefill", "chunk"))
+    check_case(make(spec))
+
+
+def test_prefill_noncausal():
+    spec = small_spec(820, H=4, Hkv=2, d=128, bs=32, n_req=3, max_s=400, causal=0,
+                      kinds=("prefill", "chunk"))
+    check_case(make(spec))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mixed_batches(seed):
+    spec = small_spec(900 + seed, H=8, Hkv=2, d=128, bs=16, n_req=7, max_s=520,
+                      window=[0, 64][seed % 2], kinds=("prefill", "decode", "chunk", "empty"))
+    check_case(make(spec))
+
+
+def test_tiles_span_several_and_ragged_tail():
+    # 3 x 128 + 37 query rows, chunked on 300 cached tokens
+    spec = W.CaseSpec("ragged", [421, 1, 129], [721, 50, 129], 8, 2, 128, 16, seed=77)
+    check_case(make(spec))
+
+
+def test_tiny_mixed_workload_all_rows():
+    check_case(make(W.config_spec(1)))
+
+
+def test_decode_first_and_prefill_first_orders_agree():
+    a = W.CaseSpec("pf_first", [64, 1, 1], [100, 300, 90], 8, 2, 128, 16, seed=88)
+    case = make(a)
+    out1 = run_gpu(case)
+    # same requests, decodes first
+    order = [1, 2, 0]
+    ql = [a.q_lens[i] for i in order]
+    qsl = torch.zeros(4, dtype=torch.int32)
+    qsl[1:] = torch.cumsum(torch.tensor(ql), 0)
+    old = case.query_start_loc.cpu()
+    q2 = torch.cat([case.q[int(old[i]):int(old[i + 1])] for i in order])
+    case2 = W.Case(spec=W.CaseSpec("dec_first", ql, [a.seq_lens[i] for i in order], 8, 2, 128,
+                                   16, seed=88),
+                   q=q2, kv_cache=case.kv_cache, block_table=case.block_table[order].contiguous(),
+                   seq_lens=case.seq_lens[order].contiguous(), query_start_loc=qsl.to(DEV),
+                   scale=case.scale)
+    out2 = run_gpu(case2)
+    back = torch.cat([out2[2:66], out2[0:1], out2[1:2]])
+    assert torch.equal(out1, back)
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+def test_block_shuffle_is_bitwise_invariant_on_gpu():
+    spec = small_spec(1000, H=8, Hkv=2, d=128, bs=16, n_req=6, max_s=500, extra_pool=20,
+                      kinds=("prefill", "decode", "chunk"))
+    case = make(spec)
+    a = run_gpu(case)
+    b = run_gpu(shuffle_blocks(case, 5))
+    assert torch.equal(a, b)
+
+
+def test_poisoned_unused_slots_and_blocks():
+    spec = small_spec(1100, H=8, Hkv=2, d=128, bs=16, n_req=6, max_s=500, extra_pool=10,
+                      kinds=("prefill", "decode", "chunk"))
+    case = make(spec)
+    ref = run_gpu(case).clone()
+    kv = case.kv_cache.clone()
+    bs = spec.block_size
+    used = set()
+    for r in range(case.num_seqs):
+        s = int(case.seq_lens[r])
+        nb = (s + bs - 1) // bs
+        used.update(int(b) for b in case.block_table[r, :nb])
+        last = int(case.block_table[r, nb - 1])
+        kv[:, last, s - (nb - 1) * bs:] = float("nan")
+    for b in range(kv.shape[1]):
+        if b not in used:
+            kv[:, b] = float("nan")
+    pc = W.Case(spec=spec, q=case.q, kv_cache=kv, block_table=case.block_table,
+                seq_lens=case.seq_lens, query_start_loc=case.query_start_loc, scale=case.scale)
+    got = run_gpu(pc)
+    assert torch.equal(ref, got)
+
+
+def test_window_at_least_seq_len_equals_full_on_gpu():
+    spec = small_spec(1200, H=8, Hkv=2, d=128, bs=16, n_req=5, max_s=300,
+                      kinds=("prefill", "decode", "chunk"))
+    case = make(spec)
+    full = run_gpu(case)
+    spec_w = W.CaseSpec(**{**spec.__dict__, "window": 300})
+    case_w = W.Case(spec=spec_w, q=case.q, kv_cache=case.kv_cache,
+                    block_table=case.block_table, seq_lens=case.seq_lens,
+                    query_start_loc=case.query_start_loc, scale=case.scale)
+    assert torch.equal(full, run_gpu(case_w))
+
+
+def test_split_count_changes_only_rounding():
+    spec = small_spec(1300, H=8, Hkv=2, d=128, bs=16, n_req=6, max_s=3000, kinds=("decode",))
+    case = make(spec)
+    a = run_gpu(case, num_splits=1).float()
+    b = run_gpu(case, num_splits=16).float()
+    assert (a - b).abs().max().item() <= 1e-2
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample_rows(case, n_per_req=3, heads=None, max_reqs=12, seed=0):
+    rng = np.random.default_rng(seed)
+    qsl = case.query_start_loc.cpu().numpy()
+    H = case.spec.num_heads
+    B = len(qsl) - 1
+    reqs = sorted(set([0, B - 1] + list(rng.choice(B, size=min(B, max_reqs), replace=False))))
+    rows = []
+    for r in reqs:
+        t0, t1 = int(qsl[r]), int(qsl[r + 1])
+        if t1 == t0:
+            continue
+        cand = {t0, t1 - 1}
+        if t1 - t0 > 1:
+            for edge in (127, 128, 255, 256):
+                if t0 + edge < t1:
+                    cand.add(t0 + edge)
+            cand.update(int(x) for x in rng.integers(t0, t1, size=n_per_req))
+        hs = heads if heads is not None else sorted(set([0, H - 1] + list(rng.integers(0, H, 2))))
+        for t in sorted(cand):
+            for h in hs:
+                rows.append((t, h))
+    return rows
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_workload_sampled_rows(cfg):
+    case = make(W.config_spec(cfg))
+    out = run_gpu(case)
+    rows = _sample_rows(case, seed=cfg)
+    ref, _ = oracle_sampled(case, rows)
+    t = torch.tensor([r[0] for r in rows], device=DEV)
+    h = torch.tensor([r[1] for r in rows], device=DEV)
+    got = out[t, h].float().cpu().numpy()
+    assert_close(got, ref, case.spec.kv_dtype)
+    assert torch.isfinite(out.float()).all()
+    del case, out
+    torch.cuda.empty_cache()
