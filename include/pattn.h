@@ -84,6 +84,12 @@ typedef struct {
   void* workspace;        /* [device] scratch of >= workspace_bytes, 256-B aligned */
   size_t workspace_bytes;
   void* stream;           /* cudaStream_t; NULL = the legacy default stream   */
+  void* const* timing_events; /* optional host array of 8 cudaEvent_t, or NULL.
+                             If set, events [2k] and [2k+1] are recorded on
+                             stream right before and after phase k: 0 plan,
+                             1 prefill, 2 decode, 3 combine (a phase that does
+                             not run records both back to back).  For
+                             profiling; the caller owns the events.          */
 } pattn_ext_t;
 
 #define PATTN_MAX_SPLITS 64

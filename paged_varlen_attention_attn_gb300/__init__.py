@@ -41,7 +41,10 @@ class Ext(ctypes.Structure):
                 ("num_blocks", ctypes.c_int), ("max_query_len", ctypes.c_int),
                 ("max_seq_len", ctypes.c_int), ("num_splits", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("stream", ctypes.c_void_p)]
+                ("stream", ctypes.c_void_p),
+                ("timing_events", ctypes.POINTER(ctypes.c_void_p))]
+
+PHASES = ("plan", "prefill", "decode", "combine")
 
 
 _lib = None
@@ -80,7 +83,8 @@ def load(path=None):
 
 
 def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_len,
-             max_seq_len, num_splits=0, workspace=0, workspace_bytes=0, stream=0):
+             max_seq_len, num_splits=0, workspace=0, workspace_bytes=0, stream=0,
+             timing_events=None):
     e = Ext()
     e.struct_size = ctypes.sizeof(Ext)
     e.num_seqs, e.num_tokens = int(num_seqs), int(num_tokens)
@@ -90,6 +94,10 @@ def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_
     e.workspace = int(workspace) or None
     e.workspace_bytes = int(workspace_bytes)
     e.stream = int(stream) or None
+    if timing_events is not None:
+        arr = (ctypes.c_void_p * 8)(*[int(x) for x in timing_events])
+        e._events_keepalive = arr
+        e.timing_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
     return e
 
 
@@ -149,11 +157,12 @@ _default_ws = Workspace()
 def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_heads,
             num_kv_heads, head_size, block_size, window=0, causal=1, kv_dtype=KV_BF16,
             kv_scale=None, max_query_len, max_seq_len, num_splits=0, out=None,
-            workspace=None, stream=None, check=True):
+            workspace=None, stream=None, timing_events=None, check=True):
     """pattn_varlen_fwd on torch tensors (all on one CUDA device).
 
     max_query_len / max_seq_len are host ints (as in FlashAttentionMetadata):
-    the library never reads device memory on the host.  Returns ``out``.
+    the library never reads device memory on the host.  ``timing_events``:
+    optional 8 raw cudaEvent_t handles (see pattn_ext_t).  Returns ``out``.
     """
     import torch
     dev = q.device
@@ -165,7 +174,8 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
     ext = make_ext(num_seqs=seq_lens.shape[0], num_tokens=T,
                    max_blocks_per_seq=block_table.shape[1], num_blocks=kv_cache.shape[1],
                    max_query_len=max_query_len, max_seq_len=max_seq_len,
-                   num_splits=num_splits, stream=stream.cuda_stream)
+                   num_splits=num_splits, stream=stream.cuda_stream,
+                   timing_events=timing_events)
     need = pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size)
     if need == 0:
         raise PattnError(1, "pattn_workspace_bytes")

@@ -231,7 +231,16 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.stream = static_cast<cudaStream_t>(ext->stream);
 
+  // Optional per-phase events (profiling): [2k] before and [2k+1] after phase k.
+  auto mark = [&](int idx) {
+    if (ext->timing_events && ext->timing_events[idx])
+      cudaEventRecord(static_cast<cudaEvent_t>(ext->timing_events[idx]), p.stream);
+  };
+
+  mark(0);
   if (launch_plan(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  mark(1);
+  mark(2);
 
   if (ext->max_query_len > 1) {
     EncodeTiledFn enc = encode_fn();
@@ -266,8 +275,13 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
     }
     if (launch_prefill(p, qmap, kvmap) != cudaSuccess) return PATTN_ERR_CUDA;
   }
+  mark(3);
+  mark(4);
   if (launch_decode(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  mark(5);
+  mark(6);
   if (splits > 1 && launch_combine(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  mark(7);
   return PATTN_OK;
 }
 

@@ -36,9 +36,10 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_ext_struct_layout_matches_c():
-    # size_t + 7 ints (padded) + void* + size_t + void*
-    assert ctypes.sizeof(pa.Ext) == 64
+    # size_t + 7 ints (padded) + void* + size_t + void* + void**
+    assert ctypes.sizeof(pa.Ext) == 72
     assert pa.Ext.workspace.offset == 40 and pa.Ext.stream.offset == 56
+    assert pa.Ext.timing_events.offset == 64
 
 
 def _ext(**kw):
