@@ -162,6 +162,43 @@ int pattn_decode_splits(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
  */
 pattn_status_t pattn_read_device_status(const pattn_ext_t* ext);
 
+/*
+ * pattn_decode_fwd_static -- the decode rows of a batch, with no workspace.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that cannot allocate device memory or hand over a workspace: a plugin inside
+ * an application whose allocator owns all device memory, or code on a
+ * latency-critical path where cudaMalloc / cudaFree would synchronise the
+ * device.  It computes exactly what pattn_varlen_fwd computes for the requests
+ * with query_len == 1 (same kernels, same partition count for the same sizes),
+ * leaves the rows of every other request untouched, and allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Arguments are those of pattn_varlen_fwd; the sizes of pattn_ext_t are passed
+ * directly and `stream` is a cudaStream_t (NULL = legacy default stream).
+ * Scratch comes from a fixed device array of PATTN_STATIC_SCRATCH_BYTES
+ * inside the library, held by every GPU that loads the library until the
+ * process exits.  A batch whose partials need more
+ * (num_seqs * num_heads * splits * (head_size + 1) * 4 bytes, roughly) returns
+ * PATTN_ERR_WORKSPACE_TOO_SMALL; pass a smaller num_splits or use
+ * pattn_varlen_fwd.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the array and it keeps the
+ * last call's contents: calls whose work may overlap on the GPU (different
+ * streams or host threads) race and must be serialised by the caller.
+ * Device-detected metadata errors are clamped as in pattn_varlen_fwd but are
+ * not reported (there is no workspace to read a status from).
+ */
+#define PATTN_STATIC_SCRATCH_BYTES (32u << 20)
+pattn_status_t pattn_decode_fwd_static(const void* q, const void* kv_cache,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       const int32_t* query_start_loc, void* out, float scale,
+                                       int num_heads, int num_kv_heads, int head_size,
+                                       int block_size, int window, int causal, int kv_dtype,
+                                       const float* kv_scale, int num_seqs, int num_tokens,
+                                       int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                       int num_splits, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* pattn_status_string(int status);
 

@@ -25,7 +25,9 @@ STATUS = {0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARGUMENT", 2: "PATTN_ERR_UNSUPPOR
           5: "PATTN_ERR_BAD_METADATA", 6: "PATTN_ERR_DEVICE_TIMEOUT"}
 
 EXPORTS = ("pattn_varlen_fwd", "pattn_workspace_bytes", "pattn_decode_splits",
-           "pattn_read_device_status", "pattn_status_string", "pattn_version")
+           "pattn_read_device_status", "pattn_status_string", "pattn_version",
+           "pattn_decode_fwd_static")
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class PattnError(RuntimeError):
@@ -77,6 +79,9 @@ def load(path=None):
     lib.pattn_status_string.argtypes = [i]
     lib.pattn_version.restype = i
     lib.pattn_version.argtypes = []
+    lib.pattn_decode_fwd_static.restype = i
+    lib.pattn_decode_fwd_static.argtypes = [vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp,
+                                            i, i, i, i, i, i, vp]
     if path is None:
         _lib = lib
     return lib
@@ -113,6 +118,25 @@ def pattn_varlen_fwd(q, kv_cache, block_table, seq_lens, query_start_loc, out, s
                                 float(scale), int(num_heads), int(num_kv_heads),
                                 int(head_size), int(block_size), int(window), int(causal),
                                 int(kv_dtype), ks, ctypes.byref(ext))
+
+
+def pattn_decode_fwd_static(q, kv_cache, block_table, seq_lens, query_start_loc, out, scale,
+                            num_heads, num_kv_heads, head_size, block_size, window, causal,
+                            kv_dtype, kv_scale, num_seqs, num_tokens, max_blocks_per_seq,
+                            num_blocks, max_seq_len, num_splits, stream, lib=None):
+    """Raw call of the workspace-free decode entry point; returns the status.
+    For callers that cannot allocate device memory (see include/pattn.h)."""
+    lib = lib or load()
+    ks = None
+    if kv_scale is not None:
+        ks = (ctypes.c_float * 2)(float(kv_scale[0]), float(kv_scale[1]))
+    return lib.pattn_decode_fwd_static(q, kv_cache, block_table, seq_lens, query_start_loc,
+                                       out, float(scale), int(num_heads), int(num_kv_heads),
+                                       int(head_size), int(block_size), int(window),
+                                       int(causal), int(kv_dtype), ks, int(num_seqs),
+                                       int(num_tokens), int(max_blocks_per_seq),
+                                       int(num_blocks), int(max_seq_len), int(num_splits),
+                                       int(stream) or None)
 
 
 def pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size, lib=None):
