@@ -32,8 +32,9 @@ struct Problem {
   int B, T, mbps, NB, max_q, max_s, splits;
   // workspace views
   WsHeader* hdr;
-  int2* tiles;       // (request, q-tile) pairs sorted by cost, descending
+  int2* tiles;       // (request, row-item) pairs sorted by cost, descending
   int max_tiles;     // capacity of tiles[]
+  int rows_per_item; // query rows of one prefill work item (128 or 256)
   float* o_part;     // [B][H][splits][D]  (splits > 1)
   float* lse_part;   // [B][H][splits]     (log2 domain)
   cudaStream_t stream;
@@ -51,5 +52,8 @@ cudaError_t launch_plan(const Problem& p);
 cudaError_t launch_decode(const Problem& p);
 cudaError_t launch_combine(const Problem& p);
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
+// Query rows one prefill CTA covers: two heads x 128 rows when the GQA group
+// size is even, else one head x 256 rows.
+int prefill_rows_per_item(int G);
 
 }  // namespace pattn

@@ -227,6 +227,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.tiles = reinterpret_cast<int2*>(ws + L.tiles_off);
   p.max_tiles = L.max_tiles;
+  p.rows_per_item = prefill_rows_per_item(p.G);
   p.o_part = reinterpret_cast<float*>(ws + L.o_part_off);
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.stream = static_cast<cudaStream_t>(ext->stream);

@@ -4,7 +4,7 @@
 // computes the distribution of work before the attention kernel runs; this is
 // the same idea with a layout of our own: one CTA reads query_start_loc and
 // seq_lens, validates them, and writes the prefill tiles (request, 128-row
-// query tile) ordered by their number of key tiles, largest first, so the
+// query-row item) ordered by their number of key tiles, largest first, so the
 // heaviest tiles start first (longest-processing-time order).  It also clears
 // the status word, so later kernels of the same call report into a clean one.
 #include "common.cuh"
@@ -25,8 +25,8 @@ __device__ __forceinline__ bool request_ok(const Problem& p, int r, int& q_len, 
 
 __device__ __forceinline__ int tile_cost(const Problem& p, int q_len, int s, int qt) {
   const int ctx = s - q_len;
-  const int i0 = qt * BLOCK_M;
-  const int i_last = min(q_len, i0 + BLOCK_M) - 1;
+  const int i0 = qt * p.rows_per_item;
+  const int i_last = min(q_len, i0 + p.rows_per_item) - 1;
   const int lo = (p.window > 0) ? max(0, ctx + i0 - p.window + 1) : 0;
   const int hi = p.causal ? min(s, ctx + i_last + 1) : s;
   const int c = (hi + BLOCK_N - 1) / BLOCK_N - lo / BLOCK_N;
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
       continue;
     }
     if (q_len <= 1) continue;
-    const int nt = (q_len + BLOCK_M - 1) / BLOCK_M;
+    const int nt = (q_len + p.rows_per_item - 1) / p.rows_per_item;
     for (int qt = 0; qt < nt; ++qt) atomicAdd(&hist[tile_cost(p, q_len, s, qt)], 1);
   }
   __syncthreads();
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   for (int r = tid; r < p.B; r += PLAN_THREADS) {
     int q_len, s, t0;
     if (!request_ok(p, r, q_len, s, t0) || q_len <= 1) continue;
-    const int nt = (q_len + BLOCK_M - 1) / BLOCK_M;
+    const int nt = (q_len + p.rows_per_item - 1) / p.rows_per_item;
     for (int qt = 0; qt < nt; ++qt) {
       const int slot = atomicAdd(&hist[tile_cost(p, q_len, s, qt)], 1);
       if (slot < p.max_tiles) p.tiles[slot] = make_int2(r, qt);

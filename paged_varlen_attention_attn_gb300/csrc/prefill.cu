@@ -4,73 +4,131 @@
 // per 128x128 tile, S = Q K^T and O += P V are two 128x128xD MMAs on the
 // 5th-generation tensor cores.  The method is the tiled, IO-aware attention
 // of "[vLLM] FlashAttention" (introduction; "paper summary"): Q, K and V tiles
-// are staged in on-chip memory, the softmax is fused, and the N x N score
-// matrix never reaches HBM; the online softmax keeps the result exact (same
-// page, "why this design" item 4).
+// are staged on chip, the softmax is fused, and the N x N score matrix never
+// reaches HBM; the online softmax keeps the result exact (same page, "why this
+// design" item 4).
 //
-// One CTA computes one 128-row query tile of one head (rows of one request),
-// six warps:
-//   warps 0-3  softmax + epilogue, thread i owns query row i (TMEM lane i);
-//   warp  4    TMA producer: the Q tile once, then K and V tiles page by page
-//              through block_table into a NST-stage ring;
-//   warp  5    MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//              score buffers, then O += P_j V_j with P_j read back from TMEM.
-// TMEM: S buffers at columns [0,128) and [128,256), O at [256, 256 + D).
-// P_j (bf16) overwrites the first 64 columns of its own S buffer.
+// One CTA owns two 128-row query sub-tiles that read the same K/V tiles:
+// two query heads of one KV group (GQA, num_queries_per_kv even) or, when the
+// group size is odd, two consecutive row tiles of one head.  Twelve warps:
+//   warps 0-3  softmax + epilogue of sub-tile A, thread i owns row i (TMEM lane i)
+//   warps 4-7  softmax + epilogue of sub-tile B
+//   warp  8    TMA producer: both Q tiles once, then K and V tiles page by
+//              page through block_table into two-stage rings
+//   warp  9    MMA issuer (one thread)
+//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
+// [384,384+D).  P (bf16, 64 columns) overwrites the upper half of its S
+// buffer and is read back from TMEM as the A operand of P V.  Issue order does
+// not make an MMA's TMEM operand reads finish before a later MMA writes the
+// same columns, so the next scores of a sub-tile are split in two N = 64
+// halves: keys 0-63 (columns 0-63, disjoint from P) go right after P V, keys
+// 64-127 (columns 64-127, over P) only once P V has completed.
+//
+// The issue order S_A(0), S_B(0), then per key tile j: P V_A(j), S_A(j+1),
+// P V_B(j), S_B(j+1) makes the two sub-tiles ping-pong: while one softmax
+// warpgroup works on its scores the tensor core runs the other sub-tile's
+// MMAs.  Because S_X(j+1) is issued after P V_X(j), the commit that announces
+// S_X(j+1) also covers P V_X(j), so a softmax warpgroup may rescale its O in
+// TMEM as soon as it sees its next scores.
 //
 // The cache is addressed by one 4-D TMA tensor map over
 // [2 * num_blocks][block_size][num_kv_heads][head_size]; a 128-key tile is
-// 128 / block_size page loads (or one partial-page load when block_size >
-// 128), each landing at its rows' offset of a 128-byte-swizzled tile, which is
-// exactly the K-major (for S) and MN-major (for P V) operand layout the MMA
-// descriptors name.  Pages wholly past seq_len are not loaded; V rows at or
-// past seq_len are zeroed in shared memory before P V so stale or NaN slots
-// cannot leak through 0 * NaN.
-//
-// Key tiles wholly outside the causal band or the window are never visited;
-// tiles that straddle an edge are masked per element.  The running max is
-// updated lazily: O in TMEM is rescaled only when a row max grows by more
-// than 2^8, which keeps the result exact because the final normalisation
-// divides by the sum taken with the same reference max.
+// 128 / block_size page loads (one partial-page load when block_size > 128),
+// each landing at its rows' offset of a 128-byte-swizzled tile -- the K-major
+// (for S) and MN-major (for P V) operand layouts the MMA descriptors name.
+// Pages wholly past seq_len are not loaded; V rows at or past seq_len are
+// zeroed in shared memory before P V so stale or NaN slots cannot leak
+// through 0 * NaN.  Key tiles wholly outside the causal band or the window are
+// never visited; tiles that straddle an edge are masked per element.  The
+// running max moves lazily: O is rescaled only when a row max grows by more
+// than 2^8, which stays exact because the final normalisation divides by the
+// sum taken against the same reference max.
 #include "common.cuh"
 #include "internal.h"
 
 namespace pattn {
 namespace {
 
-constexpr int PF_THREADS = 192;
+constexpr int PF_THREADS = 384;
+// Register split (setmaxnreg): the two softmax warpgroups take SOFTMAX_REGS
+// per thread, the producer / MMA warpgroup gives its share back.  The sum must
+// stay within the launch allocation (PF_THREADS x the kernel's register count,
+// checked on the host before every launch) or setmaxnreg.inc would wait forever.
+constexpr int SOFTMAX_REGS = 208;
+constexpr int OTHER_REGS = 80;
+constexpr int SPLIT_REGS_TOTAL = 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS;
 constexpr int PF_NST = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+constexpr unsigned FULL = 0xffffffffu;
 
 template <int D>
 struct PrefillCfg {
   static constexpr int DH = D / 64;                 // 128-byte column blocks
   static constexpr int HALF = BLOCK_M * 128;        // bytes of one 128-row column block
   static constexpr int TILE = DH * HALF;            // bytes of a Q, K or V tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TILE;
+  static constexpr int Q_OFF = 0;                   // two Q tiles
+  static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + PF_NST * TILE;
   static constexpr int BAR_OFF = V_OFF + PF_NST * TILE;
-  // + barriers + alignment slack; at least 116 KB so one CTA holds an SM
-  // (and its 512 TMEM columns) alone
-  static constexpr int SMEM_RAW = BAR_OFF + 256 + 1024;
+  // + barriers + alignment slack; at least 116 KB so one CTA holds an SM (and
+  // its 512 TMEM columns) alone
+  static constexpr int SMEM_RAW = BAR_OFF + 512 + 1024;
   static constexpr int SMEM = SMEM_RAW > 118784 ? SMEM_RAW : 118784;
-  static constexpr unsigned S_COL0 = 0, S_COL1 = 128, O_COL = 256;
+  // TMEM columns of sub-tile X's scores and output
+  __device__ static constexpr unsigned s_col(int X) { return X ? 128u : 0u; }
+  __device__ static constexpr unsigned o_col(int X) { return X ? 384u : 256u; }
 };
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full[2];
   uint64_t k_full[PF_NST];
   uint64_t v_full[PF_NST];
-  uint64_t kv_empty[PF_NST];
-  uint64_t s_full[2];
+  uint64_t k_empty[PF_NST];
+  uint64_t v_empty[PF_NST];
+  uint64_t s_full[2];   // one phase per key tile of sub-tile X
   uint64_t p_full[2];
-  uint64_t o_done;   // one phase per P V
-  uint64_t o_final;  // the last P V only (an unambiguous wait for the epilogue)
-  uint64_t drain;    // every MMA issued, before TMEM is released
+  uint64_t o_final[2];  // the last P V of sub-tile X
+  uint64_t pv_done[2];  // one phase per P V of sub-tile X (read back by the MMA thread)
+  uint64_t drain;       // every MMA issued, before TMEM is released
   unsigned tmem_base;
   int abort_flag;
 };
+
+struct Sub {
+  int h, i0, i_last, x0, x1;
+  bool valid;
+  __device__ bool active(int kt) const { return valid && kt >= x0 && kt < x1; }
+};
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0, a1) * (b, b) + (c, c) on the paired fp32 pipe.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%0, %1};\n\t"
+      "mov.b64 rb, {%2, %2};\n\t"
+      "mov.b64 rc, {%3, %3};\n\t"
+      "fma.rn.f32x2 ra, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rb;\n\t"
+      "mov.b64 ra, {%0, %1};\n\t"
+      "mov.b64 rb, {%2, %3};\n\t"
+      "add.f32x2 ra, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
 
 template <int D>
 __global__ void __launch_bounds__(PF_THREADS, 1)
@@ -83,8 +141,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + C::BAR_OFF);
   unsigned* status = &p.hdr->status;
 
-  const int rank = blockIdx.x / p.H;
-  const int h = blockIdx.x % p.H;
+  // ------------------------------------------------------------ work item
+  const bool head_pairs = (p.G % 2) == 0;
+  const int NP = head_pairs ? p.H / 2 : p.H;
+  const int rank = blockIdx.x / NP;
+  const int pidx = blockIdx.x % NP;
   if (rank >= p.hdr->num_prefill_tiles) return;
   const int2 tl = p.tiles[rank];
   const int r = tl.x, qt = tl.y;
@@ -92,30 +153,44 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int q_len = p.qsl[r + 1] - t0;
   const int s = p.seq_lens[r];
   const int ctx = s - q_len;
-  const int i0 = qt * BLOCK_M;
-  const int i_last = min(q_len, i0 + BLOCK_M) - 1;
-  const int g = h / p.G;
   const int W = p.window;
-  const int lo = (W > 0) ? max(0, ctx + i0 - W + 1) : 0;
-  const int hi = p.causal ? min(s, ctx + i_last + 1) : s;
-  const int kt_begin = lo / BLOCK_N;
-  const int n_tiles = max(0, (hi + BLOCK_N - 1) / BLOCK_N - kt_begin);
+
+  // Sub-tile X of this item (no array: the softmax warps pick X at run time).
+  auto make_sub = [&](int X) {
+    Sub u;
+    u.h = head_pairs ? 2 * pidx + X : pidx;
+    u.i0 = head_pairs ? qt * BLOCK_M : qt * 2 * BLOCK_M + X * BLOCK_M;
+    u.valid = u.i0 < q_len;
+    u.i_last = min(q_len, u.i0 + BLOCK_M) - 1;
+    const int lo = (W > 0) ? max(0, ctx + u.i0 - W + 1) : 0;
+    const int hi = p.causal ? min(s, ctx + u.i_last + 1) : s;
+    u.x0 = lo / BLOCK_N;
+    u.x1 = u.valid ? max(u.x0, (hi + BLOCK_N - 1) / BLOCK_N) : u.x0;
+    if (!u.valid) u.x0 = u.x1 = 0;
+    return u;
+  };
+  const Sub subA = make_sub(0), subB = make_sub(1);
+  const int u0 = subB.valid ? min(subA.x0, subB.x0) : subA.x0;
+  const int u1 = subB.valid ? max(subA.x1, subB.x1) : subA.x1;
+  const int n_union = u1 - u0;
+  const int g = subA.h / p.G;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], BLOCK_M);
+      mbar_init(&bars->o_final[i], 1);
+      mbar_init(&bars->pv_done[i], 1);
+    }
     for (int i = 0; i < PF_NST; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], BLOCK_M);
-    }
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_final, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -136,193 +211,267 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int rows_box = p.bs < BLOCK_N ? p.bs : BLOCK_N;
   const int pages_per_tile = BLOCK_N / rows_box;
 
-  if (warp == 4) {
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(OTHER_REGS));
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_union > 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kvmap);
-      mbar_arrive_expect_tx(&bars->q_full, C::TILE);
 #pragma unroll
-      for (int dh = 0; dh < C::DH; ++dh)
-        tma_load_3d(sQ + dh * C::HALF, &qmap, &bars->q_full, dh * 64, h, t0 + i0);
+      for (int X = 0; X < 2; ++X) {
+        const Sub& u = X ? subB : subA;
+        if (!u.valid) continue;
+        mbar_arrive_expect_tx(&bars->q_full[X], C::TILE);
+#pragma unroll
+        for (int dh = 0; dh < C::DH; ++dh)
+          tma_load_3d(sQ + X * C::TILE + dh * C::HALF, &qmap, &bars->q_full[X], dh * 64, u.h,
+                      t0 + u.i0);
+      }
       const int* bt = p.block_table + static_cast<int64_t>(r) * p.mbps;
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int j = 0; j < n_union; ++j) {
         const int st = j % PF_NST;
-        if (j >= PF_NST && !mbar_wait(&bars->kv_empty[st], ((j / PF_NST) - 1) & 1, status, abort_flag))
-          break;
-        const int key_base = (kt_begin + j) * BLOCK_N;
+        const unsigned ph_prev = ((j / PF_NST) - 1) & 1;
+        const int key_base = (u0 + j) * BLOCK_N;
         int n_load = 0;
         for (int pg = 0; pg < pages_per_tile; ++pg)
           if (key_base + pg * rows_box < s) ++n_load;
         const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
-        unsigned char* dk = sK + st * C::TILE;
-        unsigned char* dv = sV + st * C::TILE;
-        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-        for (int pg = 0; pg < pages_per_tile; ++pg) {
-          const int key0 = key_base + pg * rows_box;
-          if (key0 >= s) break;
-          int blk = bt[key0 / p.bs];
-          if (blk < 0 || blk >= p.NB) {
-            flag_status(status, PATTN_DEV_BAD_METADATA);
-            blk = min(max(blk, 0), p.NB - 1);
-          }
-          const int slot = key0 % p.bs;
+        // K first: the next scores need it before the next P V needs V.
+        for (int kv = 0; kv < 2; ++kv) {
+          uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+          uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
+          if (j >= PF_NST && !mbar_wait(empty, ph_prev, status, abort_flag)) break;
+          unsigned char* dst = (kv ? sV : sK) + st * C::TILE;
+          mbar_arrive_expect_tx(full, bytes);
+          for (int pg = 0; pg < pages_per_tile; ++pg) {
+            const int key0 = key_base + pg * rows_box;
+            if (key0 >= s) break;
+            int blk = bt[key0 / p.bs];
+            if (blk < 0 || blk >= p.NB) {
+              flag_status(status, PATTN_DEV_BAD_METADATA);
+              blk = min(max(blk, 0), p.NB - 1);
+            }
 #pragma unroll
-          for (int dh = 0; dh < C::DH; ++dh) {
-            tma_load_4d(dk + dh * C::HALF + pg * rows_box * 128, &kvmap, &bars->k_full[st],
-                        dh * 64, g, slot, blk);
-            tma_load_4d(dv + dh * C::HALF + pg * rows_box * 128, &kvmap, &bars->v_full[st],
-                        dh * 64, g, slot, p.NB + blk);
+            for (int dh = 0; dh < C::DH; ++dh)
+              tma_load_4d(dst + dh * C::HALF + pg * rows_box * 128, &kvmap, full, dh * 64, g,
+                          key0 % p.bs, kv * p.NB + blk);
           }
         }
+        if (*abort_flag) break;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, true, false);
+    if (lane == 0 && n_union > 0) {
+      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N / 2, true, false);
       constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, true, true);
-      const unsigned q_a = smem_u32(sQ), k_a = smem_u32(sK), v_a = smem_u32(sV);
-      auto issue_s = [&](int j) {
-        const int st = j % PF_NST;
-        const unsigned d_t = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
+      // Base descriptors; a byte offset o moves the start address field by
+      // o >> 4 (shared addresses stay far below the field's 256 KB range).
+      const uint64_t q_d = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t k_d = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t v_d = smem_desc_sw128(smem_u32(sV), C::HALF, 1024);
+      int n_pv0 = 0, n_pv1 = 0;
+      bool q_ready0 = false, q_ready1 = false;
+      bool ok = true;
+      for (int j = 0; ok && j <= n_union; ++j) {
+        const int kt = u0 + j;
+        bool k_ready = false, v_ready = false;
+#pragma unroll 1
+        for (int X = 0; X < 2; ++X) {
+          const Sub& u = X ? subB : subA;
+          int& n_pv = X ? n_pv1 : n_pv0;
+          bool& q_ready = X ? q_ready1 : q_ready0;
+          // P V for the previous key tile
+          if (j >= 1 && u.active(kt - 1)) {
+            const int stp = (j - 1) % PF_NST;
+            if (!mbar_wait(&bars->p_full[X], n_pv & 1, status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (!v_ready) {
+              if (!mbar_wait(&bars->v_full[stp], ((j - 1) / PF_NST) & 1, status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              v_ready = true;
+            }
+            tc_fence_after();
+            const unsigned p_t = tmem + C::s_col(X) + 64;
+            const unsigned o_t = tmem + C::o_col(X);
+            const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const unsigned off = (kk >> 2) * C::HALF + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(q_a + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(k_a + st * C::TILE + off, 16, 1024);
-          tc_mma_ss(d_t, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&bars->s_full[j & 1]);
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, status, abort_flag);
-      if (ok) ok = mbar_wait(&bars->k_full[0], 0, status, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) {
-          const int st1 = (j + 1) % PF_NST;
-          if (!mbar_wait(&bars->k_full[st1], ((j + 1) / PF_NST) & 1, status, abort_flag)) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        const int st = j % PF_NST;
-        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, status, abort_flag)) break;
-        if (!mbar_wait(&bars->v_full[st], (j / PF_NST) & 1, status, abort_flag)) break;
-        tc_fence_after();
-        const unsigned p_t = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
+            for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+              tc_mma_ts(o_t, p_t + kk * 8, vb + ((kk * 16 * 128) >> 4), idesc_pv,
+                        (n_pv > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&bars->pv_done[X]);
+            ++n_pv;
+            if (kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
+            if (X == 1 || !subB.active(kt - 1)) tc_commit(&bars->v_empty[stp]);
+          }
+          // scores for this key tile
+          if (j < n_union && u.active(kt)) {
+            const int st = j % PF_NST;
+            if (!k_ready) {
+              if (!mbar_wait(&bars->k_full[st], (j / PF_NST) & 1, status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              k_ready = true;
+            }
+            if (!q_ready) {
+              if (!mbar_wait(&bars->q_full[X], 0, status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              q_ready = true;
+            }
+            tc_fence_after();
+            const uint64_t qb = q_d + ((X * C::TILE) >> 4);
+            const uint64_t kb = k_d + ((st * C::TILE) >> 4);
+            const unsigned s_t = tmem + C::s_col(X);
 #pragma unroll
-        for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          const uint64_t bd =
-              smem_desc_sw128(v_a + st * C::TILE + kk * 16 * 128, C::HALF, 1024);
-          tc_mma_ts(tmem + C::O_COL, p_t + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int hh = 0; hh < 2; ++hh) {
+              // The upper half overwrites P of the previous tile: wait until
+              // that P V has finished reading it.
+              if (hh == 1 && n_pv > 0 &&
+                  !mbar_wait(&bars->pv_done[X], (n_pv - 1) & 1, status, abort_flag)) {
+                ok = false;
+                break;
+              }
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
+                tc_mma_ss(s_t + hh * 64, qb + off, kb + off + ((hh * 64 * 128) >> 4), idesc_s,
+                          kk > 0 ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
+            tc_commit(&bars->s_full[X]);
+            if (X == 1 || !subB.active(kt)) tc_commit(&bars->k_empty[st]);
+          }
         }
-        tc_commit(&bars->o_done);
-        tc_commit(&bars->kv_empty[st]);
-        if (j == n_tiles - 1) tc_commit(&bars->o_final);
       }
       // No MMA may still be running when TMEM is released (matters only when
       // a role gave up on a wait).
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, status, nullptr);
     }
+  }
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int i = i0 + row;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
+    // ------------------------------------------------------------ softmax warpgroups
+    const int X = warp >> 2;            // 0: A (warps 0-3), 1: B (warps 4-7)
+    const Sub u = make_sub(X);
+    const int row = threadIdx.x & 127;  // TMEM lane
+    const int i = u.i0 + row;
     const int pos = ctx + i;
     const int kmax_row = p.causal ? min(s, pos + 1) : s;
-    const int kmin_row = (W > 0) ? pos - W + 1 : -0x7fffffff;
-    const unsigned lane_addr = tmem + (static_cast<unsigned>(warp * 32) << 16);
+    const unsigned lane_base = tmem + (static_cast<unsigned>((warp & 3) * 32) << 16);
+    const unsigned s_t = lane_base + C::s_col(X);
+    const unsigned o_t = lane_base + C::o_col(X);
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int kt = kt_begin + j;
+    bool ok = u.valid;
+    const int nt = u.x1 - u.x0;
+    for (int c = 0; ok && c < nt; ++c) {
+      const int kt = u.x0 + c;
       const int key0 = kt * BLOCK_N;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, status, abort_flag))) {
+      if (!__all_sync(FULL, mbar_wait(&bars->s_full[X], c & 1, status, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const unsigned s_t = lane_addr + ((j & 1) ? C::S_COL1 : C::S_COL0);
       float sv[BLOCK_N];
 #pragma unroll
-      for (int c = 0; c < BLOCK_N / 32; ++c)
-        tc_ld32(s_t + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+      for (int q = 0; q < BLOCK_N / 32; ++q)
+        tc_ld32(s_t + q * 32, *reinterpret_cast<float(*)[32]>(&sv[q * 32]));
       tc_wait_ld();
 
-      // Does any row of this tile see a masked key in it?
-      const bool edge = (key0 + BLOCK_N > s) || (p.causal && key0 + BLOCK_N - 1 > ctx + i0) ||
-                        (W > 0 && (ctx + i_last) - key0 >= W);
-      float mx = -INFINITY;
+      // Does any row of this sub-tile see a masked key in this tile?
+      const bool edge = (key0 + BLOCK_N > s) ||
+                        (p.causal && key0 + BLOCK_N - 1 > ctx + u.i0) ||
+                        (W > 0 && (ctx + u.i_last) - key0 >= W);
       if (edge) {
+        // column limits of this row in the tile: visible iff lim_lo <= q < lim_hi
+        const int lim_hi = kmax_row - key0;
+        const int lim_lo = (W > 0) ? pos - W + 1 - key0 : -1;
 #pragma unroll
-        for (int c = 0; c < BLOCK_N; ++c) {
-          const int k = key0 + c;
-          const bool vis = (k < kmax_row) && (k >= kmin_row);
-          sv[c] = vis ? sv[c] : -INFINITY;
-          mx = fmaxf(mx, sv[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BLOCK_N; ++c) mx = fmaxf(mx, sv[c]);
+        for (int q = 0; q < BLOCK_N; ++q)
+          sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
       }
+      float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int q = 4; q < BLOCK_N - 4; q += 8) {
+        m4[0] = max3(m4[0], sv[q + 0], sv[q + 1]);
+        m4[1] = max3(m4[1], sv[q + 2], sv[q + 3]);
+        m4[2] = max3(m4[2], sv[q + 4], sv[q + 5]);
+        m4[3] = max3(m4[3], sv[q + 6], sv[q + 7]);
+      }
+      m4[0] = max3(m4[0], sv[BLOCK_N - 4], sv[BLOCK_N - 3]);
+      m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
+      const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
       const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
 
       // Lazy rescale: move the reference max only when it grows by > 2^8.
       const bool grow = mx_s > m_run + RESCALE_THRESHOLD;
-      const bool need_o = grow && (m_run != -INFINITY) && (j > 0);
+      const bool need_o = grow && (m_run != -INFINITY) && (c > 0);
       float alpha = 1.f;
       if (grow) {
         alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mx_s);
         l_run *= alpha;
         m_run = mx_s;
       }
-      if (__any_sync(0xffffffffu, need_o)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done, (j - 1) & 1, status, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      if (__any_sync(FULL, need_o)) {
+        // P V of the previous tile is complete: the commit that announced
+        // these scores was issued after it.
         const float a = need_o ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int q = 0; q < D / 32; ++q) {
           float ov[32];
-          tc_ld32(lane_addr + C::O_COL + c * 32, ov);
+          tc_ld32(o_t + q * 32, ov);
           tc_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] *= a;
-          tc_st32(lane_addr + C::O_COL + c * 32, ov);
+          tc_st32(o_t + q * 32, ov);
         }
       }
 
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float psum = 0.f;
-      unsigned pk[BLOCK_N / 2];
+      const float neg_m = -((m_run == -INFINITY) ? 0.f : m_run);
+      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
-      for (int c = 0; c < BLOCK_N; c += 2) {
-        float p0 = fast_exp2(fmaf(sv[c], sl2, -m_use));
-        float p1 = fast_exp2(fmaf(sv[c + 1], sl2, -m_use));
-        if (edge) {
-          p0 = (sv[c] == -INFINITY) ? 0.f : p0;
-          p1 = (sv[c + 1] == -INFINITY) ? 0.f : p1;
+      for (int q = 0; q < BLOCK_N; q += 32) {
+        unsigned pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          float a0 = sv[q + e], a1 = sv[q + e + 1], a2 = sv[q + e + 2], a3 = sv[q + e + 3];
+          ffma2(a0, a1, sl2, neg_m);
+          ffma2(a2, a3, sl2, neg_m);
+          a0 = fast_exp2(a0);
+          a1 = fast_exp2(a1);
+          a2 = fast_exp2(a2);
+          a3 = fast_exp2(a3);
+          if (edge) {
+            a0 = (sv[q + e] == -INFINITY) ? 0.f : a0;
+            a1 = (sv[q + e + 1] == -INFINITY) ? 0.f : a1;
+            a2 = (sv[q + e + 2] == -INFINITY) ? 0.f : a2;
+            a3 = (sv[q + e + 3] == -INFINITY) ? 0.f : a3;
+          }
+          fadd2(ps0, ps1, a0, a1);
+          fadd2(ps2, ps3, a2, a3);
+          pk[e / 2] = pack2<false>(a0, a1);
+          pk[e / 2 + 1] = pack2<false>(a2, a3);
         }
-        psum += p0 + p1;
-        pk[c / 2] = pack2<false>(p0, p1);
+        tc_st16u(s_t + 64 + q / 2, pk);
       }
-      l_run += psum;
-#pragma unroll
-      for (int c = 0; c < BLOCK_N / 2; c += 16)
-        tc_st16u(s_t + c, *reinterpret_cast<unsigned(*)[16]>(&pk[c]));
+      l_run += (ps0 + ps1) + (ps2 + ps3);
       tc_wait_st();
 
-      // Zero V rows at or past seq_len before P V reads them.
-      if (key0 + BLOCK_N > s) {
+      // Zero V rows at or past seq_len before P V reads them (done by the
+      // first sub-tile whose P V reads this tile).
+      if (key0 + BLOCK_N > s && (X == 0 || !subA.active(kt))) {
+        const int j = kt - u0;
         const int st = j % PF_NST;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j / PF_NST) & 1, status, abort_flag))) {
+        if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], (j / PF_NST) & 1, status, abort_flag))) {
           ok = false;
           break;
         }
@@ -331,26 +480,26 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
           for (int dh = 0; dh < C::DH; ++dh)
 #pragma unroll
-            for (int c = 0; c < 128; c += 16)
-              *reinterpret_cast<uint4*>(vrow + dh * C::HALF + c) = make_uint4(0, 0, 0, 0);
+            for (int b = 0; b < 128; b += 16)
+              *reinterpret_cast<uint4*>(vrow + dh * C::HALF + b) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(&bars->p_full[j & 1]);
+      mbar_arrive(&bars->p_full[X]);
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && n_tiles > 0 &&
-        __all_sync(0xffffffffu, mbar_wait(&bars->o_final, 0, status, abort_flag))) {
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                          (static_cast<int64_t>(t0 + i) * p.H + u.h) * D;
+    if (u.valid && ok && nt > 0 &&
+        __all_sync(FULL, mbar_wait(&bars->o_final[X], 0, status, abort_flag))) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                            (static_cast<int64_t>(t0 + i) * p.H + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int q = 0; q < D / 32; ++q) {
         float ov[32];
-        tc_ld32(lane_addr + C::O_COL + c * 32, ov);
+        tc_ld32(o_t + q * 32, ov);
         tc_wait_ld();
         if (i < q_len) {
           unsigned pkd[16];
@@ -358,14 +507,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           for (int e = 0; e < 16; ++e) pkd[e] = pack2<false>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<uint4*>(orow + c * 32 + e * 2) =
+            *reinterpret_cast<uint4*>(orow + q * 32 + e * 2) =
                 make_uint4(pkd[e], pkd[e + 1], pkd[e + 2], pkd[e + 3]);
         }
       }
-    } else if (i < q_len) {
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                            (static_cast<int64_t>(t0 + i) * p.H + h) * D;
-      for (int c = 0; c < D; ++c) orow[c] = __float2bfloat16_rn(0.f);
+    } else if (u.valid && i < q_len) {
+      for (int e = 0; e < D; ++e) orow[e] = __float2bfloat16_rn(0.f);
     }
   }
 
@@ -379,24 +526,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map) {
-  const long long grid = static_cast<long long>(p.max_tiles) * p.H;
-  if (grid == 0) return cudaSuccess;
-  const float sl2 = p.scale * LOG2E;
-  if (p.D == 128) {
-    auto k = prefill_kernel<128>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PrefillCfg<128>::SMEM);
-    if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(grid), PF_THREADS, PrefillCfg<128>::SMEM, p.stream>>>(p, q_map, kv_map, sl2);
-  } else {
-    auto k = prefill_kernel<64>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PrefillCfg<64>::SMEM);
-    if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(grid), PF_THREADS, PrefillCfg<64>::SMEM, p.stream>>>(p, q_map, kv_map, sl2);
-  }
+int prefill_rows_per_item(int G) { return (G % 2 == 0) ? BLOCK_M : 2 * BLOCK_M; }
+
+template <int D>
+cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                             unsigned grid) {
+  auto k = prefill_kernel<D>;
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, k);
+  if (e != cudaSuccess) return e;
+  // The register split must fit in what the CTA is launched with.
+  if (static_cast<long long>(attr.numRegs) * PF_THREADS < SPLIT_REGS_TOTAL)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  k<<<grid, PF_THREADS, PrefillCfg<D>::SMEM, p.stream>>>(p, q_map, kv_map, p.scale * LOG2E);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map) {
+  const int NP = (p.G % 2 == 0) ? p.H / 2 : p.H;
+  const long long grid = static_cast<long long>(p.max_tiles) * NP;
+  if (grid == 0) return cudaSuccess;
+  return p.D == 128 ? launch_prefill_t<128>(p, q_map, kv_map, static_cast<unsigned>(grid))
+                    : launch_prefill_t<64>(p, q_map, kv_map, static_cast<unsigned>(grid));
 }
 
 }  // namespace pattn

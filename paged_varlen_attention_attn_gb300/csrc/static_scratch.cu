@@ -135,6 +135,7 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.tiles = nullptr;
   p.max_tiles = 0;
+  p.rows_per_item = prefill_rows_per_item(p.G);
   p.o_part = reinterpret_cast<float*>(ws + L.o_part_off);
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.stream = static_cast<cudaStream_t>(stream);
