@@ -19,11 +19,10 @@
 //   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
 // [384,384+D).  P (bf16, 64 columns) overwrites the upper half of its S
-// buffer and is read back from TMEM as the A operand of P V.  Issue order does
-// not make an MMA's TMEM operand reads finish before a later MMA writes the
-// same columns, so the next scores of a sub-tile are split in two N = 64
-// halves: keys 0-63 (columns 0-63, disjoint from P) go right after P V, keys
-// 64-127 (columns 64-127, over P) only once P V has completed.
+// buffer and is read back from TMEM as the A operand of P V; the next scores
+// of that sub-tile are issued right after P V and overwrite it.  The tensor
+// core executes one thread's MMAs in issue order, so P V has read its operand
+// before the next S writes the same columns.
 //
 // The issue order S_A(0), S_B(0), then per key tile j: P V_A(j), S_A(j+1),
 // P V_B(j), S_B(j+1) makes the two sub-tiles ping-pong: while one softmax
@@ -55,8 +54,8 @@ constexpr int PF_THREADS = 384;
 // per thread, the producer / MMA warpgroup gives its share back.  The sum must
 // stay within the launch allocation (PF_THREADS x the kernel's register count,
 // checked on the host before every launch) or setmaxnreg.inc would wait forever.
-constexpr int SOFTMAX_REGS = 208;
-constexpr int OTHER_REGS = 80;
+constexpr int SOFTMAX_REGS = 216;
+constexpr int OTHER_REGS = 64;
 constexpr int SPLIT_REGS_TOTAL = 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS;
 constexpr int PF_NST = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
@@ -89,7 +88,6 @@ struct Bars {
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
-  uint64_t pv_done[2];  // one phase per P V of sub-tile X (read back by the MMA thread)
   uint64_t drain;       // every MMA issued, before TMEM is released
   unsigned tmem_base;
   int abort_flag;
@@ -183,7 +181,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], BLOCK_M);
       mbar_init(&bars->o_final[i], 1);
-      mbar_init(&bars->pv_done[i], 1);
     }
     for (int i = 0; i < PF_NST; ++i) {
       mbar_init(&bars->k_full[i], 1);
@@ -215,56 +212,80 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(OTHER_REGS));
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_union > 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kvmap);
+    // The whole warp reads the block ids of a key tile in one coalesced load,
+    // one tile ahead; lane 0 issues the copies.
+    if (n_union > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kvmap);
 #pragma unroll
-      for (int X = 0; X < 2; ++X) {
-        const Sub& u = X ? subB : subA;
-        if (!u.valid) continue;
-        mbar_arrive_expect_tx(&bars->q_full[X], C::TILE);
+        for (int X = 0; X < 2; ++X) {
+          const Sub& u = X ? subB : subA;
+          if (!u.valid) continue;
+          mbar_arrive_expect_tx(&bars->q_full[X], C::TILE);
 #pragma unroll
-        for (int dh = 0; dh < C::DH; ++dh)
-          tma_load_3d(sQ + X * C::TILE + dh * C::HALF, &qmap, &bars->q_full[X], dh * 64, u.h,
-                      t0 + u.i0);
+          for (int dh = 0; dh < C::DH; ++dh)
+            tma_load_3d(sQ + X * C::TILE + dh * C::HALF, &qmap, &bars->q_full[X], dh * 64, u.h,
+                        t0 + u.i0);
+        }
       }
       const int* bt = p.block_table + static_cast<int64_t>(r) * p.mbps;
-      for (int j = 0; j < n_union; ++j) {
-        const int st = j % PF_NST;
-        const unsigned ph_prev = ((j / PF_NST) - 1) & 1;
-        const int key_base = (u0 + j) * BLOCK_N;
-        int n_load = 0;
-        for (int pg = 0; pg < pages_per_tile; ++pg)
-          if (key_base + pg * rows_box < s) ++n_load;
-        const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
-        // K first: the next scores need it before the next P V needs V.
-        for (int kv = 0; kv < 2; ++kv) {
-          uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
-          uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-          if (j >= PF_NST && !mbar_wait(empty, ph_prev, status, abort_flag)) break;
-          unsigned char* dst = (kv ? sV : sK) + st * C::TILE;
-          mbar_arrive_expect_tx(full, bytes);
-          for (int pg = 0; pg < pages_per_tile; ++pg) {
-            const int key0 = key_base + pg * rows_box;
-            if (key0 >= s) break;
-            int blk = bt[key0 / p.bs];
-            if (blk < 0 || blk >= p.NB) {
-              flag_status(status, PATTN_DEV_BAD_METADATA);
-              blk = min(max(blk, 0), p.NB - 1);
-            }
-#pragma unroll
-            for (int dh = 0; dh < C::DH; ++dh)
-              tma_load_4d(dst + dh * C::HALF + pg * rows_box * 128, &kvmap, full, dh * 64, g,
-                          key0 % p.bs, kv * p.NB + blk);
+      // block id of page `lane` of key tile kt (0 when that page is past seq_len)
+      auto page_block = [&](int kt) {
+        const int key0 = kt * BLOCK_N + lane * rows_box;
+        int blk = 0;
+        if (lane < pages_per_tile && key0 < s) {
+          blk = bt[key0 / p.bs];
+          if (blk < 0 || blk >= p.NB) {
+            flag_status(status, PATTN_DEV_BAD_METADATA);
+            blk = min(max(blk, 0), p.NB - 1);
           }
         }
-        if (*abort_flag) break;
+        return blk;
+      };
+      int blk_next = page_block(u0);
+      for (int j = 0; j < n_union; ++j) {
+        int ids[BLOCK_N / 16];
+#pragma unroll
+        for (int pg = 0; pg < BLOCK_N / 16; ++pg) ids[pg] = __shfl_sync(FULL, blk_next, pg);
+        if (j + 1 < n_union) blk_next = page_block(u0 + j + 1);
+        int ok = 1;
+        if (lane == 0) {
+          const int st = j % PF_NST;
+          const unsigned ph_prev = ((j / PF_NST) - 1) & 1;
+          const int key_base = (u0 + j) * BLOCK_N;
+          int n_load = 0;
+          for (int pg = 0; pg < pages_per_tile; ++pg)
+            if (key_base + pg * rows_box < s) ++n_load;
+          const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
+          // K first: the next scores need it before the next P V needs V.
+          for (int kv = 0; kv < 2 && ok; ++kv) {
+            uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+            uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
+            if (j >= PF_NST && !mbar_wait(empty, ph_prev, status, abort_flag)) {
+              ok = 0;
+              break;
+            }
+            unsigned char* dst = (kv ? sV : sK) + st * C::TILE;
+            mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+            for (int pg = 0; pg < BLOCK_N / 16; ++pg) {
+              const int key0 = key_base + pg * rows_box;
+              if (pg >= pages_per_tile || key0 >= s) break;
+#pragma unroll
+              for (int dh = 0; dh < C::DH; ++dh)
+                tma_load_4d(dst + dh * C::HALF + pg * rows_box * 128, &kvmap, full, dh * 64, g,
+                            key0 % p.bs, kv * p.NB + ids[pg]);
+            }
+          }
+        }
+        if (!__shfl_sync(FULL, ok, 0)) break;
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_union > 0) {
-      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N / 2, true, false);
+      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, true, false);
       constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, true, true);
       // Base descriptors; a byte offset o moves the start address field by
       // o >> 4 (shared addresses stay far below the field's 256 KB range).
@@ -304,7 +325,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             for (int kk = 0; kk < BLOCK_N / 16; ++kk)
               tc_mma_ts(o_t, p_t + kk * 8, vb + ((kk * 16 * 128) >> 4), idesc_pv,
                         (n_pv > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&bars->pv_done[X]);
             ++n_pv;
             if (kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
             if (X == 1 || !subB.active(kt - 1)) tc_commit(&bars->v_empty[stp]);
@@ -331,22 +351,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const uint64_t kb = k_d + ((st * C::TILE) >> 4);
             const unsigned s_t = tmem + C::s_col(X);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              // The upper half overwrites P of the previous tile: wait until
-              // that P V has finished reading it.
-              if (hh == 1 && n_pv > 0 &&
-                  !mbar_wait(&bars->pv_done[X], (n_pv - 1) & 1, status, abort_flag)) {
-                ok = false;
-                break;
-              }
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
-                tc_mma_ss(s_t + hh * 64, qb + off, kb + off + ((hh * 64 * 128) >> 4), idesc_s,
-                          kk > 0 ? 1u : 0u);
-              }
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
+              tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
             }
-            if (!ok) break;
             tc_commit(&bars->s_full[X]);
             if (X == 1 || !subB.active(kt)) tc_commit(&bars->k_empty[st]);
           }
