@@ -3,66 +3,115 @@
 // Decode rows (query_len == 1; the prefill/decode split with threshold 1 of
 // "[vLLM] Lightning & Linear Attention") are bound by reading K/V from HBM:
 // each KV byte feeds 2G (bf16) FLOPs, far below the tensor ridge.  One CTA
-// takes one (request, KV head, partition) item, so the G query heads of a KV
-// head share every page it reads (FlashAttentionImpl's num_queries_per_kv).
-// The partition is a run of whole KV blocks ("RBLN Attention modes": flash
-// attention processes the cache by partitions and merges them with online
-// softmax); partial results go to the workspace as (o_p, lse_p) and
-// combine_kernel merges them, or the CTA writes the output directly when
-// there is one partition.
+// takes one (request, group of HG KV heads, partition) item, so the G query
+// heads of a KV head share every page it reads (FlashAttentionImpl's
+// num_queries_per_kv).  The partition is a run of whole KV blocks ("RBLN
+// Attention modes": flash attention processes the cache by partitions and
+// merges them with online softmax); partial results go to the workspace as
+// (o_p, lse_p) and combine_kernel merges them, or the CTA writes the output
+// directly when there is one partition.
 //
-// Data path: each warp streams 16-key units (one unit never straddles a KV
-// block because block_size % 16 == 0) through its own cp.async ring of
-// 16-byte vectors, with a 128-byte XOR swizzle so ldmatrix reads are
-// conflict-free.  Scores and P.V run on mma.sync m16n8k16 with the G heads as
-// the M rows: at G <= 8 that wastes half the MMA rows, which costs nothing
-// here because the kernel waits on HBM.  e4m3 units are widened to f16 in
-// shared memory (exact: every e4m3 value is an f16 value) by CUDA's paired
-// conversion intrinsic; the per-tensor scales are folded into the softmax
-// scale (K) and the final normalisation (V).
+// Data path: a producer warp streams 16-key units through a ring of
+// shared-memory stages; one unit is 16 rows of all HG heads of the group, K
+// and V, fetched with two TMA tensor copies (a 5-D map for 16-bit data, whose
+// box spans both 64-element halves of the head dimension, a 4-D map for e4m3;
+// 128-byte swizzle so ldmatrix reads are conflict-free).  One unit never
+// straddles a KV block because block_size % 16 == 0.  Few, large copies keep
+// many bytes in flight per SM with little issue work, which is what a
+// bandwidth-bound stream needs.  One consumer warp per KV head computes
+// S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 with the keys (and d)
+// as the M rows and the G heads as N, so no MMA rows are wasted at small G;
+// the tensor work is far below what HBM allows either way.  e4m3 K fragments
+// are widened to f16 in registers and V in shared memory with integer bit
+// operations (exact: every e4m3 value times 2^-8 is an f16 value); the
+// per-tensor scales (times 2^8) are folded into the softmax scale (K) and the
+// final normalisation (V).
 #include "common.cuh"
 #include "internal.h"
 
 namespace pattn {
 namespace {
 
-constexpr int DEC_WARPS = 4;
-constexpr int DEC_STAGES = 3;
+// A CTA serves one (request, group of HG KV heads, partition) item: HG
+// consumer warps, one per KV head, plus one producer warp.
 constexpr int UNIT = 16;  // keys per unit
 
-template <int D, bool FP8>
+// KV heads per CTA: 4, or the largest of 2 / 1 dividing num_kv_heads.
+__host__ __device__ constexpr int decode_head_group(int Hkv) {
+  return (Hkv % 4 == 0) ? 4 : (Hkv % 2 == 0) ? 2 : 1;
+}
+
+template <int D, bool FP8, int HG>
 struct DecodeCfg {
+  static constexpr int NST = FP8 ? 4 : 3;           // stages
   static constexpr int ES = FP8 ? 1 : 2;
-  static constexpr int RAW_ROW = D * ES;            // bytes of one key row in the cache
-  static constexpr int RAW_UNIT = UNIT * RAW_ROW;   // bytes of one K (or V) unit
+  static constexpr int RAW_ROW = D * ES;            // bytes of one key row of one head
+  static constexpr int RAW_UNIT = UNIT * RAW_ROW;   // bytes of one head's K (or V) unit
+  static constexpr int KV_UNIT = HG * RAW_UNIT;     // K (or V) of the whole head group
   static constexpr int H_ROW = D * 2;               // 16-bit row in shared memory
   static constexpr int H_UNIT = UNIT * H_ROW;
-  static constexpr int STAGE = 2 * RAW_UNIT;        // K + V raw unit
-  // per warp: stages + (fp8 only) one widened K/V unit pair
-  static constexpr int WARP_BYTES = DEC_STAGES * STAGE + (FP8 ? 2 * H_UNIT : 0);
-  static constexpr int SMEM = DEC_WARPS * WARP_BYTES;
-  static constexpr int MERGE_BYTES = DEC_WARPS * (16 * D + 32) * 4;
-  static constexpr int SMEM_TOTAL = SMEM > MERGE_BYTES ? SMEM : MERGE_BYTES;
+  static constexpr int STAGE = 2 * KV_UNIT;         // K + V of the head group
+  static constexpr int WIDE_OFF = NST * STAGE;      // (e4m3) one widened V unit per warp
+  static constexpr int BAR_OFF = WIDE_OFF + (FP8 ? HG * H_UNIT : 0);
+  static constexpr int SMEM = BAR_OFF + 2 * NST * 8 + 1024;
+  static constexpr int THREADS = (HG + 1) * 32;
 };
 
-// Byte offset of 16-byte chunk c of row j in a swizzled 16-bit unit.
+// Byte offset of 16-byte chunk c of row j in a swizzled 16-bit unit (the
+// widened e4m3 buffers).
 template <int D>
 __device__ __forceinline__ int swz(int j, int c) {
   return j * (D * 2) + ((c ^ (j & 7)) << 4);
 }
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(DEC_WARPS * 32)
-    decode_split_kernel(const Problem p, float sl2, float out_scale) {
-  using C = DecodeCfg<D, FP8>;
-  extern __shared__ __align__(1024) unsigned char smem[];
+// Two e4m3 codes, placed as the high bytes of the two 16-bit halves of x
+// (x = b1 << 24 | b0 << 8), to two f16 values equal to the codes' values times
+// 2^-8, exactly: with the sign moved from bit 14 to bit 15, the e4m3 fields
+// s.eeee.mmm shifted right by one become the f16 fields s.0eeee.mmm0000000, an
+// f16 whose exponent bias (15) exceeds e4m3's (7) by 8; e4m3 subnormals land on
+// f16 subnormals the same way.  The two NaN codes (S.1111.111) become +-480 *
+// 2^-8 instead of NaN.  The 2^8 is folded into the per-tensor scales.
+__device__ __forceinline__ unsigned e4m3x2_to_f16x2_scaled(unsigned x) {
+  const unsigned y = x >> 1;                          // s.eeee.mmm at bits 14..7 (+16)
+  return (y & 0x3F803F80u) | (x & 0x80008000u);       // drop the shifted sign, keep the real one
+}
+
+// Byte offset of 16-byte chunk c of row j of head hh in a K (or V) unit as
+// TMA lays it down.  16-bit data: [d half][head][row][128 bytes], 128-byte
+// swizzle (chunk index XOR line % 8, and line % 8 == row % 8 because each
+// head block holds 16 rows).  e4m3 rows of 128 bytes: [head][row][128 B],
+// same swizzle; 64-byte e4m3 rows: [head][row][64 B], no swizzle.
+template <int D, bool FP8, int HG>
+__device__ __forceinline__ int raw_off(int hh, int j, int c) {
+  if constexpr (FP8 && D == 64) {
+    return (hh * UNIT + j) * 64 + (c << 4);
+  } else if constexpr (FP8) {
+    return (hh * UNIT + j) * 128 + ((c ^ (j & 7)) << 4);
+  } else {
+    return (((c >> 3) * HG + hh) * UNIT + j) * 128 + (((c & 7) ^ (j & 7)) << 4);
+  }
+}
+
+template <int D, bool FP8, int NT, int HG>
+__global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
+    decode_split_kernel(const Problem p, const __grid_constant__ CUtensorMap kvmap, float sl2,
+                        float out_scale) {
+  using C = DecodeCfg<D, FP8, HG>;
+  constexpr int NST = C::NST;
+  extern __shared__ unsigned char smem_raw[];
+  // TMA's 128-byte swizzle is laid out from 1024-byte aligned boxes
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.splits;
+  const int n_groups = p.Hkv / HG;
   const int item = blockIdx.x;
   const int sp = item % S;
-  const int g = (item / S) % p.Hkv;
-  const int r = item / (S * p.Hkv);
+  const int grp = (item / S) % n_groups;
+  const int r = item / (S * n_groups);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
+  const int g = grp * HG + warp;              // this consumer warp's KV head
+  const int quad = lane >> 2, c4 = lane & 3;  // fragment row / column group
 
   const int t0 = p.qsl[r];
   const int q_len = p.qsl[r + 1] - t0;
@@ -84,264 +133,319 @@ __global__ void __launch_bounds__(DEC_WARPS * 32)
   const int kb = max(k_lo, (b_lo + sp * per) * p.bs);
   const int ke = min(s, (b_lo + (sp + 1) * per) * p.bs);
 
-  const int* bt = p.block_table + static_cast<int64_t>(r) * p.mbps;
-  const unsigned char* kvb = static_cast<const unsigned char*>(p.kv);
-  const int64_t row_stride = static_cast<int64_t>(p.Hkv) * C::RAW_ROW;          // bytes per slot
-  const int64_t v_plane = static_cast<int64_t>(p.NB) * p.bs * row_stride;        // K -> V
-
-  // ---------------------------------------------------------------- Q in registers
-  // A fragments of m16n8k16: rows = heads of this KV group (zero past G).
-  unsigned qa[D / 16][4];
-  {
-    const int rA = lane >> 2, c2 = (lane & 3) * 2;
-    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                (static_cast<int64_t>(t0) * p.H + g * G) * D;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = rA + ((e & 1) ? 8 : 0);
-        const int col = kk * 16 + c2 + ((e & 2) ? 8 : 0);
-        unsigned v = 0;
-        if (row < G) {
-          __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(qrow + row * D + col);
-          if constexpr (FP8) {
-            float2 f = __bfloat1622float2(x);
-            v = pack2<true>(f.x, f.y);
-          } else {
-            v = *reinterpret_cast<unsigned*>(&x);
-          }
-        }
-        qa[kk][e] = v;
-      }
-    }
-  }
-
-  // ---------------------------------------------------------------- stream units
+  // Units (16 keys of all HG heads) of this item.
   const int u_begin = kb / UNIT;
   const int u_end = (ke + UNIT - 1) / UNIT;
   const int n_units = (ke > kb) ? (u_end - u_begin) : 0;
-  const int my_units = (n_units > warp) ? (n_units - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
 
-  unsigned char* wbase = smem + warp * C::WARP_BYTES;
-  auto stage_ptr = [&](int st) { return wbase + st * C::STAGE; };
-
-  // Issue the loads of this warp's i-th unit into stage st.  Rows whose key
-  // is at or past seq_len are written as zeros instead (their slots may hold
-  // anything, NaN included).
-  auto issue = [&](int i, int st) {
-    const int u = u_begin + warp + i * DEC_WARPS;
-    const int key0 = u * UNIT;
-    int blk = bt[key0 / p.bs];
-    if (blk < 0 || blk >= p.NB) {
-      flag_status(status, PATTN_DEV_BAD_METADATA);
-      blk = min(max(blk, 0), p.NB - 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // [NST]
+  uint64_t* empty = full + NST;                                       // [NST]
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NST; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], HG);
     }
-    const unsigned char* ksrc =
-        kvb + (static_cast<int64_t>(blk) * p.bs + (key0 % p.bs)) * row_stride +
-        static_cast<int64_t>(g) * C::RAW_ROW;
-    unsigned char* dk = stage_ptr(st);
-    unsigned char* dv = dk + C::RAW_UNIT;
-    constexpr int CH_ROW = C::RAW_ROW / 16;   // 16-byte chunks per row
-    constexpr int CH = UNIT * CH_ROW;          // per K (or V) unit
-#pragma unroll
-    for (int c = lane; c < CH; c += 32) {
-      const int j = c / CH_ROW, cc = c % CH_ROW;
-      // bf16 rows are stored swizzled for ldmatrix; e4m3 rows stay linear
-      // (they are widened into a swizzled buffer before use).
-      const int off = FP8 ? (j * C::RAW_ROW + cc * 16) : swz<D>(j, cc);
-      if (key0 + j < s) {
-        const unsigned char* src = ksrc + j * row_stride + cc * 16;
-        cp_async_16(dk + off, src);
-        cp_async_16(dv + off, src + v_plane);
-      } else {
-        *reinterpret_cast<uint4*>(dk + off) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(dv + off) = make_uint4(0, 0, 0, 0);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == HG) {
+    // ------------------------------------------------------------ producer warp
+    // Block ids are read 32 units at a time (one coalesced load); lane 0
+    // issues one tensor copy for K and one for V per unit (16 keys of all HG
+    // heads) as soon as the consumers release the stage.
+    if (lane == 0) tma_prefetch_desc(&kvmap);
+    const int* bt = p.block_table + static_cast<int64_t>(r) * p.mbps;
+    bool ok = true;
+    for (int base = 0; ok && base < n_units; base += 32) {
+      const int gu = base + lane;
+      int blk = 0;
+      if (gu < n_units) {
+        const int key0 = (u_begin + gu) * UNIT;
+        blk = bt[p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs)];
+        if (blk < 0 || blk >= p.NB) {
+          flag_status(status, PATTN_DEV_BAD_METADATA);
+          blk = min(max(blk, 0), p.NB - 1);
+        }
+      }
+      const int nb = min(32, n_units - base);
+      for (int l = 0; l < nb; ++l) {
+        const int b = __shfl_sync(0xffffffffu, blk, l);
+        int good = 1;
+        if (lane == 0) {
+          const int i = base + l, st = i % NST;
+          if (i >= NST && !mbar_wait(&empty[st], ((i / NST) - 1) & 1, status, nullptr)) {
+            good = 0;
+          } else {
+            const int key0 = (u_begin + i) * UNIT;
+            const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
+            unsigned char* dk = smem + st * C::STAGE;
+            mbar_arrive_expect_tx(&full[st], C::STAGE);
+            if constexpr (FP8) {
+              tma_load_4d(dk, &kvmap, &full[st], 0, slot, grp * HG, b);
+              tma_load_4d(dk + C::KV_UNIT, &kvmap, &full[st], 0, slot, grp * HG, p.NB + b);
+            } else {
+              tma_load_5d(dk, &kvmap, &full[st], 0, slot, grp * HG, 0, b);
+              tma_load_5d(dk + C::KV_UNIT, &kvmap, &full[st], 0, slot, grp * HG, 0, p.NB + b);
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
       }
     }
-  };
-
-#pragma unroll
-  for (int i = 0; i < DEC_STAGES - 1; ++i) {
-    if (i < my_units) issue(i, i);
-    cp_async_commit();
+    return;  // nothing after this needs the producer
   }
 
-  float o[D / 8][4];
+  // ---------------------------------------------------------------- consumer warps
+  // Q^T in registers.  S^T = K Q^T: the B operand (16 d x 8 heads, "col") of
+  // k-step kk and head tile nt is Q[head][d] at head = nt*8 + quad.  For
+  // 16-bit K, d = 16kk + 2*c4 (+1, +8, +9).  For e4m3 K the d axis is permuted
+  // (the same permutation on Q and K leaves every dot product unchanged) so
+  // each lane reads its K bytes contiguously: k-step kk, fragment columns
+  // 2*c4 + j and 2*c4 + 8 + j map to d = c4*D/4 + 4kk + j and + 2 + j.
+  unsigned qb[D / 16][NT][2];
+  {
+    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                (static_cast<int64_t>(t0) * p.H + g * G) * D;
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int head = nt * 8 + quad;
+          unsigned v = 0;
+          if (head < G) {
+            const int d = FP8 ? (c4 * (D / 4) + 4 * kk + 2 * e) : (kk * 16 + 2 * c4 + e * 8);
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(qrow + head * D + d);
+            if constexpr (FP8) {
+              const float2 f = __bfloat1622float2(x);
+              v = pack2<true>(f.x, f.y);
+            } else {
+              v = *reinterpret_cast<const unsigned*>(&x);
+            }
+          }
+          qb[kk][nt][e] = v;
+        }
+  }
+  float o[D / 16][NT][4];
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
+  // running max / sum of heads nt*8 + 2*c4 + e (identical across lanes with
+  // the same c4 once reduced)
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+  }
+
   const int kmin = kb, kmax = ke;
+  // ldmatrix lane addressing (matrix index = lane >> 3)
+  const int mi = lane >> 3;
+  const int s_row = (lane & 7) + ((mi & 1) << 3), s_csel = mi >> 1;    // K, non-transposed
+  const int v_row = (lane & 7) + ((mi >> 1) << 3), v_csel = mi & 1;    // V, transposed
+  // P^T gather: source lanes and half selector for this lane's B fragment
+  const int src0 = 8 * c4 + (quad >> 1), src1 = src0 + 4;
+  const unsigned half_sel = (quad & 1) ? 0x7632u : 0x5410u;
 
-  for (int i = 0; i < my_units; ++i) {
-    if (i + DEC_STAGES - 1 < my_units) issue(i + DEC_STAGES - 1, (i + DEC_STAGES - 1) % DEC_STAGES);
-    cp_async_commit();
-    cp_async_wait<DEC_STAGES - 1>();
-    __syncwarp();
+  for (int i = 0; i < n_units; ++i) {
+    const int st = i % NST;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (i / NST) & 1, status, nullptr))) break;
+    unsigned char* sk = smem + st * C::STAGE;
+    unsigned char* sv = sk + C::KV_UNIT;
+    const int key0 = (u_begin + i) * UNIT;
+    // Rows at or past seq_len may hold anything (NaN included): zero this
+    // head's rows.
+    if (key0 + UNIT > s) {
+      constexpr int CH_ROW = C::RAW_ROW / 16;
+      for (int c = lane; c < UNIT * CH_ROW; c += 32) {
+        const int j = c / CH_ROW, cc = c % CH_ROW;
+        if (key0 + j >= s) {
+          *reinterpret_cast<uint4*>(sk + raw_off<D, FP8, HG>(warp, j, cc)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sv + raw_off<D, FP8, HG>(warp, j, cc)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // the stage is refilled by TMA (async proxy) after this warp releases it
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
 
-    unsigned char* sk = stage_ptr(i % DEC_STAGES);
-    unsigned char* sv = sk + C::RAW_UNIT;
+    // S^T = K Q^T for the 16 keys of this unit: M = keys, N = heads, in two
+    // independent accumulation chains (even / odd k-steps).
+    float sc[2][NT][4];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sc[ch][nt][0] = sc[ch][nt][1] = sc[ch][nt][2] = sc[ch][nt][3] = 0.f;
+    unsigned sv_a;
     if constexpr (FP8) {
-      // widen e4m3 -> f16 into the swizzled 16-bit buffers
-      unsigned char* hk = wbase + DEC_STAGES * C::STAGE;
-      unsigned char* hv = hk + C::H_UNIT;
+      // K fragments straight from the e4m3 bytes: this lane's D/4 bytes of
+      // key rows quad and quad + 8, widened in registers.
+      constexpr int CPL = D / 64;  // 16-byte chunks per lane per row
+      uint4 kr[2][CPL];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int q = 0; q < CPL; ++q)
+          kr[hr][q] = *reinterpret_cast<const uint4*>(sk + raw_off<D, FP8, HG>(warp, quad + 8 * hr, c4 * CPL + q));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint4& ra = kr[0][kk >> 2];
+        const uint4& rb = kr[1][kk >> 2];
+        const unsigned w0 = (kk & 3) == 0 ? ra.x : (kk & 3) == 1 ? ra.y : (kk & 3) == 2 ? ra.z : ra.w;
+        const unsigned w1 = (kk & 3) == 0 ? rb.x : (kk & 3) == 1 ? rb.y : (kk & 3) == 2 ? rb.z : rb.w;
+        const unsigned a0 = e4m3x2_to_f16x2_scaled(__byte_perm(w0, 0u, 0x1404u));
+        const unsigned a2 = e4m3x2_to_f16x2_scaled(__byte_perm(w0, 0u, 0x3424u));
+        const unsigned a1 = e4m3x2_to_f16x2_scaled(__byte_perm(w1, 0u, 0x1404u));
+        const unsigned a3 = e4m3x2_to_f16x2_scaled(__byte_perm(w1, 0u, 0x3424u));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816<true>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+      }
+      // widen this head's V (e4m3 -> f16, times 2^-8) into its 16-bit buffer
+      unsigned char* hv = smem + C::WIDE_OFF + warp * C::H_UNIT;
       constexpr int CH_ROW = C::RAW_ROW / 16;
 #pragma unroll
       for (int c = lane; c < UNIT * CH_ROW; c += 32) {
         const int j = c / CH_ROW, cc = c % CH_ROW;
+        const uint4 raw = *reinterpret_cast<const uint4*>(sv + raw_off<D, FP8, HG>(warp, j, cc));
+        const unsigned w[4] = {raw.x, raw.y, raw.z, raw.w};
+        unsigned h[8];
 #pragma unroll
-        for (int kvi = 0; kvi < 2; ++kvi) {
-          const uint4 raw = *reinterpret_cast<const uint4*>((kvi ? sv : sk) + j * C::RAW_ROW + cc * 16);
-          const unsigned w[4] = {raw.x, raw.y, raw.z, raw.w};
-          unsigned h[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(w[q] & 0xFFFF), __NV_E4M3);
-            __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(w[q] >> 16), __NV_E4M3);
-            h[2 * q] = *reinterpret_cast<unsigned*>(&lo);
-            h[2 * q + 1] = *reinterpret_cast<unsigned*>(&hi);
-          }
-          unsigned char* dst = kvi ? hv : hk;
-          *reinterpret_cast<uint4*>(dst + swz<D>(j, 2 * cc)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(dst + swz<D>(j, 2 * cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        for (int q = 0; q < 4; ++q) {
+          h[2 * q] = e4m3x2_to_f16x2_scaled(__byte_perm(w[q], 0u, 0x1404u));
+          h[2 * q + 1] = e4m3x2_to_f16x2_scaled(__byte_perm(w[q], 0u, 0x3424u));
         }
+        *reinterpret_cast<uint4*>(hv + swz<D>(j, 2 * cc)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(hv + swz<D>(j, 2 * cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
       __syncwarp();
-      sk = hk;
-      sv = hv;
-    }
-
-    // S = Q K^T for the 16 keys of this unit (two n8 tiles).
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const unsigned sk_a = smem_u32(sk), sv_a = smem_u32(sv);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int row = (lane & 7) + ((lane >> 4) << 3);
-      const int chunk = 2 * kk + ((lane >> 3) & 1);
-      unsigned b00, b01, b10, b11;
-      ldsm_x4(sk_a + swz<D>(row, chunk), b00, b01, b10, b11);
-      mma_16816<FP8>(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b00, b01);
-      mma_16816<FP8>(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b10, b11);
-    }
-
-    // Mask, scale to log2 units, online softmax.
-    const int u = u_begin + warp + i * DEC_WARPS;
-    const int kbase = u * UNIT + (lane & 3) * 2;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k = kbase + n * 8 + (e & 1);
-        const float x = (k >= kmin && k < kmax) ? sc[n][e] * sl2 : -INFINITY;
-        sc[n][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    float alpha[2];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-      const float m_new = fmaxf(m_run[hr], mx[hr]);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      alpha[hr] = fast_exp2(m_run[hr] - m_use);
-      m_run[hr] = m_new;
-      mx[hr] = m_use;
-    }
-    float ps[2] = {0.f, 0.f};
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pv = fast_exp2(sc[n][e] - mx[e >> 1]);
-        sc[n][e] = pv;
-        ps[e >> 1] += pv;
-      }
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) l_run[hr] = l_run[hr] * alpha[hr] + ps[hr];
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= alpha[0];
-      o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1];
-      o[n][3] *= alpha[1];
-    }
-    const unsigned pa0 = pack2<FP8>(sc[0][0], sc[0][1]);
-    const unsigned pa1 = pack2<FP8>(sc[0][2], sc[0][3]);
-    const unsigned pa2 = pack2<FP8>(sc[1][0], sc[1][1]);
-    const unsigned pa3 = pack2<FP8>(sc[1][2], sc[1][3]);
-
-    // O += P V: V rows are keys; ldmatrix.trans yields the col-major B fragments.
-#pragma unroll
-    for (int nd = 0; nd < D / 16; ++nd) {
-      const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
-      const int chunk = 2 * nd + (lane >> 4);
-      unsigned v0, v1, v2, v3;
-      ldsm_x4_t(sv_a + swz<D>(row, chunk), v0, v1, v2, v3);
-      mma_16816<FP8>(o[2 * nd], pa0, pa1, pa2, pa3, v0, v1);
-      mma_16816<FP8>(o[2 * nd + 1], pa0, pa1, pa2, pa3, v2, v3);
-    }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-
-  // Row sums were per lane: finish them across the quad.
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
-    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
-  }
-
-  // ---------------------------------------------------------------- merge warps
-  __syncthreads();
-  float* mo = reinterpret_cast<float*>(smem);                // [WARPS][16][D]
-  float* mm = mo + DEC_WARPS * 16 * D;                       // [WARPS][16]
-  float* ml = mm + DEC_WARPS * 16;                           // [WARPS][16]
-  {
-    const int rA = lane >> 2, c2 = (lane & 3) * 2;
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = rA + ((e & 2) ? 8 : 0);
-        mo[(warp * 16 + row) * D + n * 8 + c2 + (e & 1)] = o[n][e];
-      }
-    if ((lane & 3) == 0) {
-      mm[warp * 16 + rA] = m_run[0];
-      mm[warp * 16 + rA + 8] = m_run[1];
-      ml[warp * 16 + rA] = l_run[0];
-      ml[warp * 16 + rA + 8] = l_run[1];
-    }
-  }
-  __syncthreads();
-
-  const int h0 = g * G;
-  for (int idx = threadIdx.x; idx < G * D; idx += DEC_WARPS * 32) {
-    const int row = idx / D, col = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, mm[w * 16 + row]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) {
-      const float wt = fast_exp2(mm[w * 16 + row] - Mu);
-      L += wt * ml[w * 16 + row];
-      acc += wt * mo[(w * 16 + row) * D + col];
-    }
-    const float val = (L > 0.f) ? acc / L * out_scale : 0.f;
-    if (S == 1) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-      out[(static_cast<int64_t>(t0) * p.H + h0 + row) * D + col] = __float2bfloat16_rn(val);
+      sv_a = smem_u32(hv);
     } else {
-      const int64_t prow = (static_cast<int64_t>(r) * p.H + h0 + row) * S + sp;
-      p.o_part[prow * D + col] = val;
-      if (col == 0) p.lse_part[prow] = (L > 0.f) ? M + __log2f(L) : -INFINITY;
+      const unsigned sk_a = smem_u32(sk);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        unsigned a0, a1, a2, a3;
+        ldsm_x4(sk_a + raw_off<D, FP8, HG>(warp, s_row, 2 * kk + s_csel), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816<false>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+      }
+      sv_a = smem_u32(sv);
     }
+
+    // Mask (keys quad and quad + 8 of this unit), scale to log2 units, online
+    // softmax per head (a column of S^T: reduce over the 8 lanes of a column group).
+    const int ka = key0 + quad, kb2 = ka + 8;
+    const bool va = ka >= kmin && ka < kmax, vb = kb2 >= kmin && kb2 < kmax;
+    unsigned pk_lo[NT], pk_hi[NT];
+    float alpha[NT][2];
+    bool moved = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v = sc[0][nt][e] + sc[1][nt][e];
+        x[e] = ((e < 2) ? va : vb) ? v * sl2 : -INFINITY;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float mx = fmaxf(x[hh], x[2 + hh]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m_run[nt][hh], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[nt][hh] = fast_exp2(m_run[nt][hh] - m_use);
+        moved |= (alpha[nt][hh] != 1.f);
+        m_run[nt][hh] = m_new;
+        const float pa = fast_exp2(x[hh] - m_use), pb = fast_exp2(x[2 + hh] - m_use);
+        x[hh] = pa;
+        x[2 + hh] = pb;
+        float ps = pa + pb;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l_run[nt][hh] = l_run[nt][hh] * alpha[nt][hh] + ps;
+      }
+      pk_lo[nt] = pack2<FP8>(x[0], x[1]);  // key quad,     heads 2*c4, 2*c4+1
+      pk_hi[nt] = pack2<FP8>(x[2], x[3]);  // key quad + 8, heads 2*c4, 2*c4+1
+    }
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[m][nt][0] *= alpha[nt][0];
+          o[m][nt][1] *= alpha[nt][1];
+          o[m][nt][2] *= alpha[nt][0];
+          o[m][nt][3] *= alpha[nt][1];
+        }
+    }
+    // P^T as the B operand (16 keys x 8 heads, "col"): this lane needs head
+    // nt*8 + quad at keys 2*c4, 2*c4+1 (b0) and 2*c4+8, 2*c4+9 (b1); they sit
+    // in lanes src0 (even key) and src1 (odd key), half quad & 1.
+    unsigned pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const unsigned x0 = __shfl_sync(0xffffffffu, pk_lo[nt], src0);
+      const unsigned x1 = __shfl_sync(0xffffffffu, pk_lo[nt], src1);
+      const unsigned y0 = __shfl_sync(0xffffffffu, pk_hi[nt], src0);
+      const unsigned y1 = __shfl_sync(0xffffffffu, pk_hi[nt], src1);
+      pb0[nt] = __byte_perm(x0, x1, half_sel);
+      pb1[nt] = __byte_perm(y0, y1, half_sel);
+    }
+
+    // O^T += V^T P^T: M = d (16 per tile), N = heads, K = the 16 keys.
+#pragma unroll
+    for (int m = 0; m < D / 16; ++m) {
+      unsigned a0, a1, a2, a3;
+      ldsm_x4_t(sv_a + (FP8 ? swz<D>(v_row, 2 * m + v_csel)
+                            : raw_off<D, FP8, HG>(warp, v_row, 2 * m + v_csel)),
+                a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816<FP8>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+    }
+    // Release the stage once every lane of every consumer warp has read it.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
   }
+
+  // ---------------------------------------------------------------- outputs
+  // Each consumer warp owns its KV head's G query heads: normalise and write
+  // them (bf16 output) or the partition's (o_p, lse_p) for the combine step.
+  const int h0 = g * G;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int head = nt * 8 + 2 * c4 + (e & 1);
+      if (head >= G) continue;
+      const float L = l_run[nt][e & 1];
+      const float M = m_run[nt][e & 1];
+      const float inv = (L > 0.f) ? out_scale / L : 0.f;
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m) {
+        const int d = 16 * m + quad + ((e & 2) ? 8 : 0);
+        const float val = o[m][nt][e] * inv;
+        if (S == 1) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+          out[(static_cast<int64_t>(t0) * p.H + h0 + head) * D + d] = __float2bfloat16_rn(val);
+        } else {
+          const int64_t prow = (static_cast<int64_t>(r) * p.H + h0 + head) * S + sp;
+          p.o_part[prow * D + d] = val;
+          if (m == 0 && quad == 0 && (e & 2) == 0)
+            p.lse_part[prow] = (L > 0.f) ? M + __log2f(L) : -INFINITY;
+        }
+      }
+    }
 }
 
 // One warp per (request, head): merge the partitions of a decode row.
@@ -381,27 +485,39 @@ __global__ void __launch_bounds__(128) combine_kernel(const Problem p) {
   }
 }
 
-template <int D, bool FP8>
-cudaError_t launch_decode_t(const Problem& p) {
-  using C = DecodeCfg<D, FP8>;
-  auto kern = decode_split_kernel<D, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_TOTAL);
+template <int D, bool FP8, int HG>
+cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
+  using C = DecodeCfg<D, FP8, HG>;
+  auto kern = (p.G <= 8) ? decode_split_kernel<D, FP8, 1, HG> : decode_split_kernel<D, FP8, 2, HG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const float sl2 = p.scale * LOG2E * (FP8 ? p.k_scale : 1.f);
-  const float out_scale = FP8 ? p.v_scale : 1.f;
-  const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
+  // e4m3 data is widened to f16 as value * 2^-8; the 2^8 goes into the scales.
+  const float sl2 = p.scale * LOG2E * (FP8 ? p.k_scale * 256.f : 1.f);
+  const float out_scale = FP8 ? p.v_scale * 256.f : 1.f;
+  const long long items = static_cast<long long>(p.B) * (p.Hkv / HG) * p.splits;
   if (items == 0) return cudaSuccess;
-  kern<<<static_cast<unsigned>(items), DEC_WARPS * 32, C::SMEM_TOTAL, p.stream>>>(p, sl2, out_scale);
+  kern<<<static_cast<unsigned>(items), C::THREADS, C::SMEM, p.stream>>>(p, kvmap, sl2, out_scale);
   return cudaGetLastError();
+}
+
+template <int D, bool FP8>
+cudaError_t launch_decode_hg(const Problem& p, const CUtensorMap& kvmap) {
+  switch (decode_head_group(p.Hkv)) {
+    case 4: return launch_decode_t<D, FP8, 4>(p, kvmap);
+    case 2: return launch_decode_t<D, FP8, 2>(p, kvmap);
+    default: return launch_decode_t<D, FP8, 1>(p, kvmap);
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const Problem& p) {
-  if (p.D == 128) return p.kv_dtype ? launch_decode_t<128, true>(p) : launch_decode_t<128, false>(p);
-  return p.kv_dtype ? launch_decode_t<64, true>(p) : launch_decode_t<64, false>(p);
+cudaError_t launch_decode(const Problem& p, const CUtensorMap& kvmap) {
+  if (p.D == 128)
+    return p.kv_dtype ? launch_decode_hg<128, true>(p, kvmap) : launch_decode_hg<128, false>(p, kvmap);
+  return p.kv_dtype ? launch_decode_hg<64, true>(p, kvmap) : launch_decode_hg<64, false>(p, kvmap);
 }
+
+int decode_heads_per_cta(int Hkv) { return decode_head_group(Hkv); }
 
 cudaError_t launch_combine(const Problem& p) {
   const long long rows = static_cast<long long>(p.B) * p.H;

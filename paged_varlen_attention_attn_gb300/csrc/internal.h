@@ -28,6 +28,7 @@ struct Problem {
   void* out;
   float scale;
   int H, Hkv, G, D, bs, window, causal, kv_dtype;
+  int bs_shift;  // log2(bs) when bs is a power of two, else -1
   float k_scale, v_scale;
   int B, T, mbps, NB, max_q, max_s, splits;
   // workspace views
@@ -49,9 +50,24 @@ WsLayout workspace_layout(int B, int T, int H, int D, int max_q, int splits);
 
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const Problem& p);
-cudaError_t launch_decode(const Problem& p);
+cudaError_t launch_decode(const Problem& p, const CUtensorMap& kv_map);
 cudaError_t launch_combine(const Problem& p);
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
+// TMA tensor map over the KV cache [2 * NB][bs][Hkv][D] with boxes of
+// box_rows rows of one head: 64 16-bit elements (128-byte swizzle) per box, or
+// a whole e4m3 row (128-byte swizzle at D = 128, none at D = 64).  Returns
+// false if the driver entry point is missing or rejects the map.
+bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv, int bs,
+                   int NB, int box_rows);
+
+// TMA tensor map for the decode kernel: one box is 16 rows of a group of
+// `heads` KV heads (both d halves for 16-bit data), laid out in shared memory
+// as [d half][head][row][128 bytes] (16-bit) or [head][row][row bytes] (e4m3).
+bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv,
+                       int bs, int NB, int heads);
+// KV heads one decode CTA serves (4, 2 or 1: the largest dividing Hkv).
+int decode_heads_per_cta(int Hkv);
+
 // Query rows one prefill CTA covers: two heads x 128 rows when the GQA group
 // size is even, else one head x 256 rows.
 int prefill_rows_per_item(int G);

@@ -56,17 +56,18 @@ bool ext_ok(const pattn_ext_t* ext) {
 }
 
 // Decode partition count.  A forced count is used as given; otherwise enough
-// partitions that the decode grid covers the SMs at least twice, and that no
-// partition is longer than ~1024 keys, bounded by the block count a row can
-// see and by PATTN_MAX_SPLITS.
+// partitions that the decode grid (requests x KV-head groups x partitions)
+// covers the SMs about four times, and that no partition is longer than ~1024
+// keys, bounded by the block count a row can see and by PATTN_MAX_SPLITS.
 int choose_splits(const pattn_ext_t* ext, int num_kv_heads, int block_size, int window) {
   if (ext->num_splits > 0) return ext->num_splits;
   const int visible = (window > 0) ? std::min(ext->max_seq_len, window + block_size)
                                    : ext->max_seq_len;
   const int max_blocks = std::max(1, (visible + block_size - 1) / block_size);
-  const long long items = static_cast<long long>(std::max(1, ext->num_seqs)) * num_kv_heads;
+  const long long items = static_cast<long long>(std::max(1, ext->num_seqs)) *
+                          (num_kv_heads / decode_heads_per_cta(num_kv_heads));
   const int sms = sm_count();
-  int by_grid = static_cast<int>((2LL * sms + items - 1) / items);
+  int by_grid = static_cast<int>((4LL * sms + items - 1) / items);
   int by_len = (visible + 1023) / 1024;
   int s = std::max(1, std::max(by_grid, by_len));
   s = std::min(s, max_blocks);
@@ -90,6 +91,53 @@ pattn_status_t validate(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
 }
 
 }  // namespace
+
+bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv, int bs,
+                   int NB, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const bool fp8 = kv_dtype == PATTN_KV_FP8_E4M3;
+  const cuuint64_t es = fp8 ? 1 : 2;
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * es;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(bs), 2ull * static_cast<cuuint64_t>(NB)};
+  cuuint64_t strides[3] = {row, row * Hkv, row * Hkv * bs};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(fp8 ? D : 64), 1,
+                       static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw =
+      (fp8 && D == 64) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  return enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+             const_cast<void*>(kv_cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv,
+                       int bs, int NB, int heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (kv_dtype == PATTN_KV_FP8_E4M3) {
+    const cuuint64_t row = static_cast<cuuint64_t>(D);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(bs),
+                          static_cast<cuuint64_t>(Hkv), 2ull * static_cast<cuuint64_t>(NB)};
+    cuuint64_t strides[3] = {row * Hkv, row, row * Hkv * bs};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 16, static_cast<cuuint32_t>(heads), 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv_cache), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               D == 64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+  cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(D / 64), 2ull * static_cast<cuuint64_t>(NB)};
+  cuuint64_t strides[4] = {row * Hkv, row, 128, row * Hkv * bs};
+  cuuint32_t box[5] = {64, 16, static_cast<cuuint32_t>(heads), static_cast<cuuint32_t>(D / 64), 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv_cache), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 WsLayout workspace_layout(int B, int T, int H, int D, int max_q, int splits) {
   WsLayout L;
@@ -211,6 +259,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.G = num_heads / num_kv_heads;
   p.D = head_size;
   p.bs = block_size;
+  p.bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(block_size)) : -1;
   p.window = window;
   p.causal = causal;
   p.kv_dtype = kv_dtype;
@@ -260,25 +309,18 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PATTN_ERR_CUDA;
     }
-    {
-      const cuuint64_t row = static_cast<cuuint64_t>(head_size) * es;
-      cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_size),
-                            static_cast<cuuint64_t>(num_kv_heads),
-                            static_cast<cuuint64_t>(block_size),
-                            2ull * static_cast<cuuint64_t>(ext->num_blocks)};
-      cuuint64_t strides[3] = {row, row * num_kv_heads, row * num_kv_heads * block_size};
-      cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(std::min(block_size, BLOCK_N)), 1};
-      cuuint32_t estr[4] = {1, 1, 1, 1};
-      if (enc(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), dims,
-              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return PATTN_ERR_CUDA;
-    }
+    if (!encode_kv_map(&kvmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
+                       ext->num_blocks, std::min(block_size, BLOCK_N)))
+      return PATTN_ERR_CUDA;
     if (launch_prefill(p, qmap, kvmap) != cudaSuccess) return PATTN_ERR_CUDA;
   }
   mark(3);
   mark(4);
-  if (launch_decode(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  CUtensorMap dmap;
+  if (!encode_decode_map(&dmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
+                         ext->num_blocks, decode_heads_per_cta(num_kv_heads)))
+    return PATTN_ERR_CUDA;
+  if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
   mark(5);
   mark(6);
   if (splits > 1 && launch_combine(p) != cudaSuccess) return PATTN_ERR_CUDA;

@@ -14,7 +14,7 @@
 //   warps 0-3  softmax + epilogue of sub-tile A, thread i owns row i (TMEM lane i)
 //   warps 4-7  softmax + epilogue of sub-tile B
 //   warp  8    TMA producer: both Q tiles once, then K and V tiles page by
-//              page through block_table into two-stage rings
+//              page through block_table into 3-stage (K) and 2-stage (V) rings
 //   warp  9    MMA issuer (one thread)
 //   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
@@ -57,7 +57,10 @@ constexpr int PF_THREADS = 384;
 constexpr int SOFTMAX_REGS = 216;
 constexpr int OTHER_REGS = 64;
 constexpr int SPLIT_REGS_TOTAL = 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS;
-constexpr int PF_NST = 2;
+// K and V rings: K gets the extra stage because the next scores need it
+// before the next P V needs V.  224 KB of shared memory at head size 128.
+constexpr int PF_KST = 3;
+constexpr int PF_VST = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr unsigned FULL = 0xffffffffu;
 
@@ -68,8 +71,8 @@ struct PrefillCfg {
   static constexpr int TILE = DH * HALF;            // bytes of a Q, K or V tile
   static constexpr int Q_OFF = 0;                   // two Q tiles
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
-  static constexpr int V_OFF = K_OFF + PF_NST * TILE;
-  static constexpr int BAR_OFF = V_OFF + PF_NST * TILE;
+  static constexpr int V_OFF = K_OFF + PF_KST * TILE;
+  static constexpr int BAR_OFF = V_OFF + PF_VST * TILE;
   // + barriers + alignment slack; at least 116 KB so one CTA holds an SM (and
   // its 512 TMEM columns) alone
   static constexpr int SMEM_RAW = BAR_OFF + 512 + 1024;
@@ -81,10 +84,10 @@ struct PrefillCfg {
 
 struct Bars {
   uint64_t q_full[2];
-  uint64_t k_full[PF_NST];
-  uint64_t v_full[PF_NST];
-  uint64_t k_empty[PF_NST];
-  uint64_t v_empty[PF_NST];
+  uint64_t k_full[PF_KST];
+  uint64_t v_full[PF_VST];
+  uint64_t k_empty[PF_KST];
+  uint64_t v_empty[PF_VST];
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
@@ -182,10 +185,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->p_full[i], BLOCK_M);
       mbar_init(&bars->o_final[i], 1);
     }
-    for (int i = 0; i < PF_NST; ++i) {
+    for (int i = 0; i < PF_KST; ++i) {
       mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < PF_VST; ++i) {
+      mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
     mbar_init(&bars->drain, 1);
@@ -251,8 +256,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (j + 1 < n_union) blk_next = page_block(u0 + j + 1);
         int ok = 1;
         if (lane == 0) {
-          const int st = j % PF_NST;
-          const unsigned ph_prev = ((j / PF_NST) - 1) & 1;
           const int key_base = (u0 + j) * BLOCK_N;
           int n_load = 0;
           for (int pg = 0; pg < pages_per_tile; ++pg)
@@ -260,9 +263,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
           // K first: the next scores need it before the next P V needs V.
           for (int kv = 0; kv < 2 && ok; ++kv) {
+            const int nst = kv ? PF_VST : PF_KST;
+            const int st = j % nst;
             uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
             uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-            if (j >= PF_NST && !mbar_wait(empty, ph_prev, status, abort_flag)) {
+            if (j >= nst && !mbar_wait(empty, ((j / nst) - 1) & 1, status, abort_flag)) {
               ok = 0;
               break;
             }
@@ -305,13 +310,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           bool& q_ready = X ? q_ready1 : q_ready0;
           // P V for the previous key tile
           if (j >= 1 && u.active(kt - 1)) {
-            const int stp = (j - 1) % PF_NST;
+            const int stp = (j - 1) % PF_VST;
             if (!mbar_wait(&bars->p_full[X], n_pv & 1, status, abort_flag)) {
               ok = false;
               break;
             }
             if (!v_ready) {
-              if (!mbar_wait(&bars->v_full[stp], ((j - 1) / PF_NST) & 1, status, abort_flag)) {
+              if (!mbar_wait(&bars->v_full[stp], ((j - 1) / PF_VST) & 1, status, abort_flag)) {
                 ok = false;
                 break;
               }
@@ -331,9 +336,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           }
           // scores for this key tile
           if (j < n_union && u.active(kt)) {
-            const int st = j % PF_NST;
+            const int st = j % PF_KST;
             if (!k_ready) {
-              if (!mbar_wait(&bars->k_full[st], (j / PF_NST) & 1, status, abort_flag)) {
+              if (!mbar_wait(&bars->k_full[st], (j / PF_KST) & 1, status, abort_flag)) {
                 ok = false;
                 break;
               }
@@ -458,12 +463,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           a1 = fast_exp2(a1);
           a2 = fast_exp2(a2);
           a3 = fast_exp2(a3);
-          if (edge) {
-            a0 = (sv[q + e] == -INFINITY) ? 0.f : a0;
-            a1 = (sv[q + e + 1] == -INFINITY) ? 0.f : a1;
-            a2 = (sv[q + e + 2] == -INFINITY) ? 0.f : a2;
-            a3 = (sv[q + e + 3] == -INFINITY) ? 0.f : a3;
-          }
           fadd2(ps0, ps1, a0, a1);
           fadd2(ps2, ps3, a2, a3);
           pk[e / 2] = pack2<false>(a0, a1);
@@ -478,8 +477,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       // first sub-tile whose P V reads this tile).
       if (key0 + BLOCK_N > s && (X == 0 || !subA.active(kt))) {
         const int j = kt - u0;
-        const int st = j % PF_NST;
-        if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], (j / PF_NST) & 1, status, abort_flag))) {
+        const int st = j % PF_VST;
+        if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], (j / PF_VST) & 1, status, abort_flag))) {
           ok = false;
           break;
         }
@@ -548,7 +547,12 @@ cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const C
     return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
-  k<<<grid, PF_THREADS, PrefillCfg<D>::SMEM, p.stream>>>(p, q_map, kv_map, p.scale * LOG2E);
+  // Scores are scaled to log2 units by sl2 = scale * log2(e).  It is kept
+  // strictly positive so a masked score (-inf) always maps to exp2(-inf) = 0;
+  // at scale == 0 the visible scores become ~1e-30 * q.k, whose exp2 is 1.0f
+  // exactly (uniform weights, as the definition gives).
+  const float sl2 = fmaxf(p.scale * LOG2E, 1e-30f);
+  k<<<grid, PF_THREADS, PrefillCfg<D>::SMEM, p.stream>>>(p, q_map, kv_map, sl2);
   return cudaGetLastError();
 }
 

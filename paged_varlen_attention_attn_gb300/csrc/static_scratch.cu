@@ -120,6 +120,7 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.G = num_heads / num_kv_heads;
   p.D = head_size;
   p.bs = block_size;
+  p.bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(block_size)) : -1;
   p.window = window;
   p.causal = causal;
   p.kv_dtype = kv_dtype;
@@ -143,7 +144,11 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   // The status word must start at zero; the partials need no clearing.
   if (cudaMemsetAsync(&p.hdr->status, 0, sizeof(unsigned), p.stream) != cudaSuccess)
     return PATTN_ERR_CUDA;
-  if (launch_decode(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  CUtensorMap dmap;
+  if (!encode_decode_map(&dmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
+                         num_blocks, decode_heads_per_cta(num_kv_heads)))
+    return PATTN_ERR_CUDA;
+  if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
   if (splits > 1 && launch_combine(p) != cudaSuccess) return PATTN_ERR_CUDA;
   return PATTN_OK;
 }
