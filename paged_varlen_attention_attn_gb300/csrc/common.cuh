@@ -127,6 +127,12 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Named barrier over `count` threads (a multiple of 32) of the CTA; id 0 is
+// the one __syncthreads uses.
+__device__ __forceinline__ void named_bar_sync(unsigned id, unsigned count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -18,62 +18,81 @@
 // 128-byte swizzle so ldmatrix reads are conflict-free).  One unit never
 // straddles a KV block because block_size % 16 == 0.  Few, large copies keep
 // many bytes in flight per SM with little issue work, which is what a
-// bandwidth-bound stream needs.  One consumer warp per KV head computes
-// S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 with the keys (and d)
-// as the M rows and the G heads as N, so no MMA rows are wasted at small G;
-// the tensor work is far below what HBM allows either way.  e4m3 K fragments
-// are widened to f16 in registers and V in shared memory with integer bit
-// operations (exact: every e4m3 value times 2^-8 is an f16 value); the
-// per-tensor scales (times 2^8) are folded into the softmax scale (K) and the
-// final normalisation (V).
+// bandwidth-bound stream needs.  Consumer warps compute S^T = K Q^T and
+// O^T += V^T P^T on mma.sync m16n8k16 with the keys (and d) as the M rows and
+// the G heads as N, so no MMA rows are wasted at small G; the tensor work is
+// far below what HBM allows either way.  At G <= 8 two warps serve each KV
+// head, taking the partition's units in turn, and merge their (o, m, l) at the
+// end, which doubles the warps that hide load latency.  e4m3 K and V
+// fragments are widened to f16 in registers with integer operations (exact:
+// every e4m3 value times 2^-8 is an f16 value); the per-tensor scales (times
+// 2^8) are folded into the softmax scale (K) and the final normalisation (V).
 #include "common.cuh"
 #include "internal.h"
 
 namespace pattn {
 namespace {
 
-// A CTA serves one (request, group of HG KV heads, partition) item: HG
-// consumer warps, one per KV head, plus one producer warp.
+// A CTA serves one (request, group of HG KV heads, partition) item: WPH
+// consumer warps per KV head, which take the partition's 16-key units in turn
+// and merge their partial results at the end, plus one producer warp.
 constexpr int UNIT = 16;  // keys per unit
 
-// KV heads per CTA: 4, or the largest of 2 / 1 dividing num_kv_heads.
-__host__ __device__ constexpr int decode_head_group(int Hkv) {
-  return (Hkv % 4 == 0) ? 4 : (Hkv % 2 == 0) ? 2 : 1;
+// KV heads per CTA: the largest of 4 / 2 / 1 that divides num_kv_heads and
+// keeps one stage (K + V of 16 keys of the group) within 16 KB, so the ring
+// holds six or more stages in ~96 KB.
+__host__ __device__ constexpr int decode_head_group(int Hkv, int D, bool fp8) {
+  return (Hkv % 4 == 0 && 4 * 2 * 16 * D * (fp8 ? 1 : 2) <= 16384) ? 4
+         : (Hkv % 2 == 0) ? 2
+                          : 1;
 }
 
-template <int D, bool FP8, int HG>
+template <int D, bool FP8, int NT, int HG, int WPH>
 struct DecodeCfg {
-  static constexpr int NST = FP8 ? 4 : 3;           // stages
   static constexpr int ES = FP8 ? 1 : 2;
   static constexpr int RAW_ROW = D * ES;            // bytes of one key row of one head
   static constexpr int RAW_UNIT = UNIT * RAW_ROW;   // bytes of one head's K (or V) unit
   static constexpr int KV_UNIT = HG * RAW_UNIT;     // K (or V) of the whole head group
-  static constexpr int H_ROW = D * 2;               // 16-bit row in shared memory
-  static constexpr int H_UNIT = UNIT * H_ROW;
   static constexpr int STAGE = 2 * KV_UNIT;         // K + V of the head group
-  static constexpr int WIDE_OFF = NST * STAGE;      // (e4m3) one widened V unit per warp
-  static constexpr int BAR_OFF = WIDE_OFF + (FP8 ? HG * H_UNIT : 0);
+  // Ring depth: as many stages as fit in ~96 KB (two CTAs per SM), at most 8,
+  // rounded down to a multiple of WPH.  Unit i goes to warp slot i % WPH and
+  // stage i % NST; with NST a multiple of WPH every use of a stage belongs to
+  // one slot, so a warp waiting on a stage's full barrier has itself consumed
+  // the stage's previous phase and is never two phases ahead of it (where a
+  // parity wait would pass at once).
+  static constexpr int NST_FIT = (96 * 1024) / STAGE;
+  static constexpr int NST_CAP = NST_FIT > 8 ? 8 : NST_FIT;
+  static constexpr int NST = (NST_CAP / WPH) * WPH < 2 * WPH ? 2 * WPH : (NST_CAP / WPH) * WPH;
+  static_assert(NST % WPH == 0, "each stage must belong to one warp slot");
+  static constexpr int NW = HG * WPH;               // consumer warps
+  // Partial state one warp hands over for the merge: o, m, l per lane.
+  static constexpr int MERGE_FLOATS = (D / 16) * NT * 4 + 4 * NT;
+  static constexpr int MERGE_BYTES = (WPH - 1) * HG * MERGE_FLOATS * 32 * 4;
+  static constexpr int RING_BYTES = NST * STAGE;
+  static constexpr int BAR_OFF = RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES;
   static constexpr int SMEM = BAR_OFF + 2 * NST * 8 + 1024;
-  static constexpr int THREADS = (HG + 1) * 32;
+  static constexpr int THREADS = (NW + 1) * 32;
 };
 
-// Byte offset of 16-byte chunk c of row j in a swizzled 16-bit unit (the
-// widened e4m3 buffers).
-template <int D>
-__device__ __forceinline__ int swz(int j, int c) {
-  return j * (D * 2) + ((c ^ (j & 7)) << 4);
+// e4m3 -> f16 widening, exact: a code s.eeee.mmm shifted left by 7 is the
+// f16 pattern 0.seeee.mmm0000000, and moving the sign from bit 14 to bit 15
+// (t + (t & bit 14): the bit doubles into the next position) gives
+// s.0eeee.mmm0000000, the f16 equal to the code's value times 2^-8 -- f16's
+// exponent bias (15) exceeds e4m3's (7) by 8, and e4m3 subnormals land on f16
+// subnormals the same way.  The two NaN codes (S.1111.111) become +-480 *
+// 2^-8 instead of NaN.  The 2^8 is folded into the per-tensor scales.  The
+// shift and the add are integer multiply-adds, which can run on the FMA pipe;
+// only the two masks need the integer ALU.
+//
+// Codes in bytes 0 and 2 of x (bytes 1 and 3 ignored) -> f16x2 (lo, hi).
+__device__ __forceinline__ unsigned e4m3_b02_to_f16x2(unsigned x) {
+  const unsigned t = (x & 0x00FF00FFu) * 128u;
+  return t + (t & 0x40004000u);
 }
-
-// Two e4m3 codes, placed as the high bytes of the two 16-bit halves of x
-// (x = b1 << 24 | b0 << 8), to two f16 values equal to the codes' values times
-// 2^-8, exactly: with the sign moved from bit 14 to bit 15, the e4m3 fields
-// s.eeee.mmm shifted right by one become the f16 fields s.0eeee.mmm0000000, an
-// f16 whose exponent bias (15) exceeds e4m3's (7) by 8; e4m3 subnormals land on
-// f16 subnormals the same way.  The two NaN codes (S.1111.111) become +-480 *
-// 2^-8 instead of NaN.  The 2^8 is folded into the per-tensor scales.
-__device__ __forceinline__ unsigned e4m3x2_to_f16x2_scaled(unsigned x) {
-  const unsigned y = x >> 1;                          // s.eeee.mmm at bits 14..7 (+16)
-  return (y & 0x3F803F80u) | (x & 0x80008000u);       // drop the shifted sign, keep the real one
+// Codes in bytes 1 and 3 of x (bytes 0 and 2 ignored) -> f16x2 (lo, hi).
+__device__ __forceinline__ unsigned e4m3_b13_to_f16x2(unsigned x) {
+  const unsigned t = __umulhi(x & 0xFF00FF00u, 0x80000000u);  // >> 1
+  return t + (t & 0x40004000u);
 }
 
 // Byte offset of 16-byte chunk c of row j of head hh in a K (or V) unit as
@@ -92,11 +111,25 @@ __device__ __forceinline__ int raw_off(int hh, int j, int c) {
   }
 }
 
-template <int D, bool FP8, int NT, int HG>
-__global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
+// The D / 8 bytes of e4m3 V row j of head hh that lane group q owns
+// (bytes q * D/8 .. + D/8 of the row), as D / 32 words.
+template <int D, int HG>
+__device__ __forceinline__ void load_v_bytes(const unsigned char* sv, int hh, int j, int q,
+                                             unsigned (&w)[D / 32]) {
+  if constexpr (D == 128) {
+    const uint4 x = *reinterpret_cast<const uint4*>(sv + raw_off<D, true, HG>(hh, j, q));
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+  } else {
+    const uint2 x = *reinterpret_cast<const uint2*>(sv + (hh * UNIT + j) * 64 + q * 8);
+    w[0] = x.x; w[1] = x.y;
+  }
+}
+
+template <int D, bool FP8, int NT, int HG, int WPH>
+__global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH > 1 ? 2 : 1)
     decode_split_kernel(const Problem p, const __grid_constant__ CUtensorMap kvmap, float sl2,
                         float out_scale) {
-  using C = DecodeCfg<D, FP8, HG>;
+  using C = DecodeCfg<D, FP8, NT, HG, WPH>;
   constexpr int NST = C::NST;
   extern __shared__ unsigned char smem_raw[];
   // TMA's 128-byte swizzle is laid out from 1024-byte aligned boxes
@@ -110,8 +143,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
   const int r = item / (S * n_groups);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
-  const int g = grp * HG + warp;              // this consumer warp's KV head
-  const int quad = lane >> 2, c4 = lane & 3;  // fragment row / column group
+  const int hh = warp % HG, wslot = warp / HG;  // consumer: head in the group, unit slot
+  const int g = grp * HG + hh;                  // this consumer warp's KV head
+  const int quad = lane >> 2, c4 = lane & 3;    // fragment row / column group
 
   const int t0 = p.qsl[r];
   const int q_len = p.qsl[r + 1] - t0;
@@ -149,7 +183,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
   }
   __syncthreads();
 
-  if (warp == HG) {
+  if (warp == C::NW) {
     // ------------------------------------------------------------ producer warp
     // Block ids are read 32 units at a time (one coalesced load); lane 0
     // issues one tensor copy for K and one for V per unit (16 keys of all HG
@@ -204,8 +238,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
   // k-step kk and head tile nt is Q[head][d] at head = nt*8 + quad.  For
   // 16-bit K, d = 16kk + 2*c4 (+1, +8, +9).  For e4m3 K the d axis is permuted
   // (the same permutation on Q and K leaves every dot product unchanged) so
-  // each lane reads its K bytes contiguously: k-step kk, fragment columns
-  // 2*c4 + j and 2*c4 + 8 + j map to d = c4*D/4 + 4kk + j and + 2 + j.
+  // each lane reads its K bytes contiguously and widens whole words: k-step
+  // kk, fragment columns 2*c4, 2*c4+1, 2*c4+8, 2*c4+9 map to d = base,
+  // base + 2, base + 1, base + 3 with base = c4*D/4 + 4kk (bytes 0, 2 and 1, 3
+  // of the word holding d = base..base+3).
   unsigned qb[D / 16][NT][2];
   {
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
@@ -219,13 +255,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
           const int head = nt * 8 + quad;
           unsigned v = 0;
           if (head < G) {
-            const int d = FP8 ? (c4 * (D / 4) + 4 * kk + 2 * e) : (kk * 16 + 2 * c4 + e * 8);
-            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(qrow + head * D + d);
             if constexpr (FP8) {
-              const float2 f = __bfloat1622float2(x);
-              v = pack2<true>(f.x, f.y);
+              // d = base + e and base + 2 + e, base = c4*D/4 + 4kk
+              const __nv_bfloat16* qd = qrow + head * D + c4 * (D / 4) + 4 * kk + e;
+              v = pack2<true>(__bfloat162float(qd[0]), __bfloat162float(qd[2]));
             } else {
-              v = *reinterpret_cast<const unsigned*>(&x);
+              const int d = kk * 16 + 2 * c4 + e * 8;
+              v = *reinterpret_cast<const unsigned*>(qrow + head * D + d);
             }
           }
           qb[kk][nt][e] = v;
@@ -254,7 +290,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
   const int src0 = 8 * c4 + (quad >> 1), src1 = src0 + 4;
   const unsigned half_sel = (quad & 1) ? 0x7632u : 0x5410u;
 
-  for (int i = 0; i < n_units; ++i) {
+  for (int i = wslot; i < n_units; i += WPH) {
     const int st = i % NST;
     if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (i / NST) & 1, status, nullptr))) break;
     unsigned char* sk = smem + st * C::STAGE;
@@ -267,8 +303,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
       for (int c = lane; c < UNIT * CH_ROW; c += 32) {
         const int j = c / CH_ROW, cc = c % CH_ROW;
         if (key0 + j >= s) {
-          *reinterpret_cast<uint4*>(sk + raw_off<D, FP8, HG>(warp, j, cc)) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sv + raw_off<D, FP8, HG>(warp, j, cc)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sk + raw_off<D, FP8, HG>(hh, j, cc)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sv + raw_off<D, FP8, HG>(hh, j, cc)) = make_uint4(0, 0, 0, 0);
         }
       }
       // the stage is refilled by TMA (async proxy) after this warp releases it
@@ -283,7 +319,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
     for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) sc[ch][nt][0] = sc[ch][nt][1] = sc[ch][nt][2] = sc[ch][nt][3] = 0.f;
-    unsigned sv_a;
     if constexpr (FP8) {
       // K fragments straight from the e4m3 bytes: this lane's D/4 bytes of
       // key rows quad and quad + 8, widened in registers.
@@ -293,51 +328,31 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
       for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
         for (int q = 0; q < CPL; ++q)
-          kr[hr][q] = *reinterpret_cast<const uint4*>(sk + raw_off<D, FP8, HG>(warp, quad + 8 * hr, c4 * CPL + q));
+          kr[hr][q] = *reinterpret_cast<const uint4*>(sk + raw_off<D, FP8, HG>(hh, quad + 8 * hr, c4 * CPL + q));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint4& ra = kr[0][kk >> 2];
         const uint4& rb = kr[1][kk >> 2];
         const unsigned w0 = (kk & 3) == 0 ? ra.x : (kk & 3) == 1 ? ra.y : (kk & 3) == 2 ? ra.z : ra.w;
         const unsigned w1 = (kk & 3) == 0 ? rb.x : (kk & 3) == 1 ? rb.y : (kk & 3) == 2 ? rb.z : rb.w;
-        const unsigned a0 = e4m3x2_to_f16x2_scaled(__byte_perm(w0, 0u, 0x1404u));
-        const unsigned a2 = e4m3x2_to_f16x2_scaled(__byte_perm(w0, 0u, 0x3424u));
-        const unsigned a1 = e4m3x2_to_f16x2_scaled(__byte_perm(w1, 0u, 0x1404u));
-        const unsigned a3 = e4m3x2_to_f16x2_scaled(__byte_perm(w1, 0u, 0x3424u));
+        const unsigned a0 = e4m3_b02_to_f16x2(w0);   // key quad,     d base, base + 2
+        const unsigned a2 = e4m3_b13_to_f16x2(w0);   // key quad,     d base + 1, base + 3
+        const unsigned a1 = e4m3_b02_to_f16x2(w1);   // key quad + 8
+        const unsigned a3 = e4m3_b13_to_f16x2(w1);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           mma_16816<true>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
       }
-      // widen this head's V (e4m3 -> f16, times 2^-8) into its 16-bit buffer
-      unsigned char* hv = smem + C::WIDE_OFF + warp * C::H_UNIT;
-      constexpr int CH_ROW = C::RAW_ROW / 16;
-#pragma unroll
-      for (int c = lane; c < UNIT * CH_ROW; c += 32) {
-        const int j = c / CH_ROW, cc = c % CH_ROW;
-        const uint4 raw = *reinterpret_cast<const uint4*>(sv + raw_off<D, FP8, HG>(warp, j, cc));
-        const unsigned w[4] = {raw.x, raw.y, raw.z, raw.w};
-        unsigned h[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          h[2 * q] = e4m3x2_to_f16x2_scaled(__byte_perm(w[q], 0u, 0x1404u));
-          h[2 * q + 1] = e4m3x2_to_f16x2_scaled(__byte_perm(w[q], 0u, 0x3424u));
-        }
-        *reinterpret_cast<uint4*>(hv + swz<D>(j, 2 * cc)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(hv + swz<D>(j, 2 * cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-      }
-      __syncwarp();
-      sv_a = smem_u32(hv);
     } else {
       const unsigned sk_a = smem_u32(sk);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         unsigned a0, a1, a2, a3;
-        ldsm_x4(sk_a + raw_off<D, FP8, HG>(warp, s_row, 2 * kk + s_csel), a0, a1, a2, a3);
+        ldsm_x4(sk_a + raw_off<D, FP8, HG>(hh, s_row, 2 * kk + s_csel), a0, a1, a2, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           mma_16816<false>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
       }
-      sv_a = smem_u32(sv);
     }
 
     // Mask (keys quad and quad + 8 of this unit), scale to log2 units, online
@@ -356,24 +371,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
         x[e] = ((e < 2) ? va : vb) ? v * sl2 : -INFINITY;
       }
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float mx = fmaxf(x[hh], x[2 + hh]);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float mx = fmaxf(x[h2], x[2 + h2]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[nt][hh], mx);
+        const float m_new = fmaxf(m_run[nt][h2], mx);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        alpha[nt][hh] = fast_exp2(m_run[nt][hh] - m_use);
-        moved |= (alpha[nt][hh] != 1.f);
-        m_run[nt][hh] = m_new;
-        const float pa = fast_exp2(x[hh] - m_use), pb = fast_exp2(x[2 + hh] - m_use);
-        x[hh] = pa;
-        x[2 + hh] = pb;
+        alpha[nt][h2] = fast_exp2(m_run[nt][h2] - m_use);
+        moved |= (alpha[nt][h2] != 1.f);
+        m_run[nt][h2] = m_new;
+        const float pa = fast_exp2(x[h2] - m_use), pb = fast_exp2(x[2 + h2] - m_use);
+        x[h2] = pa;
+        x[2 + h2] = pb;
         float ps = pa + pb;
         ps += __shfl_xor_sync(0xffffffffu, ps, 4);
         ps += __shfl_xor_sync(0xffffffffu, ps, 8);
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l_run[nt][hh] = l_run[nt][hh] * alpha[nt][hh] + ps;
+        l_run[nt][h2] = l_run[nt][h2] * alpha[nt][h2] + ps;
       }
       pk_lo[nt] = pack2<FP8>(x[0], x[1]);  // key quad,     heads 2*c4, 2*c4+1
       pk_hi[nt] = pack2<FP8>(x[2], x[3]);  // key quad + 8, heads 2*c4, 2*c4+1
@@ -404,23 +419,105 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
     }
 
     // O^T += V^T P^T: M = d (16 per tile), N = heads, K = the 16 keys.
+    if constexpr (FP8) {
+      // V^T fragments straight from the e4m3 bytes.  The d axis of V (and so
+      // of O) is permuted: tile m, fragment row quad is d = quad*D/8 + 2m and
+      // row quad + 8 is d = quad*D/8 + 2m + 1, so each lane reads D/8
+      // contiguous bytes of each of its key rows 2*c4, 2*c4+1, 2*c4+8, 2*c4+9.
+      unsigned v0[D / 32], v1[D / 32], v2[D / 32], v3[D / 32];
+      load_v_bytes<D, HG>(sv, hh, 2 * c4, quad, v0);
+      load_v_bytes<D, HG>(sv, hh, 2 * c4 + 1, quad, v1);
+      load_v_bytes<D, HG>(sv, hh, 2 * c4 + 8, quad, v2);
+      load_v_bytes<D, HG>(sv, hh, 2 * c4 + 9, quad, v3);
 #pragma unroll
-    for (int m = 0; m < D / 16; ++m) {
-      unsigned a0, a1, a2, a3;
-      ldsm_x4_t(sv_a + (FP8 ? swz<D>(v_row, 2 * m + v_csel)
-                            : raw_off<D, FP8, HG>(warp, v_row, 2 * m + v_csel)),
-                a0, a1, a2, a3);
+      for (int m = 0; m < D / 16; ++m) {
+        // bytes d0 and d0 + 1 of two key rows in one word: [r.d0, r.d0+1,
+        // r'.d0, r'.d0+1]; bytes 0 and 2 are the pair at d0, 1 and 3 at d0 + 1
+        const int wi = m >> 1;
+        const unsigned sel = (m & 1) ? 0x7632u : 0x5410u;
+        const unsigned x01 = __byte_perm(v0[wi], v1[wi], sel);
+        const unsigned x23 = __byte_perm(v2[wi], v3[wi], sel);
+        const unsigned a0 = e4m3_b02_to_f16x2(x01);
+        const unsigned a1 = e4m3_b13_to_f16x2(x01);
+        const unsigned a2 = e4m3_b02_to_f16x2(x23);
+        const unsigned a3 = e4m3_b13_to_f16x2(x23);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_16816<FP8>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816<true>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+      }
+    } else {
+      const unsigned sv_a = smem_u32(sv);
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m) {
+        unsigned a0, a1, a2, a3;
+        ldsm_x4_t(sv_a + raw_off<D, FP8, HG>(hh, v_row, 2 * m + v_csel), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816<false>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+      }
     }
     // Release the stage once every lane of every consumer warp has read it.
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
 
+  // ---------------------------------------------------------------- merge
+  // The WPH warps of a KV head saw disjoint units of the partition: the
+  // others hand (o, m, l) to warp slot 0 through shared memory (the ring is
+  // idle once every consumer has left its loop), in the same fragment layout,
+  // and slot 0 merges them with the online-softmax rule.
+  if constexpr (WPH > 1) {
+    named_bar_sync(1, C::NW * 32);
+    float* mb = reinterpret_cast<float*>(smem);
+    if (wslot > 0) {
+      float* dst = mb + ((wslot - 1) * HG + hh) * C::MERGE_FLOATS * 32 + lane;
+      int idx = 0;
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[32 * idx++] = o[m][nt][e];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          dst[32 * idx++] = m_run[nt][h2];
+          dst[32 * idx++] = l_run[nt][h2];
+        }
+    }
+    named_bar_sync(1, C::NW * 32);
+    if (wslot > 0) return;
+#pragma unroll
+    for (int ws = 1; ws < WPH; ++ws) {
+      const float* src = mb + ((ws - 1) * HG + hh) * C::MERGE_FLOATS * 32 + lane;
+      float a_self[NT][2], a_other[NT][2];
+      int idx = (D / 16) * NT * 4;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float m2 = src[32 * idx++], l2 = src[32 * idx++];
+          const float mn = fmaxf(m_run[nt][h2], m2);
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          a_self[nt][h2] = fast_exp2(m_run[nt][h2] - mu);
+          a_other[nt][h2] = fast_exp2(m2 - mu);
+          l_run[nt][h2] = l_run[nt][h2] * a_self[nt][h2] + l2 * a_other[nt][h2];
+          m_run[nt][h2] = mn;
+        }
+      idx = 0;
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[m][nt][e] = o[m][nt][e] * a_self[nt][e & 1] + src[32 * idx++] * a_other[nt][e & 1];
+          }
+    }
+  }
+
   // ---------------------------------------------------------------- outputs
-  // Each consumer warp owns its KV head's G query heads: normalise and write
-  // them (bf16 output) or the partition's (o_p, lse_p) for the combine step.
+  // Slot 0 of each KV head owns its G query heads: normalise and write them
+  // (bf16 output) or the partition's (o_p, lse_p) for the combine step.
   const int h0 = g * G;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -433,7 +530,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, HG>::THREADS)
       const float inv = (L > 0.f) ? out_scale / L : 0.f;
 #pragma unroll
       for (int m = 0; m < D / 16; ++m) {
-        const int d = 16 * m + quad + ((e & 2) ? 8 : 0);
+        const int d = FP8 ? (quad * (D / 8) + 2 * m + (e >> 1)) : (16 * m + quad + ((e & 2) ? 8 : 0));
         const float val = o[m][nt][e] * inv;
         if (S == 1) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -485,10 +582,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const Problem p) {
   }
 }
 
-template <int D, bool FP8, int HG>
+template <int D, bool FP8, int NT, int HG, int WPH>
 cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
-  using C = DecodeCfg<D, FP8, HG>;
-  auto kern = (p.G <= 8) ? decode_split_kernel<D, FP8, 1, HG> : decode_split_kernel<D, FP8, 2, HG>;
+  using C = DecodeCfg<D, FP8, NT, HG, WPH>;
+  auto kern = decode_split_kernel<D, FP8, NT, HG, WPH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // e4m3 data is widened to f16 as value * 2^-8; the 2^8 goes into the scales.
@@ -500,12 +597,20 @@ cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
   return cudaGetLastError();
 }
 
+// Up to 8 query heads per KV head (one head tile): two warps per KV head
+// share each partition; more: one warp per KV head, two head tiles.
+template <int D, bool FP8, int HG>
+cudaError_t launch_decode_g(const Problem& p, const CUtensorMap& kvmap) {
+  return (p.G <= 8) ? launch_decode_t<D, FP8, 1, HG, 2>(p, kvmap)
+                    : launch_decode_t<D, FP8, 2, HG, 1>(p, kvmap);
+}
+
 template <int D, bool FP8>
 cudaError_t launch_decode_hg(const Problem& p, const CUtensorMap& kvmap) {
-  switch (decode_head_group(p.Hkv)) {
-    case 4: return launch_decode_t<D, FP8, 4>(p, kvmap);
-    case 2: return launch_decode_t<D, FP8, 2>(p, kvmap);
-    default: return launch_decode_t<D, FP8, 1>(p, kvmap);
+  switch (decode_head_group(p.Hkv, D, FP8)) {
+    case 4: return launch_decode_g<D, FP8, 4>(p, kvmap);
+    case 2: return launch_decode_g<D, FP8, 2>(p, kvmap);
+    default: return launch_decode_g<D, FP8, 1>(p, kvmap);
   }
 }
 
@@ -517,7 +622,9 @@ cudaError_t launch_decode(const Problem& p, const CUtensorMap& kvmap) {
   return p.kv_dtype ? launch_decode_hg<64, true>(p, kvmap) : launch_decode_hg<64, false>(p, kvmap);
 }
 
-int decode_heads_per_cta(int Hkv) { return decode_head_group(Hkv); }
+int decode_heads_per_cta(int Hkv, int D, int kv_dtype) {
+  return decode_head_group(Hkv, D, kv_dtype != 0);  // kv_dtype 1: e4m3
+}
 
 cudaError_t launch_combine(const Problem& p) {
   const long long rows = static_cast<long long>(p.B) * p.H;

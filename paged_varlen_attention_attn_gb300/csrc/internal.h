@@ -65,8 +65,9 @@ bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, 
 // as [d half][head][row][128 bytes] (16-bit) or [head][row][row bytes] (e4m3).
 bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv,
                        int bs, int NB, int heads);
-// KV heads one decode CTA serves (4, 2 or 1: the largest dividing Hkv).
-int decode_heads_per_cta(int Hkv);
+// KV heads one decode CTA serves (4, 2 or 1: the largest dividing Hkv whose
+// 16-key K + V unit fits in 16 KB).
+int decode_heads_per_cta(int Hkv, int D, int kv_dtype);
 
 // Query rows one prefill CTA covers: two heads x 128 rows when the GQA group
 // size is even, else one head x 256 rows.

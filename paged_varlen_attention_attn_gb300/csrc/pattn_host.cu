@@ -56,18 +56,19 @@ bool ext_ok(const pattn_ext_t* ext) {
 }
 
 // Decode partition count.  A forced count is used as given; otherwise enough
-// partitions that the decode grid (requests x KV-head groups x partitions)
-// covers the SMs about four times, and that no partition is longer than ~1024
-// keys, bounded by the block count a row can see and by PATTN_MAX_SPLITS.
+// partitions that there are about 8 (request, KV head, partition) items per
+// SM (2 to 4 decode CTAs, depending on how many KV heads one CTA serves), and
+// that no partition is longer than ~1024 keys, bounded by the block count a
+// row can see and by PATTN_MAX_SPLITS.  It depends on neither dtype nor head
+// size, so pattn_workspace_bytes can size the partials without them.
 int choose_splits(const pattn_ext_t* ext, int num_kv_heads, int block_size, int window) {
   if (ext->num_splits > 0) return ext->num_splits;
   const int visible = (window > 0) ? std::min(ext->max_seq_len, window + block_size)
                                    : ext->max_seq_len;
   const int max_blocks = std::max(1, (visible + block_size - 1) / block_size);
-  const long long items = static_cast<long long>(std::max(1, ext->num_seqs)) *
-                          (num_kv_heads / decode_heads_per_cta(num_kv_heads));
+  const long long items = static_cast<long long>(std::max(1, ext->num_seqs)) * num_kv_heads;
   const int sms = sm_count();
-  int by_grid = static_cast<int>((4LL * sms + items - 1) / items);
+  int by_grid = static_cast<int>((8LL * sms + items - 1) / items);
   int by_len = (visible + 1023) / 1024;
   int s = std::max(1, std::max(by_grid, by_len));
   s = std::min(s, max_blocks);
@@ -318,7 +319,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   mark(4);
   CUtensorMap dmap;
   if (!encode_decode_map(&dmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
-                         ext->num_blocks, decode_heads_per_cta(num_kv_heads)))
+                         ext->num_blocks, decode_heads_per_cta(num_kv_heads, head_size, kv_dtype)))
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
   mark(5);

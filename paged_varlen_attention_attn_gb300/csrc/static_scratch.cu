@@ -146,7 +146,7 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
     return PATTN_ERR_CUDA;
   CUtensorMap dmap;
   if (!encode_decode_map(&dmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
-                         num_blocks, decode_heads_per_cta(num_kv_heads)))
+                         num_blocks, decode_heads_per_cta(num_kv_heads, head_size, kv_dtype)))
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
   if (splits > 1 && launch_combine(p) != cudaSuccess) return PATTN_ERR_CUDA;

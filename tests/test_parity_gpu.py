@@ -61,6 +61,19 @@ def test_decode_fp8(splits):
     check_case(make(spec), num_splits=splits)
 
 
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_FP8_E4M3])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Hkv", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [4, 16])
+def test_decode_every_kernel_shape(G, Hkv, D, kv_dtype):
+    """Every decode kernel instance: head size x KV dtype x KV heads per CTA
+    (4, 2 or 1, set by Hkv and the stage size) x one or two head tiles (G up
+    to 8 or above), with partitions and a ragged last page."""
+    spec = small_spec(800 + G * 31 + Hkv * 7 + D + kv_dtype, H=G * Hkv, Hkv=Hkv, d=D,
+                      bs=16, n_req=3, max_s=700, kv_dtype=kv_dtype, kinds=("decode",))
+    check_case(make(spec), num_splits=3)
+
+
 def test_decode_noncausal():
     spec = small_spec(610, H=8, Hkv=2, d=64, bs=16, n_req=4, max_s=300, causal=0,
                       kinds=("decode",))
