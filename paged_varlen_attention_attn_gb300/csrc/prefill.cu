@@ -13,10 +13,12 @@
 // group size is odd, two consecutive row tiles of one head.  Twelve warps:
 //   warps 0-3  softmax + epilogue of sub-tile A, thread i owns row i (TMEM lane i)
 //   warps 4-7  softmax + epilogue of sub-tile B
-//   warp  8    TMA producer: both Q tiles once, then K and V tiles page by
-//              page through block_table into 3-stage (K) and 2-stage (V) rings
+//   warp  8    TMA producer of both Q tiles (once) and the K tiles, page by
+//              page through block_table into a 3-stage ring, one lane per
+//              page copy
 //   warp  9    MMA issuer (one thread)
-//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+//   warp 10    TMA producer of the V tiles (2-stage ring), likewise
+//   warp 11    idle (it completes the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
 // [384,384+D).  P (bf16, 64 columns) overwrites the upper half of its S
 // buffer and is read back from TMEM as the A operand of P V; the next scores
@@ -55,7 +57,7 @@ constexpr int PF_THREADS = 384;
 // stay within the launch allocation (PF_THREADS x the kernel's register count,
 // checked on the host before every launch) or setmaxnreg.inc would wait forever.
 constexpr int SOFTMAX_REGS = 216;
-constexpr int OTHER_REGS = 64;
+constexpr int OTHER_REGS = 72;
 constexpr int SPLIT_REGS_TOTAL = 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS;
 // K and V rings: K gets the extra stage because the next scores need it
 // before the next P V needs V.  224 KB of shared memory at head size 128.
@@ -215,12 +217,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(OTHER_REGS));
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    // The whole warp reads the block ids of a key tile in one coalesced load,
-    // one tile ahead; lane 0 issues the copies.
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 8 streams Q (once) and the K tiles, warp 10 the V tiles, each
+    // through its own ring, so a K tile never queues behind a V slot.  Each
+    // warp reads the block ids of a key tile in one coalesced load, one tile
+    // ahead.  Lane 0 waits for the stage and posts the tile's bytes; the
+    // tile's copies (one per page and d half) then go out from one lane each,
+    // so a tile costs one copy instruction, not 2 x pages of them in one
+    // thread.
+    const int kv = (warp == 10) ? 1 : 0;
     if (n_union > 0) {
-      if (lane == 0) {
+      if (kv == 0 && lane == 0) {
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kvmap);
 #pragma unroll
@@ -249,42 +257,33 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         return blk;
       };
       int blk_next = page_block(u0);
+      // Copy `lane` of a tile: page lane / DH, d half lane % DH.
+      const int my_pg = lane / C::DH, my_dh = lane % C::DH;
+      const int nst = kv ? PF_VST : PF_KST;
+      unsigned char* ring = kv ? sV : sK;
       for (int j = 0; j < n_union; ++j) {
-        int ids[BLOCK_N / 16];
-#pragma unroll
-        for (int pg = 0; pg < BLOCK_N / 16; ++pg) ids[pg] = __shfl_sync(FULL, blk_next, pg);
+        const int key_base = (u0 + j) * BLOCK_N;
+        const int my_blk = __shfl_sync(FULL, blk_next, my_pg);
         if (j + 1 < n_union) blk_next = page_block(u0 + j + 1);
+        // pages of this tile that hold keys below seq_len
+        const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
+        const int my_key0 = key_base + my_pg * rows_box;
+        const int my_slot = p.bs_shift >= 0 ? (my_key0 & (p.bs - 1)) : (my_key0 % p.bs);
+        const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
+        const int st = j % nst;
+        uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+        uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
         int ok = 1;
         if (lane == 0) {
-          const int key_base = (u0 + j) * BLOCK_N;
-          int n_load = 0;
-          for (int pg = 0; pg < pages_per_tile; ++pg)
-            if (key_base + pg * rows_box < s) ++n_load;
-          const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
-          // K first: the next scores need it before the next P V needs V.
-          for (int kv = 0; kv < 2 && ok; ++kv) {
-            const int nst = kv ? PF_VST : PF_KST;
-            const int st = j % nst;
-            uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
-            uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-            if (j >= nst && !mbar_wait(empty, ((j / nst) - 1) & 1, status, abort_flag)) {
-              ok = 0;
-              break;
-            }
-            unsigned char* dst = (kv ? sV : sK) + st * C::TILE;
+          if (j >= nst && !mbar_wait(empty, ((j / nst) - 1) & 1, status, abort_flag))
+            ok = 0;
+          else
             mbar_arrive_expect_tx(full, bytes);
-#pragma unroll
-            for (int pg = 0; pg < BLOCK_N / 16; ++pg) {
-              const int key0 = key_base + pg * rows_box;
-              if (pg >= pages_per_tile || key0 >= s) break;
-#pragma unroll
-              for (int dh = 0; dh < C::DH; ++dh)
-                tma_load_4d(dst + dh * C::HALF + pg * rows_box * 128, &kvmap, full, dh * 64, g,
-                            key0 % p.bs, kv * p.NB + ids[pg]);
-            }
-          }
         }
         if (!__shfl_sync(FULL, ok, 0)) break;
+        if (my_pg < n_load)
+          tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap, full,
+                      my_dh * 64, g, my_slot, kv * p.NB + my_blk);
       }
     }
   } else if (warp == 9) {
@@ -303,7 +302,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       for (int j = 0; ok && j <= n_union; ++j) {
         const int kt = u0 + j;
         bool k_ready = false, v_ready = false;
-#pragma unroll 1
+        // Unrolled: every per-sub-tile value stays in a register (a runtime
+        // choice between two locals would put them in local memory).
+#pragma unroll
         for (int X = 0; X < 2; ++X) {
           const Sub& u = X ? subB : subA;
           int& n_pv = X ? n_pv1 : n_pv0;
