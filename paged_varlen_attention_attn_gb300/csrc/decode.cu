@@ -8,8 +8,8 @@
 // num_queries_per_kv).  The partition is a run of whole KV blocks ("RBLN
 // Attention modes": flash attention processes the cache by partitions and
 // merges them with online softmax); partial results go to the workspace as
-// (o_p, lse_p) and combine_kernel merges them, or the CTA writes the output
-// directly when there is one partition.
+// (o_p, lse_p) and the last CTA of each (request, group) to finish merges
+// them, or the CTA writes the output directly when there is one partition.
 //
 // Data path: a producer warp streams 16-key units through a ring of
 // shared-memory stages; one unit is 16 rows of all HG heads of the group, K
@@ -125,6 +125,64 @@ __device__ __forceinline__ void load_v_bytes(const unsigned char* sv, int hh, in
   }
 }
 
+// One warp merges the S partitions (S <= 64) of NH decode rows (request r,
+// heads h .. h + NH - 1): out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M),
+// M = max_p lse_p (log2 units); an empty partition (lse_p = -inf) weighs 0.
+// Lanes hold the partitions' lse (two each), the max and the weight sum are
+// warp reductions, and the loads of all partitions and all NH rows are
+// independent, so the merge costs a few memory round trips, not S * NH of
+// them.  The partials were written by other CTAs: they are read past L1.
+template <int D, int NH>
+__device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h, int t0, int lane) {
+  const int S = p.splits;
+  constexpr int PER = D / 32;
+  float w0[NH], w1[NH], inv[NH], acc[NH][PER];
+#pragma unroll
+  for (int k = 0; k < NH; ++k) {
+    const int64_t prow = (static_cast<int64_t>(r) * p.H + h + k) * S;
+    w0[k] = (lane < S) ? __ldcg(p.lse_part + prow + lane) : -INFINITY;
+    w1[k] = (lane + 32 < S) ? __ldcg(p.lse_part + prow + lane + 32) : -INFINITY;
+  }
+#pragma unroll
+  for (int k = 0; k < NH; ++k) {
+    float M = fmaxf(w0[k], w1[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    w0[k] = (w0[k] == -INFINITY) ? 0.f : exp2f(w0[k] - Mu);
+    w1[k] = (w1[k] == -INFINITY) ? 0.f : exp2f(w1[k] - Mu);
+    float L = w0[k] + w1[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    inv[k] = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[k][e] = 0.f;
+  }
+#pragma unroll 2
+  for (int sp = 0; sp < S; ++sp) {
+#pragma unroll
+    for (int k = 0; k < NH; ++k) {
+      const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0[k] : w1[k], sp & 31);
+      const float* src = p.o_part + ((static_cast<int64_t>(r) * p.H + h + k) * S + sp) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+        acc[k][0] += w * v.x; acc[k][1] += w * v.y; acc[k][2] += w * v.z; acc[k][3] += w * v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+        acc[k][0] += w * v.x; acc[k][1] += w * v.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NH; ++k) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(t0) * p.H + h + k) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+      *reinterpret_cast<__nv_bfloat162*>(out + e) =
+          __floats2bfloat162_rn(acc[k][e] * inv[k], acc[k][e + 1] * inv[k]);
+  }
+}
+
 template <int D, bool FP8, int NT, int HG, int WPH>
 __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH > 1 ? 2 : 1)
     decode_split_kernel(const Problem p, const __grid_constant__ CUtensorMap kvmap, float sl2,
@@ -149,7 +207,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
 
   const int t0 = p.qsl[r];
   const int q_len = p.qsl[r + 1] - t0;
-  if (q_len != 1) return;
+  if (q_len != 1) {
+    // A call declared decode-only (max_query_len <= 1) runs no other kernel
+    // over its requests: a longer one is bad metadata, reported and zeroed
+    // here (once, clamped to the output).
+    if (p.max_q <= 1 && q_len != 0 && grp == 0 && sp == 0) {
+      if (threadIdx.x == 0) flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
+      const int64_t a = static_cast<int64_t>(max(0, t0)) * p.H * D;
+      const int64_t b = static_cast<int64_t>(min(p.T, t0 + max(q_len, 0))) * p.H * D;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+      for (int64_t e = a + threadIdx.x; e < b; e += blockDim.x) out[e] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
   int s = p.seq_lens[r];
   bool bad = (s < 1) || (s > p.mbps * p.bs) || (t0 < 0) || (t0 >= p.T);
   unsigned* status = &p.hdr->status;
@@ -485,9 +555,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         }
     }
     named_bar_sync(1, C::NW * 32);
-    if (wslot > 0) return;
+    // with a single partition the other slots have nothing left to do
+    if (wslot > 0 && S == 1) return;
 #pragma unroll
-    for (int ws = 1; ws < WPH; ++ws) {
+    for (int ws = 1; ws < (wslot == 0 ? WPH : 1); ++ws) {
       const float* src = mb + ((ws - 1) * HG + hh) * C::MERGE_FLOATS * 32 + lane;
       float a_self[NT][2], a_other[NT][2];
       int idx = (D / 16) * NT * 4;
@@ -517,10 +588,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
 
   // ---------------------------------------------------------------- outputs
   // Slot 0 of each KV head owns its G query heads: normalise and write them
-  // (bf16 output) or the partition's (o_p, lse_p) for the combine step.
+  // (bf16 output) or the partition's (o_p, lse_p) for the merge below.
   const int h0 = g * G;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int nt = 0; nt < (wslot == 0 ? NT : 0); ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int head = nt * 8 + 2 * c4 + (e & 1);
@@ -543,42 +614,40 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         }
       }
     }
-}
 
-// One warp per (request, head): merge the partitions of a decode row.
-template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const Problem p) {
-  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= p.B * p.H) return;
-  const int r = wid / p.H, h = wid % p.H;
-  const int t0 = p.qsl[r];
-  if (p.qsl[r + 1] - t0 != 1 || t0 < 0 || t0 >= p.T) return;
-  const int S = p.splits;
-  const int64_t prow = (static_cast<int64_t>(r) * p.H + h) * S;
-  float M = -INFINITY;
-  for (int sp = 0; sp < S; ++sp) M = fmaxf(M, p.lse_part[prow + sp]);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  constexpr int PER = D / 32;
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  for (int sp = 0; sp < S; ++sp) {
-    const float l = p.lse_part[prow + sp];
-    if (l == -INFINITY) continue;
-    const float w = exp2f(l - Mu);
-    L += w;
-    const float* src = p.o_part + (prow + sp) * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += w * src[e];
-  }
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(t0) * p.H + h) * D + lane * PER;
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
-#pragma unroll
-  for (int e = 0; e < PER; e += 2) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-    *reinterpret_cast<__nv_bfloat162*>(out + e) = v;
+  // ---------------------------------------------------------------- merge of the partitions
+  // Each CTA publishes its partition (counts it with a release); the CTA that
+  // completes the count of its (request, KV-head group) merges the group's
+  // S partitions into the output, so no separate combine launch is needed.
+  // All consumer warps are still running; the merging CTA spreads the
+  // group's HG * G query heads over them.
+  if (S > 1) {
+    __shared__ int s_last;
+    // The barrier orders every warp's partial stores before thread 0's
+    // acquire-release add (a release is cumulative), which publishes them
+    // at GPU scope; the add that completes the count acquires every other
+    // CTA's, and the second barrier hands that on to this CTA's warps.
+    named_bar_sync(2, C::NW * 32);
+    if (threadIdx.x == 0) {
+      unsigned* cnt = p.counters + static_cast<int64_t>(r) * p.Hkv + grp;
+      unsigned prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(cnt)
+                   : "memory");
+      s_last = (prev == static_cast<unsigned>(S - 1)) ? 1 : 0;
+      if (s_last) *cnt = 0u;  // every partition of the group has counted
+    }
+    named_bar_sync(2, C::NW * 32);
+    if (!s_last) return;
+    // heads in pairs (G is even, or 1: then HG * G = HG and pairs may not fit)
+    const int nq = HG * G, h_first = grp * HG * G;
+    if (nq % 2 == 0) {
+      for (int hq = 2 * warp; hq < nq; hq += 2 * C::NW)
+        merge_partitions<D, 2>(p, r, h_first + hq, t0, lane);
+    } else {
+      for (int hq = warp; hq < nq; hq += C::NW) merge_partitions<D, 1>(p, r, h_first + hq, t0, lane);
+    }
   }
 }
 
@@ -624,17 +693,6 @@ cudaError_t launch_decode(const Problem& p, const CUtensorMap& kvmap) {
 
 int decode_heads_per_cta(int Hkv, int D, int kv_dtype) {
   return decode_head_group(Hkv, D, kv_dtype != 0);  // kv_dtype 1: e4m3
-}
-
-cudaError_t launch_combine(const Problem& p) {
-  const long long rows = static_cast<long long>(p.B) * p.H;
-  if (rows == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
-  if (p.D == 128)
-    combine_kernel<128><<<grid, 128, 0, p.stream>>>(p);
-  else
-    combine_kernel<64><<<grid, 128, 0, p.stream>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace pattn

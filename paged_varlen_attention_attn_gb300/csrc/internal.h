@@ -36,22 +36,24 @@ struct Problem {
   int2* tiles;       // (request, row-item) pairs sorted by cost, descending
   int max_tiles;     // capacity of tiles[]
   int rows_per_item; // query rows of one prefill work item (128 or 256)
+  unsigned* counters;  // [B][Hkv]: partitions of a (request, KV-head group) done
   float* o_part;     // [B][H][splits][D]  (splits > 1)
   float* lse_part;   // [B][H][splits]     (log2 domain)
   cudaStream_t stream;
 };
 
 // Workspace layout for a problem (offsets in bytes, 256-byte aligned).
+// The header and the counters come first, so one memset of counters_end
+// bytes clears both.
 struct WsLayout {
-  size_t tiles_off, o_part_off, lse_off, total;
+  size_t counters_off, counters_end, tiles_off, o_part_off, lse_off, total;
   int max_tiles;
 };
-WsLayout workspace_layout(int B, int T, int H, int D, int max_q, int splits);
+WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int splits);
 
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const Problem& p);
 cudaError_t launch_decode(const Problem& p, const CUtensorMap& kv_map);
-cudaError_t launch_combine(const Problem& p);
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
 // TMA tensor map over the KV cache [2 * NB][bs][Hkv][D] with boxes of
 // box_rows rows of one head: 64 16-bit elements (128-byte swizzle) per box, or

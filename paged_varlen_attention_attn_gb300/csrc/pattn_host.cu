@@ -140,9 +140,12 @@ bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-WsLayout workspace_layout(int B, int T, int H, int D, int max_q, int splits) {
+WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int splits) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
+  L.counters_off = off;
+  L.counters_end = off + static_cast<size_t>(B) * Hkv * sizeof(unsigned);
+  off = align_up(L.counters_end, 256);
   L.max_tiles = (max_q > 1) ? (T + BLOCK_M - 1) / BLOCK_M + B : 0;
   L.tiles_off = off;
   off = align_up(off + static_cast<size_t>(L.max_tiles) * sizeof(int2), 256);
@@ -190,7 +193,7 @@ size_t pattn_workspace_bytes(const pattn_ext_t* ext, int num_heads, int num_kv_h
   if (validate(ext, num_heads, num_kv_heads, head_size, block_size) != PATTN_OK) return 0;
   // The window only lowers the automatic split count; size for no window.
   const int splits = choose_splits(ext, num_kv_heads, block_size, 0);
-  return workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, head_size,
+  return workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads, head_size,
                           ext->max_query_len, splits)
       .total;
 }
@@ -240,7 +243,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
     return PATTN_ERR_INVALID_ARGUMENT;
 
   const int splits = choose_splits(ext, num_kv_heads, block_size, window);
-  const WsLayout L = workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, head_size,
+  const WsLayout L = workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads, head_size,
                                       ext->max_query_len, splits);
   if (ext->workspace_bytes < L.total) return PATTN_ERR_WORKSPACE_TOO_SMALL;
   if (ext->num_seqs == 0 || ext->num_tokens == 0) return PATTN_OK;
@@ -278,6 +281,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.tiles = reinterpret_cast<int2*>(ws + L.tiles_off);
   p.max_tiles = L.max_tiles;
   p.rows_per_item = prefill_rows_per_item(p.G);
+  p.counters = reinterpret_cast<unsigned*>(ws + L.counters_off);
   p.o_part = reinterpret_cast<float*>(ws + L.o_part_off);
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.stream = static_cast<cudaStream_t>(ext->stream);
@@ -289,7 +293,15 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   };
 
   mark(0);
-  if (launch_plan(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  if (ext->max_query_len > 1) {
+    // The plan kernel clears the header and the counters and builds the
+    // prefill work list.
+    if (launch_plan(p) != cudaSuccess) return PATTN_ERR_CUDA;
+  } else {
+    // Decode only: nothing to plan (the decode kernel validates its own
+    // rows); clear the status word and the partition counters.
+    if (cudaMemsetAsync(ws, 0, L.counters_end, p.stream) != cudaSuccess) return PATTN_ERR_CUDA;
+  }
   mark(1);
   mark(2);
 
@@ -323,8 +335,9 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
   mark(5);
+  // The partitions are merged inside the decode kernel (its last CTA of each
+  // request and KV-head group); the combine phase is empty.
   mark(6);
-  if (splits > 1 && launch_combine(p) != cudaSuccess) return PATTN_ERR_CUDA;
   mark(7);
   return PATTN_OK;
 }

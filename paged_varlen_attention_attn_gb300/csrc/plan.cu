@@ -6,7 +6,8 @@
 // seq_lens, validates them, and writes the prefill tiles (request, 128-row
 // query-row item) ordered by their number of key tiles, largest first, so the
 // heaviest tiles start first (longest-processing-time order).  It also clears
-// the status word, so later kernels of the same call report into a clean one.
+// the status word, so later kernels of the same call report into a clean one,
+// and the decode kernel's partition counters.
 #include "common.cuh"
 #include "internal.h"
 
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __shared__ int warp_sums[PLAN_THREADS / 32];
   const int tid = threadIdx.x;
   if (tid == 0) p.hdr->status = 0u;
+  for (int i = tid; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
 

@@ -100,7 +100,8 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   ext.num_splits = num_splits;
   const int splits = pattn_decode_splits(&ext, num_heads, num_kv_heads, block_size, window);
   if (splits < 1) return PATTN_ERR_INVALID_ARGUMENT;
-  const WsLayout L = workspace_layout(num_seqs, num_tokens, num_heads, head_size, 1, splits);
+  const WsLayout L = workspace_layout(num_seqs, num_tokens, num_heads, num_kv_heads, head_size, 1,
+                                      splits);
   if (L.total > kStaticScratchBytes) return PATTN_ERR_WORKSPACE_TOO_SMALL;
 
   void* scratch = nullptr;
@@ -137,18 +138,18 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.tiles = nullptr;
   p.max_tiles = 0;
   p.rows_per_item = prefill_rows_per_item(p.G);
+  p.counters = reinterpret_cast<unsigned*>(ws + L.counters_off);
   p.o_part = reinterpret_cast<float*>(ws + L.o_part_off);
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.stream = static_cast<cudaStream_t>(stream);
 
-  // The status word must start at zero; the partials need no clearing.
-  if (cudaMemsetAsync(&p.hdr->status, 0, sizeof(unsigned), p.stream) != cudaSuccess)
-    return PATTN_ERR_CUDA;
+  // The status word and the partition counters must start at zero; the
+  // partials need no clearing.
+  if (cudaMemsetAsync(ws, 0, L.counters_end, p.stream) != cudaSuccess) return PATTN_ERR_CUDA;
   CUtensorMap dmap;
   if (!encode_decode_map(&dmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
                          num_blocks, decode_heads_per_cta(num_kv_heads, head_size, kv_dtype)))
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
-  if (splits > 1 && launch_combine(p) != cudaSuccess) return PATTN_ERR_CUDA;
   return PATTN_OK;
 }
