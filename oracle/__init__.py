@@ -39,6 +39,13 @@ def bind(path):
     lib.pattn_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.pattn_ref_bf16_to_double.restype = ctypes.c_double
     lib.pattn_ref_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.pattn_ref_e4m3_encode.restype = ctypes.c_uint8
+    lib.pattn_ref_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.pattn_ref_reshape_and_cache.restype = ctypes.c_int
+    lib.pattn_ref_reshape_and_cache.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_float, ctypes.c_float]
     return lib
 
 
@@ -54,7 +61,7 @@ class OracleError(RuntimeError):
 
 
 _ERRORS = {1: "invalid argument", 2: "invalid metadata (q_len > seq_len, "
-           "block id out of range, or token outside every request)",
+           "block id or slot out of range, or token outside every request)",
            3: "out of host memory"}
 
 
@@ -65,6 +72,33 @@ def e4m3_to_double(code: int, lib=None) -> float:
 
 def bf16_to_double(bits: int, lib=None) -> float:
     return (lib or _load()).pattn_ref_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    """Encode one fp32 value as an e4m3 byte with the oracle's own encoder
+    (round to nearest even, saturating at +-448)."""
+    return int((lib or _load()).pattn_ref_e4m3_encode(float(x)))
+
+
+def reshape_and_cache(key_bits, value_bits, kv_cache, slot_mapping, *, num_kv_heads,
+                      head_size, block_size, kv_dtype=0, kv_scale=None, lib=None):
+    """Apply a KV-cache write to a host copy of the cache (numpy, updated in
+    place and returned): bf16 key/value bits [T, Hkv, d], int64 slots [T]
+    (negative: no write).  Raises OracleError for a slot beyond the pool."""
+    lib = lib or _load()
+    key_bits = _c(key_bits, np.uint16)
+    value_bits = _c(value_bits, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    assert kv_cache.flags["C_CONTIGUOUS"]
+    assert kv_cache.dtype == (np.uint16 if kv_dtype == 0 else np.uint8)
+    ks, vs = (1.0, 1.0) if kv_dtype == 0 else (float(kv_scale[0]), float(kv_scale[1]))
+    rc = lib.pattn_ref_reshape_and_cache(
+        key_bits.ctypes.data, value_bits.ctypes.data, kv_cache.ctypes.data, slots.ctypes.data,
+        int(slots.shape[0]), num_kv_heads, head_size, block_size, int(kv_cache.shape[1]),
+        kv_dtype, ks, vs)
+    if rc != 0:
+        raise OracleError(_ERRORS.get(rc, f"error {rc}"))
+    return kv_cache
 
 
 def _c(a, dtype):

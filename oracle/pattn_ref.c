@@ -304,3 +304,85 @@ int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_tab
   for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
   return atomic_load(&jb.error);
 }
+
+/* ------------------------------------------------------------------ cache write */
+
+/*
+ * fp32 -> e4m3 byte (OCP "E4M3FN"), from the format definition: round to the
+ * nearest representable value, ties to the even code (mantissa LSB 0), with
+ * saturation -- magnitudes at or above the largest finite value 448, and
+ * infinities, give +-448 -- and NaN giving the NaN code S.1111.111.  The
+ * finite codes 0x00..0x7E are scanned in order of magnitude (they are
+ * monotonic in it): slow and plain.
+ */
+uint8_t pattn_ref_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  const int sign = signbit(x) ? 1 : 0;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)((sign << 7) | 0x7E);
+  int lo = 0; /* largest code whose magnitude is <= a */
+  for (int c = 0; c <= 0x7E; ++c)
+    if (pattn_ref_e4m3_to_double((uint8_t)c) <= a) lo = c;
+  const double below = a - pattn_ref_e4m3_to_double((uint8_t)lo);
+  const double above = pattn_ref_e4m3_to_double((uint8_t)(lo + 1)) - a;
+  int c;
+  if (below < above)
+    c = lo;
+  else if (above < below)
+    c = lo + 1;
+  else
+    c = (lo & 1) ? lo + 1 : lo;
+  return (uint8_t)((sign << 7) | c);
+}
+
+/*
+ * KV-cache write, the step that fills the cache attention reads ("[vLLM]
+ * FlashAttention", FlashAttentionMetadata.slot_mapping and the PagedAttention
+ * point of its "why this design" list; the cache-write kernel of the DiffKV
+ * backend in "[vLLM] other attention backends").  Token t with slot
+ * s = slot_mapping[t] >= 0 writes its key and value rows of every KV head to
+ * cache[0 or 1][s / bs][s % bs][h][0..d): bf16 bits as they are, or for an
+ * e4m3 cache the byte e4m3(x / scale) of the fp32 quotient (x the bf16 value,
+ * scale the K or V per-tensor scale), rounded as pattn_ref_e4m3_encode does.
+ * A negative slot writes nothing.  A slot at or beyond num_blocks * bs writes
+ * nothing and makes the call return REF_ERR_METADATA.  key and value are bf16
+ * bits [T][Hkv][d]; the cache is updated in place.
+ */
+int pattn_ref_reshape_and_cache(const uint16_t* key, const uint16_t* value, void* kv_cache,
+                                const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                int head_size, int block_size, int num_blocks, int kv_dtype,
+                                float k_scale, float v_scale) {
+  if (!key || !value || !kv_cache || !slot_mapping || num_tokens < 0 || num_kv_heads <= 0 ||
+      head_size <= 0 || block_size <= 0 || num_blocks < 0 || (kv_dtype != 0 && kv_dtype != 1))
+    return REF_ERR_ARG;
+  int err = REF_OK;
+  const int64_t pool = (int64_t)num_blocks * block_size;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    if (s >= pool) {
+      err = REF_ERR_METADATA;
+      continue;
+    }
+    const int64_t blk = s / block_size, slot = s % block_size;
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint16_t* src = kv ? value : key;
+      const float sc = kv ? v_scale : k_scale;
+      for (int h = 0; h < num_kv_heads; ++h)
+        for (int j = 0; j < head_size; ++j) {
+          const uint16_t bits = src[((int64_t)t * num_kv_heads + h) * head_size + j];
+          const int64_t dst =
+              ((((int64_t)kv * num_blocks + blk) * block_size + slot) * num_kv_heads + h) *
+                  head_size + j;
+          if (kv_dtype == 0) {
+            ((uint16_t*)kv_cache)[dst] = bits;
+          } else {
+            const float x = (float)pattn_ref_bf16_to_double(bits);
+            const float q = x / sc;
+            ((uint8_t*)kv_cache)[dst] = pattn_ref_e4m3_encode(q);
+          }
+        }
+    }
+  }
+  return err;
+}
