@@ -440,6 +440,82 @@ def workload_desc(spec, cfg):
 
 # ---------------------------------------------------------------- main
 
+def run_cache_write(args, spec, world, rank, local):
+    """Time pattn_reshape_and_cache on the workload's new tokens: request r's
+    query tokens (positions ctx .. s-1) are written through its block table,
+    key and value bf16 [T, Hkv, d] in, the cache's dtype out.  Algorithmic
+    bytes per call: T * Hkv * d * 2 * (2 bytes read + element size written)."""
+    import torch
+    import paged_varlen_attention_attn_gb300 as pa
+    import workloads as W
+    pa.load()
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    case = W.make_case(spec, device=dev)
+    bt = case.block_table.cpu()
+    slots = []
+    for r, (q, s) in enumerate(zip(spec.q_lens, spec.seq_lens)):
+        k = torch.arange(s - q, s)
+        slots.append(bt[r, k // spec.block_size].to(torch.int64) * spec.block_size
+                     + k % spec.block_size)
+    slots = torch.cat(slots).to(dev)
+    T, Hkv, d = int(slots.numel()), spec.num_kv_heads, spec.head_size
+    g = torch.Generator(device=dev).manual_seed(spec.seed + 7)
+    key = torch.randn(T, Hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    value = torch.randn(T, Hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    es = 1 if spec.kv_dtype else 2
+    nbytes = T * Hkv * d * 2 * (2 + es)
+    stream = torch.cuda.Stream(dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ks = case.kv_scale if spec.kv_dtype else None
+
+    def step():
+        pa.reshape_and_cache(key, value, case.kv_cache, slots, block_size=spec.block_size,
+                             kv_dtype=spec.kv_dtype, kv_scale=ks, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush_w.zero_(); flush_r.sum(); step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush_w.zero_(); flush_r.sum()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms = max_over_ranks(ms, device=dev)
+    pk, pk_src = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    value, _ = aggregate(gbs * (ms / 1e3), ms / 1e3, device=dev)
+    line = {"metric": "kv-cache write (reshape_and_cache) GB/s", "value": round(value, 1),
+            "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, " + ("e4m3" if spec.kv_dtype else "bf16") + " cache",
+            "data": "synthetic (seeded N(0,1) rows, the workload's block tables)",
+            "config": {"workload": f"{T} new tokens of the {spec.name} workload, Hkv {Hkv}, "
+                                   f"d {d}, block {spec.block_size}",
+                       "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "kernel": "reshape_and_cache_kernel", "peak_source": pk_src,
+                         "traffic": None},
+            "gpu_launches": K, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -451,6 +527,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--oracle-rows", type=int, default=None)
+    ap.add_argument("--op", choices=["attention", "cache_write"], default="attention",
+                    help="cache_write: time pattn_reshape_and_cache on the workload's new "
+                         "tokens instead of the attention step")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 400}.get(args.config, 100)
@@ -466,6 +545,8 @@ def main():
 
     import torch
     dist_init("nccl")
+    if args.op == "cache_write":
+        return run_cache_write(args, spec, world, rank, local)
     res = run_ours(args, spec, world, rank, local)
     pk, pk_src = peaks()
     counts = res["counts"]

@@ -199,6 +199,40 @@ pattn_status_t pattn_decode_fwd_static(const void* q, const void* kv_cache,
                                        int max_blocks_per_seq, int num_blocks, int max_seq_len,
                                        int num_splits, void* stream);
 
+/*
+ * pattn_reshape_and_cache -- write new key and value rows into the paged cache.
+ *
+ * The step that fills the cache pattn_varlen_fwd reads ("[vLLM]
+ * FlashAttention", FlashAttentionMetadata.slot_mapping; the cache-write
+ * kernel of the DiffKV backend in "[vLLM] other attention backends").
+ *
+ *   key, value      [device] bf16 [num_tokens, num_kv_heads, head_size],
+ *                   contiguous, 16-B aligned
+ *   kv_cache        [device] the cache of pattn_varlen_fwd, 16-B aligned,
+ *                   updated in place
+ *   slot_mapping    [device] int64 [num_tokens]: token t goes to block
+ *                   slot / block_size, offset slot % block_size; a negative
+ *                   slot writes nothing (padding).  Slots of one call must be
+ *                   distinct (two tokens on one slot leave either's row).
+ *   head_size       a multiple of 8; block_size a multiple of 16
+ *   kv_dtype        bf16: the bits are copied; e4m3: each element x is stored
+ *                   as e4m3(x / scale) (fp32 division, round to nearest even,
+ *                   saturated at +-448, NaN stays NaN), scale = kv_scale[0]
+ *                   for K and kv_scale[1] for V (host floats, > 0, finite)
+ *   device_status   [device] optional (may be NULL): a slot at or beyond
+ *                   num_blocks * block_size writes nothing and ORs
+ *                   PATTN_ERR_BAD_METADATA's device bit (1) into this word
+ *   stream          a cudaStream_t (NULL = legacy default stream)
+ *
+ * Returns PATTN_OK once enqueued; argument errors before any CUDA call;
+ * PATTN_ERR_CUDA if the launch fails.  Allocates nothing, never synchronises.
+ */
+pattn_status_t pattn_reshape_and_cache(const void* key, const void* value, void* kv_cache,
+                                       const int64_t* slot_mapping, int num_tokens,
+                                       int num_kv_heads, int head_size, int block_size,
+                                       int num_blocks, int kv_dtype, const float* kv_scale,
+                                       unsigned* device_status, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* pattn_status_string(int status);
 

@@ -26,7 +26,7 @@ STATUS = {0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARGUMENT", 2: "PATTN_ERR_UNSUPPOR
 
 EXPORTS = ("pattn_varlen_fwd", "pattn_workspace_bytes", "pattn_decode_splits",
            "pattn_read_device_status", "pattn_status_string", "pattn_version",
-           "pattn_decode_fwd_static")
+           "pattn_decode_fwd_static", "pattn_reshape_and_cache")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -82,9 +82,45 @@ def load(path=None):
     lib.pattn_decode_fwd_static.restype = i
     lib.pattn_decode_fwd_static.argtypes = [vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp,
                                             i, i, i, i, i, i, vp]
+    lib.pattn_reshape_and_cache.restype = i
+    lib.pattn_reshape_and_cache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
     if path is None:
         _lib = lib
     return lib
+
+
+def pattn_reshape_and_cache(key, value, kv_cache, slot_mapping, num_tokens, num_kv_heads,
+                            head_size, block_size, num_blocks, kv_dtype, kv_scale,
+                            device_status, stream, lib=None):
+    """Raw call of the KV-cache write with integer device pointers; returns
+    the status code."""
+    lib = lib or load()
+    ks = None
+    if kv_scale is not None:
+        ks = (ctypes.c_float * 2)(float(kv_scale[0]), float(kv_scale[1]))
+    return lib.pattn_reshape_and_cache(key, value, kv_cache, slot_mapping, int(num_tokens),
+                                       int(num_kv_heads), int(head_size), int(block_size),
+                                       int(num_blocks), int(kv_dtype), ks,
+                                       int(device_status) or None, int(stream) or None)
+
+
+def reshape_and_cache(key, value, kv_cache, slot_mapping, *, block_size, kv_dtype=KV_BF16,
+                      kv_scale=None, device_status=None, stream=None):
+    """pattn_reshape_and_cache on torch tensors: key/value bf16 [T, Hkv, d],
+    kv_cache [2, num_blocks, block_size, Hkv, d] (bf16, or uint8 e4m3 codes),
+    slot_mapping int64 [T].  ``device_status``: optional int32/uint32 tensor of
+    one element that collects the out-of-pool bit.  Raises PattnError."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(key.device)
+    st = pattn_reshape_and_cache(key.data_ptr(), value.data_ptr(), kv_cache.data_ptr(),
+                                 slot_mapping.data_ptr(), key.shape[0], key.shape[1],
+                                 key.shape[2], block_size, kv_cache.shape[1], kv_dtype, kv_scale,
+                                 0 if device_status is None else device_status.data_ptr(),
+                                 stream.cuda_stream)
+    if st != 0:
+        raise PattnError(st, "pattn_reshape_and_cache")
+    return kv_cache
 
 
 def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_len,

@@ -134,3 +134,33 @@ def test_status_strings(lib):
 def test_empty_batch_is_a_no_op(lib):
     ext = _ext(num_seqs=0, num_tokens=0, workspace=FAKE, workspace_bytes=1 << 20)
     assert _call(lib, ext) == 0
+
+
+# ------------------------------------------------------------------ cache write
+
+def _cw(lib, **kw):
+    a = dict(key=FAKE, value=FAKE, cache=FAKE, slots=FAKE, T=4, Hkv=2, d=128, bs=16, nb=8,
+             kv_dtype=0, kv_scale=None)
+    a.update(kw)
+    return pa.pattn_reshape_and_cache(a["key"], a["value"], a["cache"], a["slots"], a["T"],
+                                      a["Hkv"], a["d"], a["bs"], a["nb"], a["kv_dtype"],
+                                      a["kv_scale"], 0, 0, lib=lib)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(key=0), 1),                     # NULL key
+    (dict(slots=0), 1),                   # NULL slot mapping
+    (dict(bs=20), 1),                     # block size not a multiple of 16
+    (dict(T=-1), 1),                      # negative token count
+    (dict(d=12), 2),                      # head size not a multiple of 8
+    (dict(kv_dtype=3), 2),                # unknown cache dtype
+    (dict(kv_dtype=1), 1),                # e4m3 without scales
+    (dict(kv_dtype=1, kv_scale=(0.0, 1.0)), 1),
+    (dict(value=FAKE + 8), 1),            # misaligned value pointer
+])
+def test_cache_write_arguments_are_rejected_on_the_host(lib, kw, status):
+    assert _cw(lib, **kw) == status
+
+
+def test_cache_write_of_no_tokens_is_a_no_op(lib):
+    assert _cw(lib, T=0) == 0
