@@ -387,7 +387,7 @@ def oracle_sample(case, spec, max_rows):
         n = (int(sl[r]) + bs - 1) // bs
         bt[r, :n] = torch.tensor([remap[int(b)] for b in bt_full[r, :n]], dtype=torch.int32)
     q = case.q.cpu().view(torch.int16).numpy().view(np.uint16)
-    kvn = kv.view(torch.int16).numpy().view(np.uint16) if spec.kv_dtype == 0 else kv.numpy()
+    kvn = kv.view(torch.int16).numpy().view(np.uint16) if spec.kv_dtype != 1 else kv.numpy()
     sub = type(spec)(**{**spec.__dict__, "q_lens": [spec.q_lens[r] for r in reqs],
                         "seq_lens": [spec.seq_lens[r] for r in reqs]})
     return dict(q=q, kv=kvn, bt=bt.numpy(), sl=sl, qsl=qsl, rows=np.array(rows, np.int32),

@@ -39,6 +39,8 @@ def bind(path):
     lib.pattn_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.pattn_ref_bf16_to_double.restype = ctypes.c_double
     lib.pattn_ref_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.pattn_ref_f16_to_double.restype = ctypes.c_double
+    lib.pattn_ref_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.pattn_ref_e4m3_encode.restype = ctypes.c_uint8
     lib.pattn_ref_e4m3_encode.argtypes = [ctypes.c_float]
     lib.pattn_ref_reshape_and_cache.restype = ctypes.c_int
@@ -70,6 +72,11 @@ def e4m3_to_double(code: int, lib=None) -> float:
     return (lib or _load()).pattn_ref_e4m3_to_double(int(code) & 0xFF)
 
 
+def f16_to_double(bits: int, lib=None) -> float:
+    """Decode one IEEE binary16 pattern with the oracle's own decoder."""
+    return (lib or _load()).pattn_ref_f16_to_double(int(bits) & 0xFFFF)
+
+
 def bf16_to_double(bits: int, lib=None) -> float:
     return (lib or _load()).pattn_ref_bf16_to_double(int(bits) & 0xFFFF)
 
@@ -90,8 +97,8 @@ def reshape_and_cache(key_bits, value_bits, kv_cache, slot_mapping, *, num_kv_he
     value_bits = _c(value_bits, np.uint16)
     slots = _c(slot_mapping, np.int64)
     assert kv_cache.flags["C_CONTIGUOUS"]
-    assert kv_cache.dtype == (np.uint16 if kv_dtype == 0 else np.uint8)
-    ks, vs = (1.0, 1.0) if kv_dtype == 0 else (float(kv_scale[0]), float(kv_scale[1]))
+    assert kv_cache.dtype == (np.uint8 if kv_dtype == 1 else np.uint16)
+    ks, vs = (float(kv_scale[0]), float(kv_scale[1])) if kv_dtype == 1 else (1.0, 1.0)
     rc = lib.pattn_ref_reshape_and_cache(
         key_bits.ctypes.data, value_bits.ctypes.data, kv_cache.ctypes.data, slots.ctypes.data,
         int(slots.shape[0]), num_kv_heads, head_size, block_size, int(kv_cache.shape[1]),
@@ -121,7 +128,7 @@ def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
     """
     lib = lib or _load()
     q_bits = _c(q_bits, np.uint16)
-    kv = _c(kv_cache, np.uint16 if kv_dtype == 0 else np.uint8)
+    kv = _c(kv_cache, np.uint8 if kv_dtype == 1 else np.uint16)
     bt = _c(block_table, np.int32)
     if bt.ndim != 2:
         raise ValueError("block_table must be 2-D")

@@ -61,6 +61,22 @@ double pattn_ref_bf16_to_double(uint16_t b) {
   return (double)f;
 }
 
+/* IEEE binary16 -> double, from the format definition: sign, 5 exponent bits
+ * with bias 15, 10 mantissa bits; exponent 0 holds subnormals (m * 2^-24),
+ * exponent 31 infinities (m = 0) and NaNs. */
+double pattn_ref_f16_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1F;
+  const int m = h & 0x3FF;
+  double mag;
+  if (e == 0x1F) return m ? NAN : (sign ? -INFINITY : INFINITY);
+  if (e == 0)
+    mag = ldexp((double)m, -24);
+  else
+    mag = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  return sign ? -mag : mag;
+}
+
 /* e4m3 (OCP "E4M3FN") -> double, from the format definition. */
 double pattn_ref_e4m3_to_double(uint8_t b) {
   int sign = (b >> 7) & 1;
@@ -102,6 +118,7 @@ static double cache_elem(const job_t* jb, int kv_index, int block, int slot, int
   int64_t idx = ((((int64_t)kv_index * jb->num_blocks + block) * jb->block_size + slot) *
                      jb->num_kv_heads + g) * jb->head_size + j;
   if (jb->kv_dtype == 0) return pattn_ref_bf16_to_double(((const uint16_t*)jb->kv)[idx]);
+  if (jb->kv_dtype == 2) return pattn_ref_f16_to_double(((const uint16_t*)jb->kv)[idx]);
   return pattn_ref_e4m3_to_double(((const uint8_t*)jb->kv)[idx]) *
          (kv_index == 0 ? jb->k_scale : jb->v_scale);
 }
@@ -168,7 +185,10 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
   int ctx = s - q_len, i = t - jb->qsl[r], p = ctx + i;
   int g = h / (jb->num_heads / jb->num_kv_heads);
   for (int j = 0; j < d; ++j)
-    qv[j] = pattn_ref_bf16_to_double(jb->q[((int64_t)t * jb->num_heads + h) * d + j]);
+  {
+    const uint16_t bits = jb->q[((int64_t)t * jb->num_heads + h) * d + j];
+    qv[j] = jb->kv_dtype == 2 ? pattn_ref_f16_to_double(bits) : pattn_ref_bf16_to_double(bits);
+  }
   double* o = jb->out + row * d;
 
   if (jb->num_splits <= 1) {
@@ -241,7 +261,8 @@ static void* worker(void* arg) {
  * Attention for an explicit list of (token, head) rows.
  *   q          bf16 bits [num_tokens][num_heads][head_size]
  *   kv_cache   [2][num_blocks][block_size][num_kv_heads][head_size],
- *              bf16 bits (kv_dtype 0) or e4m3 bytes (kv_dtype 1)
+ *              bf16 bits (kv_dtype 0), e4m3 bytes (kv_dtype 1) or f16 bits
+ *              (kv_dtype 2, where q is f16 too; else q is bf16)
  *   kv_scale   {k_scale, v_scale}; read only for kv_dtype 1
  *   out        [n_rows][head_size] doubles, lse [n_rows] doubles
  * Returns 0, or REF_ERR_* (bad arguments, metadata, or memory).
@@ -256,7 +277,7 @@ int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_tab
   if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !out || !lse)
     return REF_ERR_ARG;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size <= 0 ||
-      block_size <= 0 || num_seqs < 0 || (kv_dtype != 0 && kv_dtype != 1) ||
+      block_size <= 0 || num_seqs < 0 || kv_dtype < 0 || kv_dtype > 2 ||
       (kv_dtype == 1 && !kv_scale))
     return REF_ERR_ARG;
   if (n_rows == 0) return REF_OK;
@@ -353,7 +374,7 @@ int pattn_ref_reshape_and_cache(const uint16_t* key, const uint16_t* value, void
                                 int head_size, int block_size, int num_blocks, int kv_dtype,
                                 float k_scale, float v_scale) {
   if (!key || !value || !kv_cache || !slot_mapping || num_tokens < 0 || num_kv_heads <= 0 ||
-      head_size <= 0 || block_size <= 0 || num_blocks < 0 || (kv_dtype != 0 && kv_dtype != 1))
+      head_size <= 0 || block_size <= 0 || num_blocks < 0 || kv_dtype < 0 || kv_dtype > 2)
     return REF_ERR_ARG;
   int err = REF_OK;
   const int64_t pool = (int64_t)num_blocks * block_size;
@@ -374,7 +395,7 @@ int pattn_ref_reshape_and_cache(const uint16_t* key, const uint16_t* value, void
           const int64_t dst =
               ((((int64_t)kv * num_blocks + blk) * block_size + slot) * num_kv_heads + h) *
                   head_size + j;
-          if (kv_dtype == 0) {
+          if (kv_dtype != 1) {  /* 16-bit cache: the bits as they are */
             ((uint16_t*)kv_cache)[dst] = bits;
           } else {
             const float x = (float)pattn_ref_bf16_to_double(bits);

@@ -18,12 +18,15 @@ def to_f64_q(q):
     return q.detach().cpu().to(torch.float32).to(torch.float64).numpy()
 
 
+def _as16(kv, kv_dtype):
+    want = torch.float16 if kv_dtype == 2 else torch.bfloat16
+    return kv if kv.dtype == want else kv.view(want)
+
+
 def to_f64_kv(kv, kv_dtype, kv_scale):
     kv = kv.detach().cpu()
-    if kv_dtype == 0:
-        if kv.dtype != torch.bfloat16:
-            kv = kv.view(torch.bfloat16)
-        return kv.to(torch.float32).to(torch.float64).numpy()
+    if kv_dtype in (0, 2):
+        return _as16(kv, kv_dtype).to(torch.float32).to(torch.float64).numpy()
     x = kv.view(torch.float8_e4m3fn).to(torch.float32).to(torch.float64).numpy()
     x = x.copy()
     x[0] *= float(kv_scale[0])

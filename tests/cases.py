@@ -46,7 +46,7 @@ def host_arrays(case):
     """(q bits, kv bits/bytes, block_table, seq_lens, qsl) as numpy arrays."""
     q = case.q.detach().cpu().view(torch.int16).numpy().view(np.uint16)
     kv = case.kv_cache.detach().cpu()
-    if case.spec.kv_dtype == W.KV_BF16:
+    if case.spec.kv_dtype in (W.KV_BF16, W.KV_F16):
         kv = kv.view(torch.int16).numpy().view(np.uint16)
     else:
         kv = kv.numpy()

@@ -29,6 +29,7 @@ import torch
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_F16 = 2  # f16 cache, and q / out in f16 too
 E4M3_MAX = 448.0
 
 
@@ -84,6 +85,18 @@ class Case:
         return max(self.spec.seq_lens) if self.spec.seq_lens else 0
 
 
+def _randn_f16(shape, gen, device, chunk_elems=1 << 28):
+    """N(0,1) drawn in fp32 chunk by chunk and rounded to f16."""
+    out = torch.empty(shape, dtype=torch.float16, device=device)
+    flat = out.view(-1)
+    n = flat.numel()
+    for s in range(0, n, chunk_elems):
+        e = min(n, s + chunk_elems)
+        flat[s:e] = torch.randn(e - s, generator=gen, device=device,
+                                dtype=torch.float32).to(torch.float16)
+    return out
+
+
 def _randn_bf16(shape, gen, device, chunk_elems=1 << 28):
     """N(0,1) drawn in fp32 chunk by chunk and rounded to bf16."""
     out = torch.empty(shape, dtype=torch.bfloat16, device=device)
@@ -132,7 +145,10 @@ def make_case(spec: CaseSpec, device="cpu") -> Case:
     H, Hkv, d = spec.num_heads, spec.num_kv_heads, spec.head_size
     q = _randn_bf16((T, H, d), gen, device)
     kv_scale = (1.0, 1.0)
-    if spec.kv_dtype == KV_BF16:
+    if spec.kv_dtype == KV_F16:
+        q = _randn_f16((T, H, d), gen, device)
+        kv = _randn_f16((2, pool, bs, Hkv, d), gen, device)
+    elif spec.kv_dtype == KV_BF16:
         kv = _randn_bf16((2, pool, bs, Hkv, d), gen, device)
     else:
         k, ks = _randn_e4m3((pool, bs, Hkv, d), gen, device)
