@@ -62,7 +62,10 @@ typedef enum {
 
 typedef enum {
   PATTN_KV_BF16 = 0,      /* K and V stored as bf16                          */
-  PATTN_KV_FP8_E4M3 = 1   /* K and V stored as e4m3 bytes, one fp32 scale each */
+  PATTN_KV_FP8_E4M3 = 1,  /* K and V stored as e4m3 bytes, one fp32 scale each */
+  PATTN_KV_F16 = 2        /* K and V stored as f16; q and out are f16 too (the
+                             FlashAttention backend supports float16 and
+                             bfloat16 models)                                 */
 } pattn_kv_dtype_t;
 
 /*
@@ -98,13 +101,15 @@ typedef struct {
  * pattn_varlen_fwd -- the forward pass.
  *
  *   q               [device] bf16 [num_tokens, num_heads, head_size], contiguous
+ *                   (f16 when kv_dtype is PATTN_KV_F16)
  *   kv_cache        [device] [2, num_blocks, block_size, num_kv_heads, head_size],
  *                   contiguous, bf16 or e4m3 bytes per kv_dtype; 16-B aligned
  *   block_table     [device] int32 [num_seqs, max_blocks_per_seq]; entries past
  *                   ceil(seq_len / block_size) are never read
  *   seq_lens        [device] int32 [num_seqs]
  *   query_start_loc [device] int32 [num_seqs + 1], non-decreasing prefix sum
- *   out             [device] bf16 [num_tokens, num_heads, head_size]; rows of
+ *   out             [device] bf16 (f16 with PATTN_KV_F16) [num_tokens, num_heads,
+ *                   head_size]; rows of
  *                   tokens outside [query_start_loc[0], query_start_loc[B]) are
  *                   left untouched
  *   scale           multiplies q . k; finite and >= 0
@@ -114,7 +119,8 @@ typedef struct {
  *   block_size      a multiple of 16 (the ValueError of get_kv_cache_shape)
  *   window          <= 0: no window; > 0: keys with p - k < window are visible
  *   causal          1: k <= p; 0: every key < seq_len (then window must be <= 0)
- *   kv_dtype        a pattn_kv_dtype_t
+ *   kv_dtype        a pattn_kv_dtype_t.  e4m3 runs decode rows only
+ *                   (a batch with max_query_len > 1 returns UNSUPPORTED)
  *   kv_scale        host float[2] {k_scale, v_scale}; required for e4m3, ignored
  *                   for bf16 (may be NULL)
  *   ext             host sizes, workspace and stream (see pattn_ext_t)

@@ -18,6 +18,7 @@ from . import _build
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_F16 = 2  # f16 cache; q and out are f16 too
 MAX_SPLITS = 64
 
 STATUS = {0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARGUMENT", 2: "PATTN_ERR_UNSUPPORTED",
@@ -228,7 +229,8 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
     dev = q.device
     T = q.shape[0]
     if out is None:
-        out = torch.empty((T, num_heads, head_size), dtype=torch.bfloat16, device=dev)
+        odt = torch.float16 if kv_dtype == KV_F16 else torch.bfloat16
+        out = torch.empty((T, num_heads, head_size), dtype=odt, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     ext = make_ext(num_seqs=seq_lens.shape[0], num_tokens=T,

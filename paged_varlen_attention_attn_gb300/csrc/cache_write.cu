@@ -78,7 +78,8 @@ extern "C" pattn_status_t pattn_reshape_and_cache(const void* key, const void* v
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PATTN_ERR_INVALID_ARGUMENT;
   if (block_size <= 0 || block_size % 16 != 0) return PATTN_ERR_INVALID_ARGUMENT;
   if (head_size <= 0 || head_size % 8 != 0) return PATTN_ERR_UNSUPPORTED;
-  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3 && kv_dtype != PATTN_KV_F16)
+    return PATTN_ERR_UNSUPPORTED;
   if (kv_dtype == PATTN_KV_FP8_E4M3 &&
       (!kv_scale || !(kv_scale[0] > 0.f) || !(kv_scale[1] > 0.f) || !(kv_scale[0] < INFINITY) ||
        !(kv_scale[1] < INFINITY)))
@@ -89,7 +90,8 @@ extern "C" pattn_status_t pattn_reshape_and_cache(const void* key, const void* v
   if (num_tokens == 0) return PATTN_OK;
   const long long n = static_cast<long long>(num_tokens) * 2 * num_kv_heads * (head_size / 8);
   const unsigned grid = static_cast<unsigned>((n + CW_THREADS - 1) / CW_THREADS);
-  const float ks = kv_dtype ? kv_scale[0] : 1.f, vs = kv_dtype ? kv_scale[1] : 1.f;
+  const bool fp8 = kv_dtype == PATTN_KV_FP8_E4M3;
+  const float ks = fp8 ? kv_scale[0] : 1.f, vs = fp8 ? kv_scale[1] : 1.f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const auto* k = static_cast<const __nv_bfloat16*>(key);
   const auto* v = static_cast<const __nv_bfloat16*>(value);

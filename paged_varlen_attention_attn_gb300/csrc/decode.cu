@@ -27,6 +27,7 @@
 // fragments are widened to f16 in registers with integer operations (exact:
 // every e4m3 value times 2^-8 is an f16 value); the per-tensor scales (times
 // 2^8) are folded into the softmax scale (K) and the final normalisation (V).
+#include "../../include/pattn.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -132,7 +133,7 @@ __device__ __forceinline__ void load_v_bytes(const unsigned char* sv, int hh, in
 // warp reductions, and the loads of all partitions and all NH rows are
 // independent, so the merge costs a few memory round trips, not S * NH of
 // them.  The partials were written by other CTAs: they are read past L1.
-template <int D, int NH>
+template <int D, int NH, bool HALF>
 __device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h, int t0, int lane) {
   const int S = p.splits;
   constexpr int PER = D / 32;
@@ -175,15 +176,17 @@ __device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h,
   }
 #pragma unroll
   for (int k = 0; k < NH; ++k) {
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(t0) * p.H + h + k) * D + lane * PER;
+    const int64_t o0 = (static_cast<int64_t>(t0) * p.H + h + k) * D + lane * PER;
 #pragma unroll
     for (int e = 0; e < PER; e += 2)
-      *reinterpret_cast<__nv_bfloat162*>(out + e) =
-          __floats2bfloat162_rn(acc[k][e] * inv[k], acc[k][e + 1] * inv[k]);
+      *(static_cast<unsigned*>(p.out) + (o0 + e) / 2) =
+          pack2<HALF>(acc[k][e] * inv[k], acc[k][e + 1] * inv[k]);
   }
 }
 
-template <int D, bool FP8, int NT, int HG, int WPH>
+// HALF: q, a 16-bit cache and out are f16 (else bf16; an e4m3 cache goes with
+// bf16 q and out).
+template <int D, bool FP8, int NT, int HG, int WPH, bool HALF>
 __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH > 1 ? 2 : 1)
     decode_split_kernel(const Problem p, const __grid_constant__ CUtensorMap kvmap, float sl2,
                         float out_scale) {
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         ldsm_x4(sk_a + raw_off<D, FP8, HG>(hh, s_row, 2 * kk + s_csel), a0, a1, a2, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          mma_16816<false>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+          mma_16816<HALF>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
       }
     }
 
@@ -460,8 +463,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
         l_run[nt][h2] = l_run[nt][h2] * alpha[nt][h2] + ps;
       }
-      pk_lo[nt] = pack2<FP8>(x[0], x[1]);  // key quad,     heads 2*c4, 2*c4+1
-      pk_hi[nt] = pack2<FP8>(x[2], x[3]);  // key quad + 8, heads 2*c4, 2*c4+1
+      pk_lo[nt] = pack2<FP8 || HALF>(x[0], x[1]);  // key quad,     heads 2*c4, 2*c4+1
+      pk_hi[nt] = pack2<FP8 || HALF>(x[2], x[3]);  // key quad + 8, heads 2*c4, 2*c4+1
     }
     if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         unsigned a0, a1, a2, a3;
         ldsm_x4_t(sv_a + raw_off<D, FP8, HG>(hh, v_row, 2 * m + v_csel), a0, a1, a2, a3);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816<false>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816<HALF>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
       }
     }
     // Release the stage once every lane of every consumer warp has read it.
@@ -604,8 +607,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         const int d = FP8 ? (quad * (D / 8) + 2 * m + (e >> 1)) : (16 * m + quad + ((e & 2) ? 8 : 0));
         const float val = o[m][nt][e] * inv;
         if (S == 1) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-          out[(static_cast<int64_t>(t0) * p.H + h0 + head) * D + d] = __float2bfloat16_rn(val);
+          const int64_t oi = (static_cast<int64_t>(t0) * p.H + h0 + head) * D + d;
+          if constexpr (HALF)
+            static_cast<__half*>(p.out)[oi] = __float2half_rn(val);
+          else
+            static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(val);
         } else {
           const int64_t prow = (static_cast<int64_t>(r) * p.H + h0 + head) * S + sp;
           p.o_part[prow * D + d] = val;
@@ -644,17 +650,18 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     const int nq = HG * G, h_first = grp * HG * G;
     if (nq % 2 == 0) {
       for (int hq = 2 * warp; hq < nq; hq += 2 * C::NW)
-        merge_partitions<D, 2>(p, r, h_first + hq, t0, lane);
+        merge_partitions<D, 2, HALF>(p, r, h_first + hq, t0, lane);
     } else {
-      for (int hq = warp; hq < nq; hq += C::NW) merge_partitions<D, 1>(p, r, h_first + hq, t0, lane);
+      for (int hq = warp; hq < nq; hq += C::NW)
+        merge_partitions<D, 1, HALF>(p, r, h_first + hq, t0, lane);
     }
   }
 }
 
-template <int D, bool FP8, int NT, int HG, int WPH>
+template <int D, bool FP8, int NT, int HG, int WPH, bool HALF>
 cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
   using C = DecodeCfg<D, FP8, NT, HG, WPH>;
-  auto kern = decode_split_kernel<D, FP8, NT, HG, WPH>;
+  auto kern = decode_split_kernel<D, FP8, NT, HG, WPH, HALF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // e4m3 data is widened to f16 as value * 2^-8; the 2^8 goes into the scales.
@@ -668,31 +675,36 @@ cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
 
 // Up to 8 query heads per KV head (one head tile): two warps per KV head
 // share each partition; more: one warp per KV head, two head tiles.
-template <int D, bool FP8, int HG>
+template <int D, bool FP8, int HG, bool HALF>
 cudaError_t launch_decode_g(const Problem& p, const CUtensorMap& kvmap) {
-  return (p.G <= 8) ? launch_decode_t<D, FP8, 1, HG, 2>(p, kvmap)
-                    : launch_decode_t<D, FP8, 2, HG, 1>(p, kvmap);
+  return (p.G <= 8) ? launch_decode_t<D, FP8, 1, HG, 2, HALF>(p, kvmap)
+                    : launch_decode_t<D, FP8, 2, HG, 1, HALF>(p, kvmap);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool HALF>
 cudaError_t launch_decode_hg(const Problem& p, const CUtensorMap& kvmap) {
   switch (decode_head_group(p.Hkv, D, FP8)) {
-    case 4: return launch_decode_g<D, FP8, 4>(p, kvmap);
-    case 2: return launch_decode_g<D, FP8, 2>(p, kvmap);
-    default: return launch_decode_g<D, FP8, 1>(p, kvmap);
+    case 4: return launch_decode_g<D, FP8, 4, HALF>(p, kvmap);
+    case 2: return launch_decode_g<D, FP8, 2, HALF>(p, kvmap);
+    default: return launch_decode_g<D, FP8, 1, HALF>(p, kvmap);
   }
+}
+
+template <int D>
+cudaError_t launch_decode_d(const Problem& p, const CUtensorMap& kvmap) {
+  if (p.kv_dtype == PATTN_KV_FP8_E4M3) return launch_decode_hg<D, true, false>(p, kvmap);
+  if (p.kv_dtype == PATTN_KV_F16) return launch_decode_hg<D, false, true>(p, kvmap);
+  return launch_decode_hg<D, false, false>(p, kvmap);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const Problem& p, const CUtensorMap& kvmap) {
-  if (p.D == 128)
-    return p.kv_dtype ? launch_decode_hg<128, true>(p, kvmap) : launch_decode_hg<128, false>(p, kvmap);
-  return p.kv_dtype ? launch_decode_hg<64, true>(p, kvmap) : launch_decode_hg<64, false>(p, kvmap);
+  return (p.D == 128) ? launch_decode_d<128>(p, kvmap) : launch_decode_d<64>(p, kvmap);
 }
 
 int decode_heads_per_cta(int Hkv, int D, int kv_dtype) {
-  return decode_head_group(Hkv, D, kv_dtype != 0);  // kv_dtype 1: e4m3
+  return decode_head_group(Hkv, D, kv_dtype == PATTN_KV_FP8_E4M3);
 }
 
 }  // namespace pattn

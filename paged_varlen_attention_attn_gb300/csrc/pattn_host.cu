@@ -108,7 +108,11 @@ bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, 
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle sw =
       (fp8 && D == 64) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  return enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+  return enc(map,
+             fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                 : (kv_dtype == PATTN_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
+             4,
              const_cast<void*>(kv_cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -135,7 +139,9 @@ bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int
                         static_cast<cuuint64_t>(D / 64), 2ull * static_cast<cuuint64_t>(NB)};
   cuuint64_t strides[4] = {row * Hkv, row, 128, row * Hkv * bs};
   cuuint32_t box[5] = {64, 16, static_cast<cuuint32_t>(heads), static_cast<cuuint32_t>(D / 64), 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv_cache), dims, strides,
+  return enc(map,
+             kv_dtype == PATTN_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             5, const_cast<void*>(kv_cache), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -224,7 +230,8 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
     return PATTN_ERR_INVALID_ARGUMENT;
   if (!(scale >= 0.f) || std::isinf(scale)) return PATTN_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return PATTN_ERR_INVALID_ARGUMENT;
-  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3 && kv_dtype != PATTN_KV_F16)
+    return PATTN_ERR_UNSUPPORTED;
   if (kv_dtype == PATTN_KV_FP8_E4M3) {
     if (!kv_scale || !(kv_scale[0] > 0.f) || !(kv_scale[1] > 0.f) || std::isinf(kv_scale[0]) ||
         std::isinf(kv_scale[1]))
@@ -267,8 +274,8 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.window = window;
   p.causal = causal;
   p.kv_dtype = kv_dtype;
-  p.k_scale = kv_dtype ? kv_scale[0] : 1.f;
-  p.v_scale = kv_dtype ? kv_scale[1] : 1.f;
+  p.k_scale = (kv_dtype == PATTN_KV_FP8_E4M3) ? kv_scale[0] : 1.f;
+  p.v_scale = (kv_dtype == PATTN_KV_FP8_E4M3) ? kv_scale[1] : 1.f;
   p.B = ext->num_seqs;
   p.T = ext->num_tokens;
   p.mbps = ext->max_blocks_per_seq;
@@ -317,7 +324,9 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
       cuuint64_t strides[2] = {head_size * es, static_cast<cuuint64_t>(num_heads) * head_size * es};
       cuuint32_t box[3] = {64, 1, BLOCK_M};
       cuuint32_t estr[3] = {1, 1, 1};
-      if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+      const CUtensorMapDataType qt = (kv_dtype == PATTN_KV_F16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      if (enc(&qmap, qt, 3, const_cast<void*>(q), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PATTN_ERR_CUDA;

@@ -45,6 +45,7 @@
 // running max moves lazily: O is rescaled only when a row max grows by more
 // than 2^8, which stays exact because the final normalisation divides by the
 // sum taken against the same reference max.
+#include "../../include/pattn.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -133,7 +134,8 @@ __device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) 
       : "f"(a0), "f"(a1));
 }
 
-template <int D>
+// HALF: q, the cache and out are f16 (else bf16).
+template <int D, bool HALF>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const Problem p, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kvmap, float sl2) {
@@ -289,8 +291,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_union > 0) {
-      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, true, false);
-      constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, true, true);
+      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !HALF, false);
+      constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, !HALF, true);
       // Base descriptors; a byte offset o moves the start address field by
       // o >> 4 (shared addresses stay far below the field's 256 KB range).
       const uint64_t q_d = smem_desc_sw128(smem_u32(sQ), 16, 1024);
@@ -466,8 +468,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           a3 = fast_exp2(a3);
           fadd2(ps0, ps1, a0, a1);
           fadd2(ps2, ps3, a2, a3);
-          pk[e / 2] = pack2<false>(a0, a1);
-          pk[e / 2 + 1] = pack2<false>(a2, a3);
+          pk[e / 2] = pack2<HALF>(a0, a1);
+          pk[e / 2 + 1] = pack2<HALF>(a2, a3);
         }
         tc_st16u(s_t + 64 + q / 2, pk);
       }
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (i < q_len) {
           unsigned pkd[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pkd[e] = pack2<false>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
+          for (int e = 0; e < 16; ++e) pkd[e] = pack2<HALF>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
             *reinterpret_cast<uint4*>(orow + q * 32 + e * 2) =
@@ -536,10 +538,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
 int prefill_rows_per_item(int G) { return (G % 2 == 0) ? BLOCK_M : 2 * BLOCK_M; }
 
-template <int D>
+template <int D, bool HALF>
 cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
                              unsigned grid) {
-  auto k = prefill_kernel<D>;
+  auto k = prefill_kernel<D, HALF>;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, k);
   if (e != cudaSuccess) return e;
@@ -561,8 +563,12 @@ cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUt
   const int NP = (p.G % 2 == 0) ? p.H / 2 : p.H;
   const long long grid = static_cast<long long>(p.max_tiles) * NP;
   if (grid == 0) return cudaSuccess;
-  return p.D == 128 ? launch_prefill_t<128>(p, q_map, kv_map, static_cast<unsigned>(grid))
-                    : launch_prefill_t<64>(p, q_map, kv_map, static_cast<unsigned>(grid));
+  const unsigned g = static_cast<unsigned>(grid);
+  if (p.kv_dtype == PATTN_KV_F16)
+    return p.D == 128 ? launch_prefill_t<128, true>(p, q_map, kv_map, g)
+                      : launch_prefill_t<64, true>(p, q_map, kv_map, g);
+  return p.D == 128 ? launch_prefill_t<128, false>(p, q_map, kv_map, g)
+                    : launch_prefill_t<64, false>(p, q_map, kv_map, g);
 }
 
 }  // namespace pattn

@@ -75,7 +75,8 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   if (num_heads / num_kv_heads > 16) return PATTN_ERR_UNSUPPORTED;
   if (!(scale >= 0.f) || std::isinf(scale)) return PATTN_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return PATTN_ERR_INVALID_ARGUMENT;
-  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3 && kv_dtype != PATTN_KV_F16)
+    return PATTN_ERR_UNSUPPORTED;
   if (kv_dtype == PATTN_KV_FP8_E4M3 &&
       (!kv_scale || !(kv_scale[0] > 0.f) || !(kv_scale[1] > 0.f) || std::isinf(kv_scale[0]) ||
        std::isinf(kv_scale[1])))
@@ -125,8 +126,8 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.window = window;
   p.causal = causal;
   p.kv_dtype = kv_dtype;
-  p.k_scale = kv_dtype ? kv_scale[0] : 1.f;
-  p.v_scale = kv_dtype ? kv_scale[1] : 1.f;
+  p.k_scale = (kv_dtype == PATTN_KV_FP8_E4M3) ? kv_scale[0] : 1.f;
+  p.v_scale = (kv_dtype == PATTN_KV_FP8_E4M3) ? kv_scale[1] : 1.f;
   p.B = num_seqs;
   p.T = num_tokens;
   p.mbps = max_blocks_per_seq;
