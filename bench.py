@@ -236,7 +236,7 @@ def call_args(case):
     return dict(scale=case.scale, num_heads=s.num_heads, num_kv_heads=s.num_kv_heads,
                 head_size=s.head_size, block_size=s.block_size, window=s.window,
                 causal=s.causal, kv_dtype=s.kv_dtype,
-                kv_scale=case.kv_scale if s.kv_dtype else None,
+                kv_scale=case.kv_scale if s.kv_dtype == 1 else None,
                 max_query_len=case.max_query_len, max_seq_len=case.max_seq_len,
                 num_splits=s.num_splits)
 
@@ -435,7 +435,7 @@ def workload_desc(spec, cfg):
             f"seq_len {min(spec.seq_lens)}..{max(spec.seq_lens)}, "
             f"H {spec.num_heads}, Hkv {spec.num_kv_heads}, d {spec.head_size}, "
             f"block {spec.block_size}, window {spec.window}, "
-            f"kv {'e4m3' if spec.kv_dtype else 'bf16'}")
+            f"kv {['bf16', 'e4m3', 'f16'][spec.kv_dtype]}")
 
 
 # ---------------------------------------------------------------- main
@@ -463,12 +463,12 @@ def run_cache_write(args, spec, world, rank, local):
     g = torch.Generator(device=dev).manual_seed(spec.seed + 7)
     key = torch.randn(T, Hkv, d, generator=g, device=dev).to(torch.bfloat16)
     value = torch.randn(T, Hkv, d, generator=g, device=dev).to(torch.bfloat16)
-    es = 1 if spec.kv_dtype else 2
+    es = 1 if spec.kv_dtype == 1 else 2
     nbytes = T * Hkv * d * 2 * (2 + es)
     stream = torch.cuda.Stream(dev)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    ks = case.kv_scale if spec.kv_dtype else None
+    ks = case.kv_scale if spec.kv_dtype == 1 else None
 
     def step():
         pa.reshape_and_cache(key, value, case.kv_cache, slots, block_size=spec.block_size,
@@ -502,7 +502,7 @@ def run_cache_write(args, spec, world, rank, local):
     line = {"metric": "kv-cache write (reshape_and_cache) GB/s", "value": round(value, 1),
             "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 in, " + ("e4m3" if spec.kv_dtype else "bf16") + " cache",
+            "vs_baseline": None, "dtype": ("f16 in, f16" if spec.kv_dtype == 2 else "bf16 in, " + ("e4m3" if spec.kv_dtype else "bf16")) + " cache",
             "data": "synthetic (seeded N(0,1) rows, the workload's block tables)",
             "config": {"workload": f"{T} new tokens of the {spec.name} workload, Hkv {Hkv}, "
                                    f"d {d}, block {spec.block_size}",
@@ -527,6 +527,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--oracle-rows", type=int, default=None)
+    ap.add_argument("--f16", action="store_true",
+                    help="run the workload with f16 q, cache and output (16-bit workloads only)")
     ap.add_argument("--op", choices=["attention", "cache_write"], default="attention",
                     help="cache_write: time pattn_reshape_and_cache on the workload's new "
                          "tokens instead of the attention step")
@@ -536,8 +538,13 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
 
+    import dataclasses
     import workloads as W
     spec = W.config_spec(args.config)
+    if args.f16:
+        if spec.kv_dtype != W.KV_BF16:
+            raise SystemExit("--f16 needs a 16-bit workload")
+        spec = dataclasses.replace(spec, kv_dtype=W.KV_F16, name=spec.name + "_f16")
     world, rank, local = dist_info()
 
     if args.impl == "reference":
@@ -577,7 +584,8 @@ def main():
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
-        "e4m3 KV, bf16 Q/out, fp32 accumulate" if spec.kv_dtype else "bf16 (fp32 accumulate)",
+        {0: "bf16 (fp32 accumulate)", 1: "e4m3 KV, bf16 Q/out, fp32 accumulate",
+         2: "f16 (fp32 accumulate)"}[spec.kv_dtype],
         "data": "synthetic (seeded N(0,1), seeded block permutation)",
         "config": {"workload": workload_desc(spec, args.config), "config_index": args.config,
                    "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
