@@ -206,6 +206,42 @@ pattn_status_t pattn_decode_fwd_static(const void* q, const void* kv_cache,
                                        int num_splits, void* stream);
 
 /*
+ * pattn_cascade_fwd -- pattn_varlen_fwd for a batch whose requests all start
+ * with the same cached prefix ("[vLLM] FlashAttention", Cascade Attention;
+ * FlashAttentionMetadata.use_cascade / common_prefix_len).
+ *
+ * The prefix's attention is computed once for every query token of the batch
+ * (one request of num_tokens queries over common_prefix_len keys, not causal:
+ * every query sits after the prefix), each request's suffix (its keys past
+ * the prefix) separately and causally, and the two are merged by
+ * log-sum-exp.  The result is pattn_varlen_fwd's up to rounding; the prefix's
+ * K/V pages are read once for the batch instead of once per request.
+ *
+ * Arguments are pattn_varlen_fwd's, plus common_prefix_len: a positive
+ * multiple of block_size, at most max_seq_len.  The first
+ * common_prefix_len / block_size block-table entries of every request must
+ * name the same blocks (the pass reads row 0's), and every request's cached
+ * context (seq_len - query_len) must cover the prefix; a request whose
+ * context does not is reported as bad metadata (its rows are finite but
+ * unspecified).  causal must be 1 and window <= 0; e4m3 caches are not
+ * supported (PATTN_ERR_UNSUPPORTED).  The workspace comes from
+ * pattn_cascade_workspace_bytes: besides the two passes' own scratch it holds
+ * their fp32 partial results, 2 * num_tokens * num_heads * (head_size + 1)
+ * floats.  The status word is read with pattn_read_device_status as usual.
+ */
+pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 const int32_t* query_start_loc, void* out, float scale,
+                                 int num_heads, int num_kv_heads, int head_size,
+                                 int block_size, int window, int causal, int kv_dtype,
+                                 const float* kv_scale, int common_prefix_len,
+                                 const pattn_ext_t* ext);
+
+/* Workspace bytes pattn_cascade_fwd needs (0 if the arguments are invalid). */
+size_t pattn_cascade_workspace_bytes(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
+                                     int head_size, int block_size, int common_prefix_len);
+
+/*
  * pattn_reshape_and_cache -- write new key and value rows into the paged cache.
  *
  * The step that fills the cache pattn_varlen_fwd reads ("[vLLM]

@@ -27,7 +27,8 @@ STATUS = {0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARGUMENT", 2: "PATTN_ERR_UNSUPPOR
 
 EXPORTS = ("pattn_varlen_fwd", "pattn_workspace_bytes", "pattn_decode_splits",
            "pattn_read_device_status", "pattn_status_string", "pattn_version",
-           "pattn_decode_fwd_static", "pattn_reshape_and_cache")
+           "pattn_decode_fwd_static", "pattn_reshape_and_cache", "pattn_cascade_fwd",
+           "pattn_cascade_workspace_bytes")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -83,6 +84,11 @@ def load(path=None):
     lib.pattn_decode_fwd_static.restype = i
     lib.pattn_decode_fwd_static.argtypes = [vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp,
                                             i, i, i, i, i, i, vp]
+    lib.pattn_cascade_fwd.restype = i
+    lib.pattn_cascade_fwd.argtypes = [vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp, i,
+                                      ctypes.POINTER(Ext)]
+    lib.pattn_cascade_workspace_bytes.restype = ctypes.c_size_t
+    lib.pattn_cascade_workspace_bytes.argtypes = [ctypes.POINTER(Ext), i, i, i, i, i]
     lib.pattn_reshape_and_cache.restype = i
     lib.pattn_reshape_and_cache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
     if path is None:
@@ -122,6 +128,54 @@ def reshape_and_cache(key, value, kv_cache, slot_mapping, *, block_size, kv_dtyp
     if st != 0:
         raise PattnError(st, "pattn_reshape_and_cache")
     return kv_cache
+
+
+def pattn_cascade_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size,
+                                  common_prefix_len, lib=None):
+    lib = lib or load()
+    return lib.pattn_cascade_workspace_bytes(ctypes.byref(ext), int(num_heads), int(num_kv_heads),
+                                             int(head_size), int(block_size),
+                                             int(common_prefix_len))
+
+
+def cascade_forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_heads,
+                    num_kv_heads, head_size, block_size, common_prefix_len, window=0, causal=1,
+                    kv_dtype=KV_BF16, kv_scale=None, max_query_len, max_seq_len, num_splits=0,
+                    out=None, workspace=None, stream=None):
+    """pattn_cascade_fwd on torch tensors: pattn_varlen_fwd for a batch whose
+    requests share their first common_prefix_len keys (same blocks).
+    Returns ``out``; raises PattnError."""
+    import torch
+    dev = q.device
+    T = q.shape[0]
+    if out is None:
+        odt = torch.float16 if kv_dtype == KV_F16 else torch.bfloat16
+        out = torch.empty((T, num_heads, head_size), dtype=odt, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    ext = make_ext(num_seqs=seq_lens.shape[0], num_tokens=T,
+                   max_blocks_per_seq=block_table.shape[1], num_blocks=kv_cache.shape[1],
+                   max_query_len=max_query_len, max_seq_len=max_seq_len,
+                   num_splits=num_splits, stream=stream.cuda_stream)
+    need = pattn_cascade_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size,
+                                         common_prefix_len)
+    if need == 0:
+        raise PattnError(1, "pattn_cascade_workspace_bytes")
+    ws = (workspace or _default_ws).get(need, dev)
+    ext.workspace = ws.data_ptr()
+    ext.workspace_bytes = ws.numel()
+    ks = None
+    if kv_scale is not None:
+        ks = (ctypes.c_float * 2)(float(kv_scale[0]), float(kv_scale[1]))
+    st = load().pattn_cascade_fwd(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
+                                  seq_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(),
+                                  float(scale), int(num_heads), int(num_kv_heads), int(head_size),
+                                  int(block_size), int(window), int(causal), int(kv_dtype), ks,
+                                  int(common_prefix_len), ctypes.byref(ext))
+    if st != 0:
+        raise PattnError(st, "pattn_cascade_fwd")
+    forward.last_ext = ext
+    return out
 
 
 def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_len,

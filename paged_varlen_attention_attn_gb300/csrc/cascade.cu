@@ -1,0 +1,100 @@
+// cascade.cu -- cascade attention: a common prefix attended once (sm_103a).
+//
+// "[vLLM] FlashAttention", Cascade Attention (and the use_cascade /
+// common_prefix_len fields of FlashAttentionMetadata): when every request of
+// a batch starts with the same cached prefix, the prefix attention is
+// computed once for all query tokens of the batch -- one request of
+// num_tokens queries over common_prefix_len keys, not causal, because every
+// query sits after the prefix -- and each request's own suffix (its keys
+// past the prefix, causal) separately; the two partial results are merged
+// by log-sum-exp.  The result equals plain attention over the whole
+// sequence; the prefix's K/V pages are read once for the batch instead of
+// once per request.
+//
+// This file holds the two small kernels around the passes (which reuse the
+// prefill and decode kernels in their partial-result mode): the set-up of
+// the passes' metadata and the final merge.
+#include "../../include/pattn.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace pattn {
+namespace {
+
+// One CTA: clears the status word, then writes the prefix pass's metadata
+// (one request spanning every query token, seq_len = prefix) and each
+// request's suffix length.  A suffix shorter than its query (the request's
+// cached context does not cover the prefix) is caught as bad metadata by the
+// suffix pass's own checks.
+__global__ void __launch_bounds__(256)
+    cascade_setup_kernel(WsHeader* hdr, const int* qsl, const int* seq_lens, int B, int prefix,
+                         int* pre_qsl, int* pre_sl, int* suf_sl) {
+  if (threadIdx.x == 0) {
+    hdr->status = 0u;
+    pre_qsl[0] = qsl[0];
+    pre_qsl[1] = qsl[B];
+    pre_sl[0] = prefix;
+  }
+  for (int r = threadIdx.x; r < B; r += blockDim.x) suf_sl[r] = seq_lens[r] - prefix;
+}
+
+// One warp per (token, head) row of the batch: out = (2^(a - M) o_a +
+// 2^(b - M) o_b) / (2^(a - M) + 2^(b - M)), a and b the passes' log2-domain
+// lse, M = max(a, b); a pass that saw no key (lse = -inf) weighs 0.  Rows of
+// tokens outside [qsl[0], qsl[B]) are left untouched.
+template <int D, bool HALF>
+__global__ void __launch_bounds__(256)
+    cascade_merge_kernel(const float* o_a, const float* lse_a, const float* o_b,
+                         const float* lse_b, void* out, const int* qsl, int B, int T, int H) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<int64_t>(T) * H) return;
+  const int t = static_cast<int>(row / H);
+  if (t < qsl[0] || t >= qsl[B]) return;
+  const float a = lse_a[row], b = lse_b[row];
+  const float M = fmaxf(a, b);
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  const float wa = (a == -INFINITY) ? 0.f : exp2f(a - Mu);
+  const float wb = (b == -INFINITY) ? 0.f : exp2f(b - Mu);
+  const float inv = (wa + wb > 0.f) ? 1.f / (wa + wb) : 0.f;
+  constexpr int PER = D / 32;
+  const int64_t e0 = row * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2) {
+    const float x0 = (wa * o_a[e0 + e] + wb * o_b[e0 + e]) * inv;
+    const float x1 = (wa * o_a[e0 + e + 1] + wb * o_b[e0 + e + 1]) * inv;
+    *(static_cast<unsigned*>(out) + (e0 + e) / 2) = pack2<HALF>(x0, x1);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cascade_setup(WsHeader* hdr, const int* qsl, const int* seq_lens, int B,
+                                 int prefix, int* pre_qsl, int* pre_sl, int* suf_sl,
+                                 cudaStream_t stream) {
+  cascade_setup_kernel<<<1, 256, 0, stream>>>(hdr, qsl, seq_lens, B, prefix, pre_qsl, pre_sl,
+                                             suf_sl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, const float* o_b,
+                                 const float* lse_b, void* out, const int* qsl, int B, int T,
+                                 int H, int D, bool half, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(T) * H;
+  if (rows == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  if (D == 128) {
+    if (half)
+      cascade_merge_kernel<128, true><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+    else
+      cascade_merge_kernel<128, false><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+  } else {
+    if (half)
+      cascade_merge_kernel<64, true><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+    else
+      cascade_merge_kernel<64, false><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pattn

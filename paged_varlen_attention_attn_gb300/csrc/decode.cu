@@ -137,7 +137,7 @@ template <int D, int NH, bool HALF>
 __device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h, int t0, int lane) {
   const int S = p.splits;
   constexpr int PER = D / 32;
-  float w0[NH], w1[NH], inv[NH], acc[NH][PER];
+  float w0[NH], w1[NH], inv[NH], acc[NH][PER], Mx[NH];
 #pragma unroll
   for (int k = 0; k < NH; ++k) {
     const int64_t prow = (static_cast<int64_t>(r) * p.H + h + k) * S;
@@ -150,6 +150,7 @@ __device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h,
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = (M == -INFINITY) ? 0.f : M;
+    Mx[k] = Mu;
     w0[k] = (w0[k] == -INFINITY) ? 0.f : exp2f(w0[k] - Mu);
     w1[k] = (w1[k] == -INFINITY) ? 0.f : exp2f(w1[k] - Mu);
     float L = w0[k] + w1[k];
@@ -177,10 +178,16 @@ __device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h,
 #pragma unroll
   for (int k = 0; k < NH; ++k) {
     const int64_t o0 = (static_cast<int64_t>(t0) * p.H + h + k) * D + lane * PER;
+    if (p.o32) {
 #pragma unroll
-    for (int e = 0; e < PER; e += 2)
-      *(static_cast<unsigned*>(p.out) + (o0 + e) / 2) =
-          pack2<HALF>(acc[k][e] * inv[k], acc[k][e + 1] * inv[k]);
+      for (int e = 0; e < PER; ++e) p.o32[o0 + e] = acc[k][e] * inv[k];
+      if (lane == 0) p.lse32[o0 / D] = (inv[k] > 0.f) ? Mx[k] - __log2f(inv[k]) : -INFINITY;
+    } else {
+#pragma unroll
+      for (int e = 0; e < PER; e += 2)
+        *(static_cast<unsigned*>(p.out) + (o0 + e) / 2) =
+            pack2<HALF>(acc[k][e] * inv[k], acc[k][e + 1] * inv[k]);
+    }
   }
 }
 
@@ -218,8 +225,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
       if (threadIdx.x == 0) flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
       const int64_t a = static_cast<int64_t>(max(0, t0)) * p.H * D;
       const int64_t b = static_cast<int64_t>(min(p.T, t0 + max(q_len, 0))) * p.H * D;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-      for (int64_t e = a + threadIdx.x; e < b; e += blockDim.x) out[e] = __float2bfloat16_rn(0.f);
+      if (p.o32) {
+        for (int64_t e = a + threadIdx.x; e < b; e += blockDim.x) p.o32[e] = 0.f;
+        for (int64_t e = a / D + threadIdx.x; e < b / D; e += blockDim.x) p.lse32[e] = -INFINITY;
+      } else {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+        for (int64_t e = a + threadIdx.x; e < b; e += blockDim.x) out[e] = __float2bfloat16_rn(0.f);
+      }
     }
     return;
   }
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     // issues one tensor copy for K and one for V per unit (16 keys of all HG
     // heads) as soon as the consumers release the stage.
     if (lane == 0) tma_prefetch_desc(&kvmap);
-    const int* bt = p.block_table + static_cast<int64_t>(r) * p.mbps;
+    const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
     bool ok = true;
     for (int base = 0; ok && base < n_units; base += 32) {
       const int gu = base + lane;
@@ -608,7 +620,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         const float val = o[m][nt][e] * inv;
         if (S == 1) {
           const int64_t oi = (static_cast<int64_t>(t0) * p.H + h0 + head) * D + d;
-          if constexpr (HALF)
+          if (p.o32) {
+            p.o32[oi] = val;
+            if (m == 0 && quad == 0 && (e & 2) == 0)
+              p.lse32[oi / D] = (L > 0.f) ? M + __log2f(L) : -INFINITY;
+          } else if constexpr (HALF)
             static_cast<__half*>(p.out)[oi] = __float2half_rn(val);
           else
             static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(val);

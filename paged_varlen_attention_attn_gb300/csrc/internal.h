@@ -31,6 +31,17 @@ struct Problem {
   int bs_shift;  // log2(bs) when bs is a power of two, else -1
   float k_scale, v_scale;
   int B, T, mbps, NB, max_q, max_s, splits;
+  int bt_stride;     // row stride of block_table (>= mbps; the cascade suffix
+                     // pass starts rows past the shared prefix)
+  int clear_status;  // the plan kernel clears the status word (else an earlier
+                     // kernel of the same call did)
+  int long_queries;  // a request may have more queries than keys (the cascade
+                     // prefix pass: every token of the batch over the prefix,
+                     // not causal); otherwise that is bad metadata
+  // Partial-result mode (cascade passes): when set, rows are written as
+  // normalised fp32 o [T][H][D] and lse [T][H] (log2 units) instead of out.
+  float* o32;
+  float* lse32;
   // workspace views
   WsHeader* hdr;
   int2* tiles;       // (request, row-item) pairs sorted by cost, descending
@@ -70,6 +81,15 @@ bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int
 // KV heads one decode CTA serves (4, 2 or 1: the largest dividing Hkv whose
 // 16-key K + V unit fits in 16 KB).
 int decode_heads_per_cta(int Hkv, int D, int kv_dtype);
+
+// Cascade attention: the metadata set-up before the two passes, and the
+// log-sum-exp merge of their partial results into out.
+cudaError_t launch_cascade_setup(WsHeader* hdr, const int* qsl, const int* seq_lens, int B,
+                                 int prefix, int* pre_qsl, int* pre_sl, int* suf_sl,
+                                 cudaStream_t stream);
+cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, const float* o_b,
+                                 const float* lse_b, void* out, const int* qsl, int B, int T,
+                                 int H, int D, bool half, cudaStream_t stream);
 
 // Query rows one prefill CTA covers: two heads x 128 rows when the GQA group
 // size is even, else one head x 256 rows.

@@ -77,6 +77,9 @@ int choose_splits(const pattn_ext_t* ext, int num_kv_heads, int block_size, int 
 }
 
 pattn_status_t validate(const pattn_ext_t* ext, int num_heads, int num_kv_heads, int head_size,
+                        int block_size);
+
+pattn_status_t validate(const pattn_ext_t* ext, int num_heads, int num_kv_heads, int head_size,
                         int block_size) {
   if (!ext_ok(ext)) return PATTN_ERR_INVALID_ARGUMENT;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
@@ -90,6 +93,140 @@ pattn_status_t validate(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
   if (num_heads / num_kv_heads > 16) return PATTN_ERR_UNSUPPORTED;
   return PATTN_OK;
 }
+
+// Argument checks shared by pattn_varlen_fwd and pattn_cascade_fwd (host
+// only, before any CUDA call).
+pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* block_table,
+                          const int32_t* seq_lens, const int32_t* query_start_loc, void* out,
+                          float scale, int num_heads, int num_kv_heads, int head_size,
+                          int block_size, int window, int causal, int kv_dtype,
+                          const float* kv_scale, const pattn_ext_t* ext) {
+  pattn_status_t v = validate(ext, num_heads, num_kv_heads, head_size, block_size);
+  if (v != PATTN_OK) return v;
+  if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !out || !ext->workspace)
+    return PATTN_ERR_INVALID_ARGUMENT;
+  if (!(scale >= 0.f) || std::isinf(scale)) return PATTN_ERR_INVALID_ARGUMENT;
+  if (causal != 0 && causal != 1) return PATTN_ERR_INVALID_ARGUMENT;
+  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3 && kv_dtype != PATTN_KV_F16)
+    return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype == PATTN_KV_FP8_E4M3) {
+    if (!kv_scale || !(kv_scale[0] > 0.f) || !(kv_scale[1] > 0.f) || std::isinf(kv_scale[0]) ||
+        std::isinf(kv_scale[1]))
+      return PATTN_ERR_INVALID_ARGUMENT;
+  }
+  if (!causal && window > 0) return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype == PATTN_KV_FP8_E4M3 && ext->max_query_len > 1) return PATTN_ERR_UNSUPPORTED;
+  // Prefill key tiles are 128 keys: a page must divide the tile or be a whole
+  // number of tiles.
+  if (ext->max_query_len > 1 && !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
+    return PATTN_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(kv_cache) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15) ||
+      (reinterpret_cast<uintptr_t>(ext->workspace) & 255))
+    return PATTN_ERR_INVALID_ARGUMENT;
+  return PATTN_OK;
+}
+
+// The fields of a Problem every pass shares.
+void base_problem(Problem& p, const void* q, const void* kv_cache, void* out, float scale,
+                  int num_heads, int num_kv_heads, int head_size, int block_size, int kv_dtype,
+                  const float* kv_scale, const pattn_ext_t* ext) {
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.kv = kv_cache;
+  p.out = out;
+  p.scale = scale;
+  p.H = num_heads;
+  p.Hkv = num_kv_heads;
+  p.G = num_heads / num_kv_heads;
+  p.D = head_size;
+  p.bs = block_size;
+  p.bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(block_size)) : -1;
+  p.kv_dtype = kv_dtype;
+  p.k_scale = (kv_dtype == PATTN_KV_FP8_E4M3) ? kv_scale[0] : 1.f;
+  p.v_scale = (kv_dtype == PATTN_KV_FP8_E4M3) ? kv_scale[1] : 1.f;
+  p.T = ext->num_tokens;
+  p.NB = ext->num_blocks;
+  p.rows_per_item = prefill_rows_per_item(p.G);
+  p.stream = static_cast<cudaStream_t>(ext->stream);
+}
+
+// TMA tensor map over q [T][H][D] with 128-row x 64-element boxes.
+bool encode_q_map(CUtensorMap* map, const void* q, int kv_dtype, int H, int D, int T) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t es = 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {D * es, static_cast<cuuint64_t>(H) * D * es};
+  cuuint32_t box[3] = {64, 1, BLOCK_M};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType qt = (kv_dtype == PATTN_KV_F16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(map, qt, 3, const_cast<void*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The prefill kernel (when the pass has rows with query_len > 1), then the
+// decode kernel, for one pass.
+pattn_status_t launch_pass(const Problem& p) {
+  if (p.max_q > 1) {
+    CUtensorMap qmap, kvmap;
+    if (!encode_q_map(&qmap, p.q, p.kv_dtype, p.H, p.D, p.T)) return PATTN_ERR_CUDA;
+    if (!encode_kv_map(&kvmap, p.kv, p.kv_dtype, p.D, p.Hkv, p.bs, p.NB, std::min(p.bs, BLOCK_N)))
+      return PATTN_ERR_CUDA;
+    if (launch_prefill(p, qmap, kvmap) != cudaSuccess) return PATTN_ERR_CUDA;
+  }
+  CUtensorMap dmap;
+  if (!encode_decode_map(&dmap, p.kv, p.kv_dtype, p.D, p.Hkv, p.bs, p.NB,
+                         decode_heads_per_cta(p.Hkv, p.D, p.kv_dtype)))
+    return PATTN_ERR_CUDA;
+  if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
+  return PATTN_OK;
+}
+
+// Workspace of a cascade call: the suffix pass's layout (its header holds the
+// call's status word), the prefix pass's, the two passes' fp32 partial
+// results, and the passes' metadata (prefix qsl[2] and seq_len, suffix
+// seq_lens[B]).
+struct CascadeLayout {
+  WsLayout suf, pre;
+  int splits_suf, splits_pre;
+  size_t pre_off, o_pre, lse_pre, o_suf, lse_suf, meta, total;
+};
+
+CascadeLayout cascade_layout(const pattn_ext_t* ext, int H, int Hkv, int D, int bs, int prefix) {
+  CascadeLayout c;
+  pattn_ext_t es = *ext;
+  es.max_seq_len = std::max(1, ext->max_seq_len - prefix);
+  pattn_ext_t ep = *ext;
+  ep.num_seqs = 1;
+  ep.max_query_len = ext->num_tokens;
+  ep.max_seq_len = prefix;
+  c.splits_suf = choose_splits(&es, Hkv, bs, 0);
+  c.splits_pre = choose_splits(&ep, Hkv, bs, 0);
+  c.suf = workspace_layout(ext->num_seqs, ext->num_tokens, H, Hkv, D, ext->max_query_len,
+                           c.splits_suf);
+  c.pre = workspace_layout(1, ext->num_tokens, H, Hkv, D, ext->num_tokens, c.splits_pre);
+  const size_t rows = static_cast<size_t>(ext->num_tokens) * H;
+  size_t off = align_up(c.suf.total, 256);
+  c.pre_off = off;
+  off = align_up(off + c.pre.total, 256);
+  c.o_pre = off;
+  off = align_up(off + rows * D * sizeof(float), 256);
+  c.lse_pre = off;
+  off = align_up(off + rows * sizeof(float), 256);
+  c.o_suf = off;
+  off = align_up(off + rows * D * sizeof(float), 256);
+  c.lse_suf = off;
+  off = align_up(off + rows * sizeof(float), 256);
+  c.meta = off;
+  off = align_up(off + (3 + static_cast<size_t>(ext->num_seqs)) * sizeof(int), 256);
+  c.total = off;
+  return c;
+}
+
 
 }  // namespace
 
@@ -224,30 +361,11 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
                                 void* out, float scale, int num_heads, int num_kv_heads,
                                 int head_size, int block_size, int window, int causal,
                                 int kv_dtype, const float* kv_scale, const pattn_ext_t* ext) {
-  pattn_status_t v = validate(ext, num_heads, num_kv_heads, head_size, block_size);
+  pattn_status_t v = check_call(q, kv_cache, block_table, seq_lens, query_start_loc, out, scale,
+                                num_heads, num_kv_heads, head_size, block_size, window, causal,
+                                kv_dtype, kv_scale, ext);
   if (v != PATTN_OK) return v;
-  if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !out || !ext->workspace)
-    return PATTN_ERR_INVALID_ARGUMENT;
-  if (!(scale >= 0.f) || std::isinf(scale)) return PATTN_ERR_INVALID_ARGUMENT;
-  if (causal != 0 && causal != 1) return PATTN_ERR_INVALID_ARGUMENT;
-  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_FP8_E4M3 && kv_dtype != PATTN_KV_F16)
-    return PATTN_ERR_UNSUPPORTED;
-  if (kv_dtype == PATTN_KV_FP8_E4M3) {
-    if (!kv_scale || !(kv_scale[0] > 0.f) || !(kv_scale[1] > 0.f) || std::isinf(kv_scale[0]) ||
-        std::isinf(kv_scale[1]))
-      return PATTN_ERR_INVALID_ARGUMENT;
-  }
-  if (!causal && window > 0) return PATTN_ERR_UNSUPPORTED;
   if (window < 0) window = 0;
-  if (kv_dtype == PATTN_KV_FP8_E4M3 && ext->max_query_len > 1) return PATTN_ERR_UNSUPPORTED;
-  // Prefill key tiles are 128 keys: a page must divide the tile or be a whole
-  // number of tiles.
-  if (ext->max_query_len > 1 && !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
-    return PATTN_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(kv_cache) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
-      (reinterpret_cast<uintptr_t>(out) & 15) ||
-      (reinterpret_cast<uintptr_t>(ext->workspace) & 255))
-    return PATTN_ERR_INVALID_ARGUMENT;
 
   const int splits = choose_splits(ext, num_kv_heads, block_size, window);
   const WsLayout L = workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads, head_size,
@@ -279,6 +397,10 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.B = ext->num_seqs;
   p.T = ext->num_tokens;
   p.mbps = ext->max_blocks_per_seq;
+  p.bt_stride = p.mbps;
+  p.clear_status = 1;
+  p.o32 = nullptr;
+  p.lse32 = nullptr;
   p.NB = ext->num_blocks;
   p.max_q = ext->max_query_len;
   p.max_s = ext->max_seq_len;
@@ -313,24 +435,9 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   mark(2);
 
   if (ext->max_query_len > 1) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return PATTN_ERR_CUDA;
     CUtensorMap qmap, kvmap;
-    const cuuint64_t es = 2;
-    {
-      cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_size),
-                            static_cast<cuuint64_t>(num_heads),
-                            static_cast<cuuint64_t>(ext->num_tokens)};
-      cuuint64_t strides[2] = {head_size * es, static_cast<cuuint64_t>(num_heads) * head_size * es};
-      cuuint32_t box[3] = {64, 1, BLOCK_M};
-      cuuint32_t estr[3] = {1, 1, 1};
-      const CUtensorMapDataType qt = (kv_dtype == PATTN_KV_F16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-      if (enc(&qmap, qt, 3, const_cast<void*>(q), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return PATTN_ERR_CUDA;
-    }
+    if (!encode_q_map(&qmap, q, kv_dtype, num_heads, head_size, ext->num_tokens))
+      return PATTN_ERR_CUDA;
     if (!encode_kv_map(&kvmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
                        ext->num_blocks, std::min(block_size, BLOCK_N)))
       return PATTN_ERR_CUDA;
@@ -348,6 +455,119 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   // request and KV-head group); the combine phase is empty.
   mark(6);
   mark(7);
+  return PATTN_OK;
+}
+
+size_t pattn_cascade_workspace_bytes(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
+                                     int head_size, int block_size, int common_prefix_len) {
+  if (validate(ext, num_heads, num_kv_heads, head_size, block_size) != PATTN_OK) return 0;
+  if (common_prefix_len <= 0 || common_prefix_len % block_size != 0) return 0;
+  return cascade_layout(ext, num_heads, num_kv_heads, head_size, block_size, common_prefix_len).total;
+}
+
+pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
+                                 const int32_t* seq_lens, const int32_t* query_start_loc,
+                                 void* out, float scale, int num_heads, int num_kv_heads,
+                                 int head_size, int block_size, int window, int causal,
+                                 int kv_dtype, const float* kv_scale, int common_prefix_len,
+                                 const pattn_ext_t* ext) {
+  pattn_status_t v = check_call(q, kv_cache, block_table, seq_lens, query_start_loc, out, scale,
+                                num_heads, num_kv_heads, head_size, block_size, window, causal,
+                                kv_dtype, kv_scale, ext);
+  if (v != PATTN_OK) return v;
+  const int P = common_prefix_len;
+  if (P <= 0 || P % block_size != 0) return PATTN_ERR_INVALID_ARGUMENT;
+  if (causal != 1 || window > 0) return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype == PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;  // the prefix pass is a prefill
+  // The prefix pass is one request of every query token: its 128-key tiles
+  // need the same page rule as any prefill.
+  if (!(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0)) return PATTN_ERR_UNSUPPORTED;
+  if (P > ext->max_seq_len || P / block_size > ext->max_blocks_per_seq)
+    return PATTN_ERR_INVALID_ARGUMENT;
+  const CascadeLayout c = cascade_layout(ext, num_heads, num_kv_heads, head_size, block_size, P);
+  if (ext->workspace_bytes < c.total) return PATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (ext->num_seqs == 0 || ext->num_tokens == 0) return PATTN_OK;
+  if (ext->num_blocks == 0) return PATTN_ERR_INVALID_ARGUMENT;
+
+  unsigned char* ws = static_cast<unsigned char*>(ext->workspace);
+  int* pre_qsl = reinterpret_cast<int*>(ws + c.meta);
+  int* pre_sl = pre_qsl + 2;
+  int* suf_sl = pre_qsl + 3;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+
+  // Prefix pass: one request spanning every query token, over the first
+  // P / block_size entries of block-table row 0 (the same blocks in every
+  // row), not causal.  It reports into the call's status word.
+  Problem pre;
+  base_problem(pre, q, kv_cache, out, scale, num_heads, num_kv_heads, head_size, block_size,
+               kv_dtype, kv_scale, ext);
+  pre.block_table = block_table;
+  pre.seq_lens = pre_sl;
+  pre.qsl = pre_qsl;
+  pre.window = 0;
+  pre.causal = 0;
+  pre.B = 1;
+  pre.mbps = P / block_size;
+  pre.bt_stride = ext->max_blocks_per_seq;
+  pre.max_q = ext->num_tokens;
+  pre.max_s = P;
+  pre.splits = c.splits_pre;
+  pre.hdr = hdr;
+  pre.clear_status = 0;
+  pre.long_queries = 1;
+  pre.tiles = reinterpret_cast<int2*>(ws + c.pre_off + c.pre.tiles_off);
+  pre.max_tiles = c.pre.max_tiles;
+  pre.counters = reinterpret_cast<unsigned*>(ws + c.pre_off + c.pre.counters_off);
+  pre.o_part = reinterpret_cast<float*>(ws + c.pre_off + c.pre.o_part_off);
+  pre.lse_part = reinterpret_cast<float*>(ws + c.pre_off + c.pre.lse_off);
+  pre.o32 = reinterpret_cast<float*>(ws + c.o_pre);
+  pre.lse32 = reinterpret_cast<float*>(ws + c.lse_pre);
+
+  // Suffix pass: every request over its own keys past the prefix, causal
+  // (positions relative to the prefix's end), block-table rows shifted by the
+  // prefix's blocks.
+  Problem suf;
+  base_problem(suf, q, kv_cache, out, scale, num_heads, num_kv_heads, head_size, block_size,
+               kv_dtype, kv_scale, ext);
+  suf.block_table = block_table + P / block_size;
+  suf.seq_lens = suf_sl;
+  suf.qsl = query_start_loc;
+  suf.window = 0;
+  suf.causal = 1;
+  suf.B = ext->num_seqs;
+  suf.mbps = ext->max_blocks_per_seq - P / block_size;
+  suf.bt_stride = ext->max_blocks_per_seq;
+  suf.max_q = ext->max_query_len;
+  suf.max_s = std::max(1, ext->max_seq_len - P);
+  suf.splits = c.splits_suf;
+  suf.hdr = hdr;
+  suf.clear_status = 0;
+  suf.tiles = reinterpret_cast<int2*>(ws + c.suf.tiles_off);
+  suf.max_tiles = c.suf.max_tiles;
+  suf.counters = reinterpret_cast<unsigned*>(ws + c.suf.counters_off);
+  suf.o_part = reinterpret_cast<float*>(ws + c.suf.o_part_off);
+  suf.lse_part = reinterpret_cast<float*>(ws + c.suf.lse_off);
+  suf.o32 = reinterpret_cast<float*>(ws + c.o_suf);
+  suf.lse32 = reinterpret_cast<float*>(ws + c.lse_suf);
+
+  cudaStream_t st = static_cast<cudaStream_t>(ext->stream);
+  if (launch_cascade_setup(hdr, query_start_loc, seq_lens, ext->num_seqs, P, pre_qsl, pre_sl,
+                           suf_sl, st) != cudaSuccess)
+    return PATTN_ERR_CUDA;
+  for (Problem* p : {&pre, &suf}) {
+    if (p->max_q > 1) {
+      if (launch_plan(*p) != cudaSuccess) return PATTN_ERR_CUDA;
+    } else if (cudaMemsetAsync(p->counters, 0, static_cast<size_t>(p->B) * p->Hkv * sizeof(unsigned),
+                               st) != cudaSuccess) {
+      return PATTN_ERR_CUDA;
+    }
+    v = launch_pass(*p);
+    if (v != PATTN_OK) return v;
+  }
+  if (launch_cascade_merge(pre.o32, pre.lse32, suf.o32, suf.lse32, out, query_start_loc,
+                           ext->num_seqs, ext->num_tokens, num_heads, head_size,
+                           kv_dtype == PATTN_KV_F16, st) != cudaSuccess)
+    return PATTN_ERR_CUDA;
   return PATTN_OK;
 }
 

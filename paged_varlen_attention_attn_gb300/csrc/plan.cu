@@ -21,7 +21,8 @@ __device__ __forceinline__ bool request_ok(const Problem& p, int r, int& q_len, 
   t0 = p.qsl[r];
   q_len = p.qsl[r + 1] - t0;
   s = p.seq_lens[r];
-  return q_len >= 0 && q_len <= s && s <= p.mbps * p.bs && t0 >= 0 && t0 + q_len <= p.T;
+  return q_len >= 0 && (q_len <= s || p.long_queries) && s <= p.mbps * p.bs && t0 >= 0 &&
+         t0 + q_len <= p.T;
 }
 
 __device__ __forceinline__ int tile_cost(const Problem& p, int q_len, int s, int qt) {
@@ -38,7 +39,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __shared__ int hist[NBUCKET];
   __shared__ int warp_sums[PLAN_THREADS / 32];
   const int tid = threadIdx.x;
-  if (tid == 0) p.hdr->status = 0u;
+  if (tid == 0 && p.clear_status) p.hdr->status = 0u;
   for (int i = tid; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
@@ -52,9 +53,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
       // handled by the decode kernel), clamped to the output buffer.
       if (q_len > 1) {
         const int a = max(0, t0), b = min(p.T, t0 + q_len);
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-        for (int64_t e = static_cast<int64_t>(a) * p.H * p.D; e < static_cast<int64_t>(b) * p.H * p.D; ++e)
-          out[e] = __float2bfloat16_rn(0.f);
+        const int64_t e0 = static_cast<int64_t>(a) * p.H * p.D, e1 = static_cast<int64_t>(b) * p.H * p.D;
+        if (p.o32) {
+          for (int64_t e = e0; e < e1; ++e) p.o32[e] = 0.f;
+          for (int64_t e = static_cast<int64_t>(a) * p.H; e < static_cast<int64_t>(b) * p.H; ++e)
+            p.lse32[e] = -INFINITY;
+        } else {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+          for (int64_t e = e0; e < e1; ++e) out[e] = __float2bfloat16_rn(0.f);
+        }
       }
       continue;
     }

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         t0 + u.i0);
         }
       }
-      const int* bt = p.block_table + static_cast<int64_t>(r) * p.mbps;
+      const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
       // block id of page `lane` of key tile kt (0 when that page is past seq_len)
       auto page_block = [&](int kt) {
         const int key0 = kt * BLOCK_N + lane * rows_box;
@@ -500,8 +500,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                          (static_cast<int64_t>(t0 + i) * p.H + u.h) * D;
+    // The normalised row goes to out, or (partial-result mode) to o32 in
+    // fp32 with its log2-domain lse = m + log2(l).
+    const int64_t ri = static_cast<int64_t>(t0 + i) * p.H + u.h;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + ri * D;
     if (u.valid && ok && nt > 0 &&
         __all_sync(FULL, mbar_wait(&bars->o_final[X], 0, status, abort_flag))) {
       tc_fence_after();
@@ -512,17 +514,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_ld32(o_t + q * 32, ov);
         tc_wait_ld();
         if (i < q_len) {
-          unsigned pkd[16];
+          if (p.o32) {
+            float4* dst = reinterpret_cast<float4*>(p.o32 + ri * D + q * 32);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pkd[e] = pack2<HALF>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
+            for (int e = 0; e < 32; e += 4)
+              dst[e / 4] = make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
+          } else {
+            unsigned pkd[16];
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<uint4*>(orow + q * 32 + e * 2) =
-                make_uint4(pkd[e], pkd[e + 1], pkd[e + 2], pkd[e + 3]);
+            for (int e = 0; e < 16; ++e) pkd[e] = pack2<HALF>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<uint4*>(orow + q * 32 + e * 2) =
+                  make_uint4(pkd[e], pkd[e + 1], pkd[e + 2], pkd[e + 3]);
+          }
         }
       }
+      if (p.o32 && i < q_len) p.lse32[ri] = (l_run > 0.f) ? m_run + __log2f(l_run) : -INFINITY;
     } else if (u.valid && i < q_len) {
-      for (int e = 0; e < D; ++e) orow[e] = __float2bfloat16_rn(0.f);
+      if (p.o32) {
+        for (int e = 0; e < D; ++e) p.o32[ri * D + e] = 0.f;
+        p.lse32[ri] = -INFINITY;
+      } else {
+        for (int e = 0; e < D; ++e) orow[e] = __float2bfloat16_rn(0.f);
+      }
     }
   }
 

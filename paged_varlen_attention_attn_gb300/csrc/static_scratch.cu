@@ -131,6 +131,10 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.B = num_seqs;
   p.T = num_tokens;
   p.mbps = max_blocks_per_seq;
+  p.bt_stride = p.mbps;
+  p.clear_status = 1;
+  p.o32 = nullptr;
+  p.lse32 = nullptr;
   p.NB = num_blocks;
   p.max_q = 1;
   p.max_s = max_seq_len;

@@ -164,3 +164,38 @@ def test_cache_write_arguments_are_rejected_on_the_host(lib, kw, status):
 
 def test_cache_write_of_no_tokens_is_a_no_op(lib):
     assert _cw(lib, T=0) == 0
+
+
+# ------------------------------------------------------------------ cascade
+
+def _casc(lib, prefix=32, **kw):
+    args = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, qsl=FAKE, out=FAKE, scale=0.125, H=4, Hkv=2,
+                D=128, bs=16, window=0, causal=1, kv_dtype=0, kv_scale=None)
+    args.update(kw)
+    ext = _ext(workspace=FAKE, workspace_bytes=1 << 30)
+    ks = None
+    if args["kv_scale"] is not None:
+        ks = (ctypes.c_float * 2)(*args["kv_scale"])
+    return lib.pattn_cascade_fwd(args["q"], args["kv"], args["bt"], args["sl"], args["qsl"],
+                                 args["out"], args["scale"], args["H"], args["Hkv"], args["D"],
+                                 args["bs"], args["window"], args["causal"], args["kv_dtype"], ks,
+                                 prefix, ctypes.byref(ext))
+
+
+@pytest.mark.parametrize("prefix,kw,status", [
+    (24, {}, 1),                                   # prefix not a multiple of block_size
+    (0, {}, 1),                                    # no prefix
+    (32, dict(causal=0), 2),                       # cascade is causal only
+    (32, dict(window=64), 2),                      # no window
+    (32, dict(kv_dtype=1, kv_scale=(1.0, 1.0)), 2),  # e4m3 cache
+])
+def test_cascade_arguments_are_rejected_on_the_host(lib, prefix, kw, status):
+    assert _casc(lib, prefix=prefix, **kw) == status
+
+
+def test_cascade_workspace_covers_partials(lib):
+    e = _ext(num_seqs=4, num_tokens=100, max_query_len=64, max_seq_len=2048)
+    plain = pa.pattn_workspace_bytes(e, 8, 2, 128, 16, lib=lib)
+    casc = pa.pattn_cascade_workspace_bytes(e, 8, 2, 128, 16, 512, lib=lib)
+    assert casc >= plain + 2 * 100 * 8 * (128 + 1) * 4
+    assert pa.pattn_cascade_workspace_bytes(e, 8, 2, 128, 16, 20, lib=lib) == 0
