@@ -440,6 +440,86 @@ def workload_desc(spec, cfg):
 
 # ---------------------------------------------------------------- main
 
+def run_cascade(args, world, rank, local, prefix):
+    """Time pattn_cascade_fwd against pattn_varlen_fwd on a decode batch whose
+    requests share a long cached prefix: 64 requests, `prefix` keys shared
+    (default 32768: 134 MB of K/V, more than L2), own suffixes U{128..1024},
+    H 32 / Hkv 8, d 128, block 16 (seed 1501).
+    value = the plain call's algorithmic KV bytes / the cascade call's time
+    (effective GB/s); the line also gives both times."""
+    import torch
+    import paged_varlen_attention_attn_gb300 as pa
+    import workloads as W
+    pa.load()
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    B = 64
+    suffix = W._uniform_ints(128, 1024, B, 1501)
+    seq = [prefix + x for x in suffix]
+    spec = W.CaseSpec("cascade_decode", [1] * B, seq, 32, 8, 128, 16,
+                      pool_blocks=sum((s + 15) // 16 for s in seq) + 8, seed=1501)
+    case = W.make_case(spec, device=dev)
+    case.block_table[:, :prefix // 16] = case.block_table[0, :prefix // 16].clone()
+    counts = work_counts(spec)
+    stream = torch.cuda.Stream(dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = torch.empty_like(case.q)
+    ws = pa.Workspace()
+    kw = dict(scale=case.scale, num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+              max_query_len=1, max_seq_len=max(seq), out=out, workspace=ws, stream=stream)
+
+    def plain():
+        pa.forward(case.q, case.kv_cache, case.block_table, case.seq_lens,
+                   case.query_start_loc, **kw)
+
+    def casc():
+        pa.cascade_forward(case.q, case.kv_cache, case.block_table, case.seq_lens,
+                           case.query_start_loc, common_prefix_len=prefix, **kw)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush_w.zero_(); flush_r.sum(); fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                flush_w.zero_(); flush_r.sum()
+                a.record(); fn(); b.record()
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    ms_plain = timed(plain)
+    ms_casc = timed(casc)
+    clk = clocks.stop()
+    ms_casc = max_over_ranks(ms_casc, device=dev)
+    pk, pk_src = peaks()
+    gbs = counts["bytes_decode"] / (ms_casc / 1e3) / 1e9
+    value, _ = aggregate(gbs * (ms_casc / 1e3), ms_casc / 1e3, device=dev)
+    line = {"metric": "cascade decode: plain algorithmic KV GB/s per cascade-call time",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_casc, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 (fp32 accumulate)", "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": f"{B} decode requests sharing a {prefix}-key prefix, "
+                                   f"suffixes 128..1024, H 32, Hkv 8, d 128, block 16",
+                       "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)"},
+            "plain_ms_per_step": round(ms_plain, 5),
+            "speedup_over_plain": round(ms_plain / ms_casc, 3),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "kernel": "whole cascade call (effective)", "peak_source": pk_src,
+                         "traffic": None},
+            "gpu_launches": 6 * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_cache_write(args, spec, world, rank, local):
     """Time pattn_reshape_and_cache on the workload's new tokens: request r's
     query tokens (positions ctx .. s-1) are written through its block table,
@@ -527,9 +607,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--oracle-rows", type=int, default=None)
+    ap.add_argument("--cascade-prefix", type=int, default=32768,
+                    help="--op cascade: shared prefix length in keys (multiple of 16)")
     ap.add_argument("--f16", action="store_true",
                     help="run the workload with f16 q, cache and output (16-bit workloads only)")
-    ap.add_argument("--op", choices=["attention", "cache_write"], default="attention",
+    ap.add_argument("--op", choices=["attention", "cache_write", "cascade"], default="attention",
                     help="cache_write: time pattn_reshape_and_cache on the workload's new "
                          "tokens instead of the attention step")
     args = ap.parse_args()
@@ -554,6 +636,8 @@ def main():
     dist_init("nccl")
     if args.op == "cache_write":
         return run_cache_write(args, spec, world, rank, local)
+    if args.op == "cascade":
+        return run_cascade(args, world, rank, local, args.cascade_prefix)
     res = run_ours(args, spec, world, rank, local)
     pk, pk_src = peaks()
     counts = res["counts"]
