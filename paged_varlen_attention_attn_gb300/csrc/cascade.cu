@@ -38,33 +38,44 @@ __global__ void __launch_bounds__(256)
   for (int r = threadIdx.x; r < B; r += blockDim.x) suf_sl[r] = seq_lens[r] - prefix;
 }
 
-// One warp per (token, head) row of the batch: out = (2^(a - M) o_a +
-// 2^(b - M) o_b) / (2^(a - M) + 2^(b - M)), a and b the passes' log2-domain
-// lse, M = max(a, b); a pass that saw no key (lse = -inf) weighs 0.  Rows of
-// tokens outside [qsl[0], qsl[B]) are left untouched.
+// One warp per (token, head) row of the batch: out = sum_i 2^(l_i - M) o_i /
+// sum_i 2^(l_i - M) over the prefix pass's KA key chunks and the suffix
+// pass, l_i their log2-domain lse, M the largest; a partial that saw no key
+// (lse = -inf) weighs 0.  Rows of tokens outside [qsl[0], qsl[B]) are left
+// untouched.
 template <int D, bool HALF>
 __global__ void __launch_bounds__(256)
-    cascade_merge_kernel(const float* o_a, const float* lse_a, const float* o_b,
+    cascade_merge_kernel(const float* o_a, const float* lse_a, int KA, const float* o_b,
                          const float* lse_b, void* out, const int* qsl, int B, int T, int H) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<int64_t>(T) * H) return;
   const int t = static_cast<int>(row / H);
   if (t < qsl[0] || t >= qsl[B]) return;
-  const float a = lse_a[row], b = lse_b[row];
-  const float M = fmaxf(a, b);
+  const float b = lse_b[row];
+  float M = b;
+  for (int c = 0; c < KA; ++c) M = fmaxf(M, lse_a[row * KA + c]);
   const float Mu = (M == -INFINITY) ? 0.f : M;
-  const float wa = (a == -INFINITY) ? 0.f : exp2f(a - Mu);
-  const float wb = (b == -INFINITY) ? 0.f : exp2f(b - Mu);
-  const float inv = (wa + wb > 0.f) ? 1.f / (wa + wb) : 0.f;
   constexpr int PER = D / 32;
+  float acc[PER];
   const int64_t e0 = row * D + lane * PER;
+  const float wb = (b == -INFINITY) ? 0.f : exp2f(b - Mu);
+  float L = wb;
 #pragma unroll
-  for (int e = 0; e < PER; e += 2) {
-    const float x0 = (wa * o_a[e0 + e] + wb * o_b[e0 + e]) * inv;
-    const float x1 = (wa * o_a[e0 + e + 1] + wb * o_b[e0 + e + 1]) * inv;
-    *(static_cast<unsigned*>(out) + (e0 + e) / 2) = pack2<HALF>(x0, x1);
+  for (int e = 0; e < PER; ++e) acc[e] = wb * o_b[e0 + e];
+  for (int c = 0; c < KA; ++c) {
+    const float a = lse_a[row * KA + c];
+    if (a == -INFINITY) continue;
+    const float wa = exp2f(a - Mu);
+    L += wa;
+    const float* src = o_a + (row * KA + c) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += wa * src[e];
   }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2)
+    *(static_cast<unsigned*>(out) + (e0 + e) / 2) = pack2<HALF>(acc[e] * inv, acc[e + 1] * inv);
 }
 
 }  // namespace
@@ -77,22 +88,22 @@ cudaError_t launch_cascade_setup(WsHeader* hdr, const int* qsl, const int* seq_l
   return cudaGetLastError();
 }
 
-cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, const float* o_b,
-                                 const float* lse_b, void* out, const int* qsl, int B, int T,
-                                 int H, int D, bool half, cudaStream_t stream) {
+cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, int chunks_a,
+                                 const float* o_b, const float* lse_b, void* out, const int* qsl,
+                                 int B, int T, int H, int D, bool half, cudaStream_t stream) {
   const long long rows = static_cast<long long>(T) * H;
   if (rows == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
   if (D == 128) {
     if (half)
-      cascade_merge_kernel<128, true><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<128, true><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
     else
-      cascade_merge_kernel<128, false><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<128, false><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
   } else {
     if (half)
-      cascade_merge_kernel<64, true><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<64, true><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
     else
-      cascade_merge_kernel<64, false><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<64, false><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
   }
   return cudaGetLastError();
 }

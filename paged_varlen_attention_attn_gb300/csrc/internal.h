@@ -42,6 +42,9 @@ struct Problem {
   // normalised fp32 o [T][H][D] and lse [T][H] (log2 units) instead of out.
   float* o32;
   float* lse32;
+  int kv_chunks;     // prefill in partial-result mode: each row item's key
+                     // tiles are cut into this many contiguous chunks, one CTA
+                     // and one (o, lse) partial each ([T][H][kv_chunks])
   // workspace views
   WsHeader* hdr;
   int2* tiles;       // (request, row-item) pairs sorted by cost, descending
@@ -87,9 +90,9 @@ int decode_heads_per_cta(int Hkv, int D, int kv_dtype);
 cudaError_t launch_cascade_setup(WsHeader* hdr, const int* qsl, const int* seq_lens, int B,
                                  int prefix, int* pre_qsl, int* pre_sl, int* suf_sl,
                                  cudaStream_t stream);
-cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, const float* o_b,
-                                 const float* lse_b, void* out, const int* qsl, int B, int T,
-                                 int H, int D, bool half, cudaStream_t stream);
+cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, int chunks_a,
+                                 const float* o_b, const float* lse_b, void* out, const int* qsl,
+                                 int B, int T, int H, int D, bool half, cudaStream_t stream);
 
 // Query rows one prefill CTA covers: two heads x 128 rows when the GQA group
 // size is even, else one head x 256 rows.

@@ -148,6 +148,7 @@ void base_problem(Problem& p, const void* q, const void* kv_cache, void* out, fl
   p.T = ext->num_tokens;
   p.NB = ext->num_blocks;
   p.rows_per_item = prefill_rows_per_item(p.G);
+  p.kv_chunks = 1;
   p.stream = static_cast<cudaStream_t>(ext->stream);
 }
 
@@ -193,6 +194,7 @@ pattn_status_t launch_pass(const Problem& p) {
 struct CascadeLayout {
   WsLayout suf, pre;
   int splits_suf, splits_pre;
+  int kc;  // key chunks of the prefix pass (its prefill CTAs per row item)
   size_t pre_off, o_pre, lse_pre, o_suf, lse_suf, meta, total;
 };
 
@@ -209,14 +211,27 @@ CascadeLayout cascade_layout(const pattn_ext_t* ext, int H, int Hkv, int D, int 
   c.suf = workspace_layout(ext->num_seqs, ext->num_tokens, H, Hkv, D, ext->max_query_len,
                            c.splits_suf);
   c.pre = workspace_layout(1, ext->num_tokens, H, Hkv, D, ext->num_tokens, c.splits_pre);
+  // Key chunks for the prefix pass: enough prefill CTAs for ~2 per SM when
+  // the batch has few query rows (one 128-row tile per head pair otherwise
+  // walks the whole prefix alone), at most one per key tile and at most 16.
+  {
+    const int G = H / Hkv;
+    const long long items = static_cast<long long>((ext->num_tokens + prefill_rows_per_item(G) - 1) /
+                                                   prefill_rows_per_item(G)) *
+                            ((G % 2 == 0) ? H / 2 : H);
+    const long long want = (2LL * sm_count() + items - 1) / std::max(1LL, items);
+    long long kc = std::min(want, 16LL);
+    kc = std::min(kc, static_cast<long long>((prefix + BLOCK_N - 1) / BLOCK_N));
+    c.kc = static_cast<int>(std::max(1LL, kc));
+  }
   const size_t rows = static_cast<size_t>(ext->num_tokens) * H;
   size_t off = align_up(c.suf.total, 256);
   c.pre_off = off;
   off = align_up(off + c.pre.total, 256);
   c.o_pre = off;
-  off = align_up(off + rows * D * sizeof(float), 256);
+  off = align_up(off + rows * c.kc * D * sizeof(float), 256);
   c.lse_pre = off;
-  off = align_up(off + rows * sizeof(float), 256);
+  off = align_up(off + rows * c.kc * sizeof(float), 256);
   c.o_suf = off;
   off = align_up(off + rows * D * sizeof(float), 256);
   c.lse_suf = off;
@@ -398,6 +413,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.T = ext->num_tokens;
   p.mbps = ext->max_blocks_per_seq;
   p.bt_stride = p.mbps;
+  p.kv_chunks = 1;
   p.clear_status = 1;
   p.o32 = nullptr;
   p.lse32 = nullptr;
@@ -522,6 +538,7 @@ pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache, const int3
   pre.lse_part = reinterpret_cast<float*>(ws + c.pre_off + c.pre.lse_off);
   pre.o32 = reinterpret_cast<float*>(ws + c.o_pre);
   pre.lse32 = reinterpret_cast<float*>(ws + c.lse_pre);
+  pre.kv_chunks = (ext->num_tokens > 1) ? c.kc : 1;  // a single token runs the decode kernel
 
   // Suffix pass: every request over its own keys past the prefix, causal
   // (positions relative to the prefix's end), block-table rows shifted by the
@@ -564,7 +581,8 @@ pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache, const int3
     v = launch_pass(*p);
     if (v != PATTN_OK) return v;
   }
-  if (launch_cascade_merge(pre.o32, pre.lse32, suf.o32, suf.lse32, out, query_start_loc,
+  if (launch_cascade_merge(pre.o32, pre.lse32, pre.kv_chunks, suf.o32, suf.lse32, out,
+                           query_start_loc,
                            ext->num_seqs, ext->num_tokens, num_heads, head_size,
                            kv_dtype == PATTN_KV_F16, st) != cudaSuccess)
     return PATTN_ERR_CUDA;

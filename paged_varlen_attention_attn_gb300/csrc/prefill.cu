@@ -149,8 +149,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   // ------------------------------------------------------------ work item
   const bool head_pairs = (p.G % 2) == 0;
   const int NP = head_pairs ? p.H / 2 : p.H;
-  const int rank = blockIdx.x / NP;
-  const int pidx = blockIdx.x % NP;
+  const int KC = p.kv_chunks;
+  const int chunk = blockIdx.x % KC;
+  const int rank = (blockIdx.x / KC) / NP;
+  const int pidx = (blockIdx.x / KC) % NP;
   if (rank >= p.hdr->num_prefill_tiles) return;
   const int2 tl = p.tiles[rank];
   const int r = tl.x, qt = tl.y;
@@ -171,6 +173,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int hi = p.causal ? min(s, ctx + u.i_last + 1) : s;
     u.x0 = lo / BLOCK_N;
     u.x1 = u.valid ? max(u.x0, (hi + BLOCK_N - 1) / BLOCK_N) : u.x0;
+    if (KC > 1) {  // this CTA's chunk of the request's key tiles
+      const int per = ((s + BLOCK_N - 1) / BLOCK_N + KC - 1) / KC;
+      u.x0 = max(u.x0, chunk * per);
+      u.x1 = max(u.x0, min(u.x1, (chunk + 1) * per));
+    }
     if (!u.valid) u.x0 = u.x1 = 0;
     return u;
   };
@@ -502,8 +509,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     // The normalised row goes to out, or (partial-result mode) to o32 in
     // fp32 with its log2-domain lse = m + log2(l).
-    const int64_t ri = static_cast<int64_t>(t0 + i) * p.H + u.h;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + ri * D;
+    const int64_t ri = (static_cast<int64_t>(t0 + i) * p.H + u.h) * KC + chunk;  // o32 / lse32 row
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                          (static_cast<int64_t>(t0 + i) * p.H + u.h) * D;
     if (u.valid && ok && nt > 0 &&
         __all_sync(FULL, mbar_wait(&bars->o_final[X], 0, status, abort_flag))) {
       tc_fence_after();
@@ -576,7 +584,7 @@ cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const C
 
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map) {
   const int NP = (p.G % 2 == 0) ? p.H / 2 : p.H;
-  const long long grid = static_cast<long long>(p.max_tiles) * NP;
+  const long long grid = static_cast<long long>(p.max_tiles) * NP * p.kv_chunks;
   if (grid == 0) return cudaSuccess;
   const unsigned g = static_cast<unsigned>(grid);
   if (p.kv_dtype == PATTN_KV_F16)

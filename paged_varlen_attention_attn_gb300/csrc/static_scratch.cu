@@ -132,6 +132,7 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.T = num_tokens;
   p.mbps = max_blocks_per_seq;
   p.bt_stride = p.mbps;
+  p.kv_chunks = 1;
   p.clear_status = 1;
   p.o32 = nullptr;
   p.lse32 = nullptr;
