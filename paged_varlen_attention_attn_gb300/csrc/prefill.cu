@@ -8,12 +8,15 @@
 // reaches HBM; the online softmax keeps the result exact (same page, "why this
 // design" item 4).
 //
-// One CTA owns two 128-row query sub-tiles that read the same K/V tiles:
+// A work item is two 128-row query sub-tiles that read the same K/V tiles:
 // two query heads of one KV group (GQA, num_queries_per_kv even) or, when the
-// group size is odd, two consecutive row tiles of one head.  Twelve warps:
+// group size is odd, two consecutive row tiles of one head.  The kernel is
+// persistent: one CTA per SM walks a fixed sequence of items from the
+// longest-first list, so one item's loads and first scores overlap the end of
+// the previous one instead of a CTA launch, set-up and drain.  Twelve warps:
 //   warps 0-3  softmax + epilogue of sub-tile A, thread i owns row i (TMEM lane i)
 //   warps 4-7  softmax + epilogue of sub-tile B
-//   warp  8    TMA producer of both Q tiles (once) and the K tiles, page by
+//   warp  8    TMA producer of both Q tiles of each item and the K tiles, page by
 //              page through block_table into a 3-stage ring, one lane per
 //              page copy
 //   warp  9    MMA issuer (one thread)
@@ -45,6 +48,8 @@
 // running max moves lazily: O is rescaled only when a row max grows by more
 // than 2^8, which stays exact because the final normalisation divides by the
 // sum taken against the same reference max.
+#include <algorithm>
+
 #include "../../include/pattn.h"
 #include "common.cuh"
 #include "internal.h"
@@ -94,6 +99,7 @@ struct Bars {
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
+  uint64_t q_empty;     // every S MMA of an item issued and done: Q may be replaced
   uint64_t drain;       // every MMA issued, before TMEM is released
   unsigned tmem_base;
   int abort_flag;
@@ -134,10 +140,77 @@ __device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) 
       : "f"(a0), "f"(a1));
 }
 
+// One work item: a 128-row query tile (two sub-tiles) of one request, one head
+// pair (or head) and one key chunk, read from the LPT-ordered tile list.
+struct Item {
+  int r, qt, t0, q_len, s, chunk, pidx;
+  bool live;
+};
+
+__device__ __forceinline__ Item load_item(const Problem& p, int item, int n_items, int NP,
+                                          int KC) {
+  Item it;
+  it.live = item < n_items;
+  it.r = it.qt = it.t0 = it.q_len = it.s = it.chunk = it.pidx = 0;
+  if (it.live) {
+    it.chunk = item % KC;
+    it.pidx = (item / KC) % NP;
+    const int2 tl = p.tiles[(item / KC) / NP];
+    it.r = tl.x;
+    it.qt = tl.y;
+    it.t0 = p.qsl[it.r];
+    it.q_len = p.qsl[it.r + 1] - it.t0;
+    it.s = p.seq_lens[it.r];
+  }
+  return it;
+}
+
+// Sub-tile X of an item and the key tiles [x0, x1) it visits.
+__device__ __forceinline__ Sub make_sub(const Problem& p, const Item& it, bool head_pairs, int X) {
+  const int ctx = it.s - it.q_len;
+  const int W = p.window;
+  Sub u;
+  u.h = head_pairs ? 2 * it.pidx + X : it.pidx;
+  u.i0 = head_pairs ? it.qt * BLOCK_M : it.qt * 2 * BLOCK_M + X * BLOCK_M;
+  u.valid = it.live && u.i0 < it.q_len;
+  u.i_last = min(it.q_len, u.i0 + BLOCK_M) - 1;
+  const int lo = (W > 0) ? max(0, ctx + u.i0 - W + 1) : 0;
+  const int hi = p.causal ? min(it.s, ctx + u.i_last + 1) : it.s;
+  u.x0 = lo / BLOCK_N;
+  u.x1 = u.valid ? max(u.x0, (hi + BLOCK_N - 1) / BLOCK_N) : u.x0;
+  if (p.kv_chunks > 1) {  // this item's chunk of the request's key tiles
+    const int per = ((it.s + BLOCK_N - 1) / BLOCK_N + p.kv_chunks - 1) / p.kv_chunks;
+    u.x0 = max(u.x0, it.chunk * per);
+    u.x1 = max(u.x0, min(u.x1, (it.chunk + 1) * per));
+  }
+  if (!u.valid) u.x0 = u.x1 = 0;
+  return u;
+}
+
+// Key tiles [u0, u0 + n) that either sub-tile visits (the two ranges touch or
+// overlap); a sub-tile without key tiles does not widen the range.
+__device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) {
+  const bool ha = a.x1 > a.x0, hb = b.x1 > b.x0;
+  u0 = ha ? (hb ? min(a.x0, b.x0) : a.x0) : b.x0;
+  const int u1 = ha ? (hb ? max(a.x1, b.x1) : a.x1) : b.x1;
+  return u1 - u0;
+}
+
 // HALF: q, the cache and out are f16 (else bf16).
+//
+// Persistent: the grid holds at most one CTA per SM and CTA b takes items
+// b, 2G-1-b, 2G+b, ... of the LPT-ordered list (G = grid size; the order
+// snakes so that no CTA draws the heaviest item of every round).  Every role
+// walks the same item sequence and keeps its ring stages and barrier phases as
+// running counts across items, so the next item's Q, K and first scores go out
+// while the last P V and the epilogue of the current one run.  Two orderings
+// carry across an item boundary: Q is reloaded only after the q_empty commit
+// that follows the item's last S MMA, and the first P V of the next item
+// (which overwrites O) waits on p_full, which the softmax warps arrive on only
+// after their epilogue has read O.
 template <int D, bool HALF>
 __global__ void __launch_bounds__(PF_THREADS, 1)
-    prefill_kernel(const Problem p, const __grid_constant__ CUtensorMap qmap,
+    prefill_kernel(const __grid_constant__ Problem p, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kvmap, float sl2) {
   using C = PrefillCfg<D>;
   extern __shared__ unsigned char smem_raw[];
@@ -146,46 +219,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + C::BAR_OFF);
   unsigned* status = &p.hdr->status;
 
-  // ------------------------------------------------------------ work item
   const bool head_pairs = (p.G % 2) == 0;
   const int NP = head_pairs ? p.H / 2 : p.H;
   const int KC = p.kv_chunks;
-  const int chunk = blockIdx.x % KC;
-  const int rank = (blockIdx.x / KC) / NP;
-  const int pidx = (blockIdx.x / KC) % NP;
-  if (rank >= p.hdr->num_prefill_tiles) return;
-  const int2 tl = p.tiles[rank];
-  const int r = tl.x, qt = tl.y;
-  const int t0 = p.qsl[r];
-  const int q_len = p.qsl[r + 1] - t0;
-  const int s = p.seq_lens[r];
-  const int ctx = s - q_len;
-  const int W = p.window;
-
-  // Sub-tile X of this item (no array: the softmax warps pick X at run time).
-  auto make_sub = [&](int X) {
-    Sub u;
-    u.h = head_pairs ? 2 * pidx + X : pidx;
-    u.i0 = head_pairs ? qt * BLOCK_M : qt * 2 * BLOCK_M + X * BLOCK_M;
-    u.valid = u.i0 < q_len;
-    u.i_last = min(q_len, u.i0 + BLOCK_M) - 1;
-    const int lo = (W > 0) ? max(0, ctx + u.i0 - W + 1) : 0;
-    const int hi = p.causal ? min(s, ctx + u.i_last + 1) : s;
-    u.x0 = lo / BLOCK_N;
-    u.x1 = u.valid ? max(u.x0, (hi + BLOCK_N - 1) / BLOCK_N) : u.x0;
-    if (KC > 1) {  // this CTA's chunk of the request's key tiles
-      const int per = ((s + BLOCK_N - 1) / BLOCK_N + KC - 1) / KC;
-      u.x0 = max(u.x0, chunk * per);
-      u.x1 = max(u.x0, min(u.x1, (chunk + 1) * per));
-    }
-    if (!u.valid) u.x0 = u.x1 = 0;
-    return u;
+  const int n_items = p.hdr->num_prefill_tiles * NP * KC;
+  const int GS = gridDim.x;
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
+  auto item_at = [&](int k) {
+    return k * GS + ((k & 1) ? GS - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
   };
-  const Sub subA = make_sub(0), subB = make_sub(1);
-  const int u0 = subB.valid ? min(subA.x0, subB.x0) : subA.x0;
-  const int u1 = subB.valid ? max(subA.x1, subB.x1) : subA.x1;
-  const int n_union = u1 - u0;
-  const int g = subA.h / p.G;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -204,6 +246,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
+    mbar_init(&bars->q_empty, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -228,7 +271,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(OTHER_REGS));
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ TMA producers
-    // Warp 8 streams Q (once) and the K tiles, warp 10 the V tiles, each
+    // Warp 8 streams the Q tiles and the K tiles, warp 10 the V tiles, each
     // through its own ring, so a K tile never queues behind a V slot.  Each
     // warp reads the block ids of a key tile in one coalesced load, one tile
     // ahead.  Lane 0 waits for the stage and posts the tile's bytes; the
@@ -236,22 +279,45 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // so a tile costs one copy instruction, not 2 x pages of them in one
     // thread.
     const int kv = (warp == 10) ? 1 : 0;
-    if (n_union > 0) {
+    const int nst = kv ? PF_VST : PF_KST;
+    unsigned char* ring = kv ? sV : sK;
+    // Copy `lane` of a tile: page lane / DH, d half lane % DH.
+    const int my_pg = lane / C::DH, my_dh = lane % C::DH;
+    if (kv == 0 && lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kvmap);
+    }
+    int jg = 0;        // key tiles streamed so far (ring position)
+    int n_worked = 0;  // items with at least one key tile so far
+    Item nxt = load_item(p, item_at(0), n_items, NP, KC);
+    for (int k = 0; k * GS < n_items; ++k) {
+      const Item it = nxt;
+      nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
+      const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
+      int u0;
+      const int n_union = union_tiles(subA, subB, u0);
+      if (n_union <= 0) continue;
+      const int g = subA.h / p.G;
+      const int s = it.s;
+      int ok = 1;
       if (kv == 0 && lane == 0) {
-        tma_prefetch_desc(&qmap);
-        tma_prefetch_desc(&kvmap);
+        // Q buffers are free once every S MMA of the previous item is done.
+        if (n_worked > 0 && !mbar_wait(&bars->q_empty, (n_worked - 1) & 1, status, abort_flag))
+          ok = 0;
 #pragma unroll
         for (int X = 0; X < 2; ++X) {
           const Sub& u = X ? subB : subA;
-          if (!u.valid) continue;
+          if (!ok || u.x1 <= u.x0) continue;
           mbar_arrive_expect_tx(&bars->q_full[X], C::TILE);
 #pragma unroll
           for (int dh = 0; dh < C::DH; ++dh)
             tma_load_3d(sQ + X * C::TILE + dh * C::HALF, &qmap, &bars->q_full[X], dh * 64, u.h,
-                        t0 + u.i0);
+                        it.t0 + u.i0);
         }
       }
-      const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
+      ok = __shfl_sync(FULL, ok, 0);
+      if (!ok) break;
+      const int* bt = p.block_table + static_cast<int64_t>(it.r) * p.bt_stride;
       // block id of page `lane` of key tile kt (0 when that page is past seq_len)
       auto page_block = [&](int kt) {
         const int key0 = kt * BLOCK_N + lane * rows_box;
@@ -266,11 +332,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         return blk;
       };
       int blk_next = page_block(u0);
-      // Copy `lane` of a tile: page lane / DH, d half lane % DH.
-      const int my_pg = lane / C::DH, my_dh = lane % C::DH;
-      const int nst = kv ? PF_VST : PF_KST;
-      unsigned char* ring = kv ? sV : sK;
-      for (int j = 0; j < n_union; ++j) {
+      for (int j = 0; j < n_union; ++j, ++jg) {
         const int key_base = (u0 + j) * BLOCK_N;
         const int my_blk = __shfl_sync(FULL, blk_next, my_pg);
         if (j + 1 < n_union) blk_next = page_block(u0 + j + 1);
@@ -279,25 +341,27 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int my_key0 = key_base + my_pg * rows_box;
         const int my_slot = p.bs_shift >= 0 ? (my_key0 & (p.bs - 1)) : (my_key0 % p.bs);
         const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
-        const int st = j % nst;
+        const int st = jg % nst;
         uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
         uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-        int ok = 1;
         if (lane == 0) {
-          if (j >= nst && !mbar_wait(empty, ((j / nst) - 1) & 1, status, abort_flag))
+          if (jg >= nst && !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
             ok = 0;
           else
             mbar_arrive_expect_tx(full, bytes);
         }
-        if (!__shfl_sync(FULL, ok, 0)) break;
+        ok = __shfl_sync(FULL, ok, 0);
+        if (!ok) break;
         if (my_pg < n_load)
           tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap, full,
                       my_dh * 64, g, my_slot, kv * p.NB + my_blk);
       }
+      if (!ok) break;
+      ++n_worked;
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_union > 0) {
+    if (lane == 0) {
       constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !HALF, false);
       constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, !HALF, true);
       // Base descriptors; a byte offset o moves the start address field by
@@ -305,247 +369,315 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const uint64_t q_d = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_d = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t v_d = smem_desc_sw128(smem_u32(sV), C::HALF, 1024);
-      int n_pv0 = 0, n_pv1 = 0;
-      bool q_ready0 = false, q_ready1 = false;
-      bool ok = true;
-      for (int j = 0; ok && j <= n_union; ++j) {
-        const int kt = u0 + j;
-        bool k_ready = false, v_ready = false;
-        // Unrolled: every per-sub-tile value stays in a register (a runtime
-        // choice between two locals would put them in local memory).
+      int jg = 0;                  // key tiles consumed so far (ring position)
+      int pv_tot0 = 0, pv_tot1 = 0;  // P V of sub-tile X so far (p_full phase)
+      int q_tot0 = 0, q_tot1 = 0;    // Q tiles of sub-tile X so far (q_full phase)
+      bool issued = false, ok = true;
+      // The next item's metadata is read when the item starts: the issuer
+      // then waits for that item's Q tiles anyway.
+      for (int k = 0; ok && k * GS < n_items; ++k) {
+        const Item it = load_item(p, item_at(k), n_items, NP, KC);
+        const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
+        int u0;
+        const int n_union = union_tiles(subA, subB, u0);
+        if (n_union <= 0) continue;
+        issued = true;
+        int n_pv0 = 0, n_pv1 = 0;
+        bool q_ready0 = false, q_ready1 = false;
+        for (int j = 0; ok && j <= n_union; ++j) {
+          const int kt = u0 + j;
+          const int jj = jg + j;
+          bool k_ready = false, v_ready = false;
+          // Unrolled: every per-sub-tile value stays in a register (a runtime
+          // choice between two locals would put them in local memory).
 #pragma unroll
-        for (int X = 0; X < 2; ++X) {
-          const Sub& u = X ? subB : subA;
-          int& n_pv = X ? n_pv1 : n_pv0;
-          bool& q_ready = X ? q_ready1 : q_ready0;
-          // P V for the previous key tile
-          if (j >= 1 && u.active(kt - 1)) {
-            const int stp = (j - 1) % PF_VST;
-            if (!mbar_wait(&bars->p_full[X], n_pv & 1, status, abort_flag)) {
-              ok = false;
-              break;
-            }
-            if (!v_ready) {
-              if (!mbar_wait(&bars->v_full[stp], ((j - 1) / PF_VST) & 1, status, abort_flag)) {
+          for (int X = 0; X < 2; ++X) {
+            const Sub& u = X ? subB : subA;
+            int& n_pv = X ? n_pv1 : n_pv0;
+            int& pv_tot = X ? pv_tot1 : pv_tot0;
+            int& q_tot = X ? q_tot1 : q_tot0;
+            bool& q_ready = X ? q_ready1 : q_ready0;
+            // P V for the previous key tile
+            if (j >= 1 && u.active(kt - 1)) {
+              const int stp = (jj - 1) % PF_VST;
+              if (!mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag)) {
                 ok = false;
                 break;
               }
-              v_ready = true;
-            }
-            tc_fence_after();
-            const unsigned p_t = tmem + C::s_col(X) + 64;
-            const unsigned o_t = tmem + C::o_col(X);
-            const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
+              if (!v_ready) {
+                if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                v_ready = true;
+              }
+              tc_fence_after();
+              // The base addresses are made opaque here so that their per-MMA
+              // offsets are added at each use instead of being hoisted out of
+              // the loops as 16 live registers.
+              unsigned p_t = tmem + C::s_col(X) + 64;
+              unsigned o_t = tmem + C::o_col(X);
+              asm volatile("" : "+r"(p_t), "+r"(o_t));
+              const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-              tc_mma_ts(o_t, p_t + kk * 8, vb + ((kk * 16 * 128) >> 4), idesc_pv,
-                        (n_pv > 0 || kk > 0) ? 1u : 0u);
-            ++n_pv;
-            if (kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
-            if (X == 1 || !subB.active(kt - 1)) tc_commit(&bars->v_empty[stp]);
+              for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+                tc_mma_ts(o_t, p_t + kk * 8, vb + ((kk * 16 * 128) >> 4), idesc_pv,
+                          (n_pv > 0 || kk > 0) ? 1u : 0u);
+              ++n_pv;
+              ++pv_tot;
+              if (kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
+              if (X == 1 || !subB.active(kt - 1)) tc_commit(&bars->v_empty[stp]);
+            }
+            // scores for this key tile
+            if (j < n_union && u.active(kt)) {
+              const int st = jj % PF_KST;
+              if (!k_ready) {
+                if (!mbar_wait(&bars->k_full[st], (jj / PF_KST) & 1, status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                k_ready = true;
+              }
+              if (!q_ready) {
+                if (!mbar_wait(&bars->q_full[X], q_tot & 1, status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                q_ready = true;
+                ++q_tot;
+              }
+              tc_fence_after();
+              uint64_t qb = q_d + ((X * C::TILE) >> 4);
+              unsigned s_t = tmem + C::s_col(X);
+              asm volatile("" : "+l"(qb), "+r"(s_t));
+              const uint64_t kb = k_d + ((st * C::TILE) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
+                tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+              }
+              tc_commit(&bars->s_full[X]);
+              if (X == 1 || !subB.active(kt)) tc_commit(&bars->k_empty[st]);
+            }
           }
-          // scores for this key tile
-          if (j < n_union && u.active(kt)) {
-            const int st = j % PF_KST;
-            if (!k_ready) {
-              if (!mbar_wait(&bars->k_full[st], (j / PF_KST) & 1, status, abort_flag)) {
-                ok = false;
-                break;
-              }
-              k_ready = true;
-            }
-            if (!q_ready) {
-              if (!mbar_wait(&bars->q_full[X], 0, status, abort_flag)) {
-                ok = false;
-                break;
-              }
-              q_ready = true;
-            }
-            tc_fence_after();
-            const uint64_t qb = q_d + ((X * C::TILE) >> 4);
-            const uint64_t kb = k_d + ((st * C::TILE) >> 4);
-            const unsigned s_t = tmem + C::s_col(X);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
-              tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(&bars->s_full[X]);
-            if (X == 1 || !subB.active(kt)) tc_commit(&bars->k_empty[st]);
-          }
+          // every S of this item is issued: its Q tiles may be replaced
+          if (ok && j == n_union - 1) tc_commit(&bars->q_empty);
         }
+        jg += n_union;
       }
       // No MMA may still be running when TMEM is released (matters only when
       // a role gave up on a wait).
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, status, nullptr);
+      if (issued) {
+        tc_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, status, nullptr);
+      }
     }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
     // ------------------------------------------------------------ softmax warpgroups
     const int X = warp >> 2;            // 0: A (warps 0-3), 1: B (warps 4-7)
-    const Sub u = make_sub(X);
     const int row = threadIdx.x & 127;  // TMEM lane
-    const int i = u.i0 + row;
-    const int pos = ctx + i;
-    const int kmax_row = p.causal ? min(s, pos + 1) : s;
     const unsigned lane_base = tmem + (static_cast<unsigned>((warp & 3) * 32) << 16);
     const unsigned s_t = lane_base + C::s_col(X);
     const unsigned o_t = lane_base + C::o_col(X);
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = u.valid;
-    const int nt = u.x1 - u.x0;
-    for (int c = 0; ok && c < nt; ++c) {
-      const int kt = u.x0 + c;
-      const int key0 = kt * BLOCK_N;
-      if (!__all_sync(FULL, mbar_wait(&bars->s_full[X], c & 1, status, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[BLOCK_N];
+    const int W = p.window;
+    // Phases carried across items, packed in one word to spare registers:
+    // bit 0 the s_full phase of this sub-tile, bit 1 its o_final phase, bits
+    // 2-3 the V ring position of the key tiles so far modulo 2 x PF_VST (a
+    // V slot's stage and parity).
+    static_assert(PF_VST == 2, "the packed V ring position assumes two stages");
+    unsigned ph = 0;
+    bool ok = true;
+    Item it = load_item(p, item_at(0), n_items, NP, KC);
+    for (int k = 0; ok && k * GS < n_items; ++k) {
+      const Sub u = make_sub(p, it, head_pairs, X);
+      const Sub subA = X ? make_sub(p, it, head_pairs, 0) : u;
+      const Sub subB = X ? u : make_sub(p, it, head_pairs, 1);
+      int u0;
+      const int n_union = union_tiles(subA, subB, u0);
+      // Per-item constants, folded so that few registers stay live through
+      // the key-tile loop.  Row i of the sub-tile sees keys [kmin_row, kmax_row).
+      const int s = it.s;
+      const int ctx = s - it.q_len;
+      const int i = u.i0 + row;
+      const bool row_ok = i < it.q_len;
+      const int kmax_row = p.causal ? min(s, ctx + i + 1) : s;
+      const int kmin_row = (W > 0) ? ctx + i - W + 1 : -(1 << 30);
+      // A tile needs the per-element mask when key0 > edge_hi (keys at or past
+      // seq_len, or past the causal limit of the first row) or key0 <= edge_lo
+      // (keys below the window of the last row).
+      const int edge_hi = min(s - BLOCK_N, p.causal ? ctx + u.i0 - (BLOCK_N - 1) : s);
+      const int edge_lo = (W > 0) ? ctx + u.i_last - W : -(1 << 30);
+      // The tile holding seq_len - 1 has V rows at or past seq_len; they are
+      // zeroed by the first sub-tile whose P V reads it.
+      const int tail_kt = (s - 1) / BLOCK_N;
+      const int vz_kt = (u.active(tail_kt) && (X == 0 || !subA.active(tail_kt))) ? tail_kt : -1;
+      const unsigned vz_m = ((ph >> 2) + (tail_kt - u0)) & 3;  // its V ring position mod 4
+      const int vz_row = s - tail_kt * BLOCK_N;                  // first row to zero
+      // output row of the epilogue
+      const int64_t orow_i = static_cast<int64_t>(it.t0 + i) * p.H + u.h;
+      const int chunk = it.chunk;
+      float m_run = -INFINITY, l_run = 0.f;
+      const int nt = u.x1 - u.x0;
+      for (int c = 0; c < nt; ++c) {
+        const int kt = u.x0 + c;
+        const int key0 = kt * BLOCK_N;
+        if (!__all_sync(FULL, mbar_wait(&bars->s_full[X], (ph ^ c) & 1, status, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[BLOCK_N];
 #pragma unroll
-      for (int q = 0; q < BLOCK_N / 32; ++q)
-        tc_ld32(s_t + q * 32, *reinterpret_cast<float(*)[32]>(&sv[q * 32]));
-      tc_wait_ld();
+        for (int q = 0; q < BLOCK_N / 32; ++q)
+          tc_ld32(s_t + q * 32, *reinterpret_cast<float(*)[32]>(&sv[q * 32]));
+        tc_wait_ld();
 
-      // Does any row of this sub-tile see a masked key in this tile?
-      const bool edge = (key0 + BLOCK_N > s) ||
-                        (p.causal && key0 + BLOCK_N - 1 > ctx + u.i0) ||
-                        (W > 0 && (ctx + u.i_last) - key0 >= W);
-      if (edge) {
-        // column limits of this row in the tile: visible iff lim_lo <= q < lim_hi
-        const int lim_hi = kmax_row - key0;
-        const int lim_lo = (W > 0) ? pos - W + 1 - key0 : -1;
+        // Does any row of this sub-tile see a masked key in this tile?
+        if (key0 > edge_hi || key0 <= edge_lo) {
+          // column limits of this row in the tile: visible iff lim_lo <= q < lim_hi
+          const int lim_hi = kmax_row - key0;
+          const int lim_lo = kmin_row - key0;
 #pragma unroll
-        for (int q = 0; q < BLOCK_N; ++q)
-          sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
-      }
-      float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+          for (int q = 0; q < BLOCK_N; ++q)
+            sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
+        }
+        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-      for (int q = 4; q < BLOCK_N - 4; q += 8) {
-        m4[0] = max3(m4[0], sv[q + 0], sv[q + 1]);
-        m4[1] = max3(m4[1], sv[q + 2], sv[q + 3]);
-        m4[2] = max3(m4[2], sv[q + 4], sv[q + 5]);
-        m4[3] = max3(m4[3], sv[q + 6], sv[q + 7]);
-      }
-      m4[0] = max3(m4[0], sv[BLOCK_N - 4], sv[BLOCK_N - 3]);
-      m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
-      const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
-      const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+        for (int q = 4; q < BLOCK_N - 4; q += 8) {
+          m4[0] = max3(m4[0], sv[q + 0], sv[q + 1]);
+          m4[1] = max3(m4[1], sv[q + 2], sv[q + 3]);
+          m4[2] = max3(m4[2], sv[q + 4], sv[q + 5]);
+          m4[3] = max3(m4[3], sv[q + 6], sv[q + 7]);
+        }
+        m4[0] = max3(m4[0], sv[BLOCK_N - 4], sv[BLOCK_N - 3]);
+        m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
+        const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+        const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
 
-      // Lazy rescale: move the reference max only when it grows by > 2^8.
-      const bool grow = mx_s > m_run + RESCALE_THRESHOLD;
-      const bool need_o = grow && (m_run != -INFINITY) && (c > 0);
-      float alpha = 1.f;
-      if (grow) {
-        alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mx_s);
-        l_run *= alpha;
-        m_run = mx_s;
+        // Lazy rescale: move the reference max only when it grows by > 2^8.
+        const bool grow = mx_s > m_run + RESCALE_THRESHOLD;
+        const bool need_o = grow && (m_run != -INFINITY) && (c > 0);
+        float alpha = 1.f;
+        if (grow) {
+          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mx_s);
+          l_run *= alpha;
+          m_run = mx_s;
+        }
+        if (__any_sync(FULL, need_o)) {
+          // P V of the previous tile is complete: the commit that announced
+          // these scores was issued after it.
+          const float a = need_o ? alpha : 1.f;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            float ov[32];
+            tc_ld32(o_t + q * 32, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] *= a;
+            tc_st32(o_t + q * 32, ov);
+          }
+        }
+
+        const float neg_m = -((m_run == -INFINITY) ? 0.f : m_run);
+        float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+#pragma unroll
+        for (int q = 0; q < BLOCK_N; q += 32) {
+          unsigned pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float a0 = sv[q + e], a1 = sv[q + e + 1], a2 = sv[q + e + 2], a3 = sv[q + e + 3];
+            ffma2(a0, a1, sl2, neg_m);
+            ffma2(a2, a3, sl2, neg_m);
+            a0 = fast_exp2(a0);
+            a1 = fast_exp2(a1);
+            a2 = fast_exp2(a2);
+            a3 = fast_exp2(a3);
+            fadd2(ps0, ps1, a0, a1);
+            fadd2(ps2, ps3, a2, a3);
+            pk[e / 2] = pack2<HALF>(a0, a1);
+            pk[e / 2 + 1] = pack2<HALF>(a2, a3);
+          }
+          tc_st16u(s_t + 64 + q / 2, pk);
+        }
+        l_run += (ps0 + ps1) + (ps2 + ps3);
+        tc_wait_st();
+
+        // Zero V rows at or past seq_len before P V reads them (done by the
+        // first sub-tile whose P V reads this tile).
+        if (kt == vz_kt) {
+          const int st = vz_m & 1;
+          if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], vz_m >> 1, status, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (row >= vz_row) {
+            unsigned char* vrow = sV + st * C::TILE + row * 128;
+#pragma unroll
+            for (int dh = 0; dh < C::DH; ++dh)
+#pragma unroll
+              for (int b = 0; b < 128; b += 16)
+                *reinterpret_cast<uint4*>(vrow + dh * C::HALF + b) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[X]);
       }
-      if (__any_sync(FULL, need_o)) {
-        // P V of the previous tile is complete: the commit that announced
-        // these scores was issued after it.
-        const float a = need_o ? alpha : 1.f;
+      ph = ((ph ^ (nt & 1)) & 3) | ((((ph >> 2) + n_union) & 3) << 2);
+      // The next item's metadata is fetched here, where the score registers
+      // are dead, and lands while the epilogue runs.
+      const Item nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
+
+      // ---------------------------------------------------------- epilogue
+      // The normalised row goes to out, or (partial-result mode) to o32 in
+      // fp32 with its log2-domain lse = m + log2(l).
+      const int64_t ri = orow_i * KC + chunk;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + orow_i * D;
+      bool have_o = false;
+      if (u.valid && ok && nt > 0) {
+        have_o = __all_sync(FULL, mbar_wait(&bars->o_final[X], (ph >> 1) & 1, status, abort_flag));
+        ph ^= 2;
+        if (!have_o) ok = false;
+      }
+      if (have_o) {
+        tc_fence_after();
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           float ov[32];
           tc_ld32(o_t + q * 32, ov);
           tc_wait_ld();
+          if (row_ok) {
+            if (p.o32) {
+              float4* dst = reinterpret_cast<float4*>(p.o32 + ri * D + q * 32);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] *= a;
-          tc_st32(o_t + q * 32, ov);
-        }
-      }
-
-      const float neg_m = -((m_run == -INFINITY) ? 0.f : m_run);
-      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+              for (int e = 0; e < 32; e += 4)
+                dst[e / 4] =
+                    make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
+            } else {
+              unsigned pkd[16];
 #pragma unroll
-      for (int q = 0; q < BLOCK_N; q += 32) {
-        unsigned pk[16];
+              for (int e = 0; e < 16; ++e)
+                pkd[e] = pack2<HALF>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float a0 = sv[q + e], a1 = sv[q + e + 1], a2 = sv[q + e + 2], a3 = sv[q + e + 3];
-          ffma2(a0, a1, sl2, neg_m);
-          ffma2(a2, a3, sl2, neg_m);
-          a0 = fast_exp2(a0);
-          a1 = fast_exp2(a1);
-          a2 = fast_exp2(a2);
-          a3 = fast_exp2(a3);
-          fadd2(ps0, ps1, a0, a1);
-          fadd2(ps2, ps3, a2, a3);
-          pk[e / 2] = pack2<HALF>(a0, a1);
-          pk[e / 2 + 1] = pack2<HALF>(a2, a3);
-        }
-        tc_st16u(s_t + 64 + q / 2, pk);
-      }
-      l_run += (ps0 + ps1) + (ps2 + ps3);
-      tc_wait_st();
-
-      // Zero V rows at or past seq_len before P V reads them (done by the
-      // first sub-tile whose P V reads this tile).
-      if (key0 + BLOCK_N > s && (X == 0 || !subA.active(kt))) {
-        const int j = kt - u0;
-        const int st = j % PF_VST;
-        if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], (j / PF_VST) & 1, status, abort_flag))) {
-          ok = false;
-          break;
-        }
-        if (key0 + row >= s) {
-          unsigned char* vrow = sV + st * C::TILE + row * 128;
-#pragma unroll
-          for (int dh = 0; dh < C::DH; ++dh)
-#pragma unroll
-            for (int b = 0; b < 128; b += 16)
-              *reinterpret_cast<uint4*>(vrow + dh * C::HALF + b) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[X]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    // The normalised row goes to out, or (partial-result mode) to o32 in
-    // fp32 with its log2-domain lse = m + log2(l).
-    const int64_t ri = (static_cast<int64_t>(t0 + i) * p.H + u.h) * KC + chunk;  // o32 / lse32 row
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                          (static_cast<int64_t>(t0 + i) * p.H + u.h) * D;
-    if (u.valid && ok && nt > 0 &&
-        __all_sync(FULL, mbar_wait(&bars->o_final[X], 0, status, abort_flag))) {
-      tc_fence_after();
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        float ov[32];
-        tc_ld32(o_t + q * 32, ov);
-        tc_wait_ld();
-        if (i < q_len) {
-          if (p.o32) {
-            float4* dst = reinterpret_cast<float4*>(p.o32 + ri * D + q * 32);
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              dst[e / 4] = make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
-          } else {
-            unsigned pkd[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) pkd[e] = pack2<HALF>(ov[2 * e] * inv, ov[2 * e + 1] * inv);
-#pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              *reinterpret_cast<uint4*>(orow + q * 32 + e * 2) =
-                  make_uint4(pkd[e], pkd[e + 1], pkd[e + 2], pkd[e + 3]);
+              for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<uint4*>(orow + q * 32 + e * 2) =
+                    make_uint4(pkd[e], pkd[e + 1], pkd[e + 2], pkd[e + 3]);
+            }
           }
         }
+        if (p.o32 && row_ok) p.lse32[ri] = (l_run > 0.f) ? m_run + __log2f(l_run) : -INFINITY;
+      } else if (u.valid && row_ok) {
+        if (p.o32) {
+          for (int e = 0; e < D; ++e) p.o32[ri * D + e] = 0.f;
+          p.lse32[ri] = -INFINITY;
+        } else {
+          for (int e = 0; e < D; ++e) orow[e] = __float2bfloat16_rn(0.f);
+        }
       }
-      if (p.o32 && i < q_len) p.lse32[ri] = (l_run > 0.f) ? m_run + __log2f(l_run) : -INFINITY;
-    } else if (u.valid && i < q_len) {
-      if (p.o32) {
-        for (int e = 0; e < D; ++e) p.o32[ri * D + e] = 0.f;
-        p.lse32[ri] = -INFINITY;
-      } else {
-        for (int e = 0; e < D; ++e) orow[e] = __float2bfloat16_rn(0.f);
-      }
+      it = nxt;
     }
   }
 
@@ -582,11 +714,27 @@ cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const C
   return cudaGetLastError();
 }
 
+// Number of SMs of the current device (cached per device).
+static int prefill_sms() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map) {
   const int NP = (p.G % 2 == 0) ? p.H / 2 : p.H;
-  const long long grid = static_cast<long long>(p.max_tiles) * NP * p.kv_chunks;
-  if (grid == 0) return cudaSuccess;
-  const unsigned g = static_cast<unsigned>(grid);
+  // Persistent grid: one CTA per SM (the shared memory and the 512 TMEM
+  // columns of one CTA fill an SM), capped by the host-side bound on items.
+  const long long items = static_cast<long long>(p.max_tiles) * NP * p.kv_chunks;
+  if (items == 0) return cudaSuccess;
+  const unsigned g = static_cast<unsigned>(std::min<long long>(items, prefill_sms()));
   if (p.kv_dtype == PATTN_KV_F16)
     return p.D == 128 ? launch_prefill_t<128, true>(p, q_map, kv_map, g)
                       : launch_prefill_t<64, true>(p, q_map, kv_map, g);
