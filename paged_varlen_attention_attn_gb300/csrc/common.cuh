@@ -92,6 +92,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
   }
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Block until the kernel this one depends on (launched before it in the
+// stream) has finished and its writes are visible; a no-op without a
+// programmatic dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the dependent kernel to launch once every CTA of this grid has executed
+// this (or exited).
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -222,7 +222,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     // over its requests: a longer one is bad metadata, reported and zeroed
     // here (once, clamped to the output).
     if (p.max_q <= 1 && q_len != 0 && grp == 0 && sp == 0) {
-      if (threadIdx.x == 0) flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
+      if (threadIdx.x == 0) {
+        if (p.pdl_wait) grid_dep_wait();
+        flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
+      }
       const int64_t a = static_cast<int64_t>(max(0, t0)) * p.H * D;
       const int64_t b = static_cast<int64_t>(min(p.T, t0 + max(q_len, 0))) * p.H * D;
       if (p.o32) {
@@ -239,7 +242,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   bool bad = (s < 1) || (s > p.mbps * p.bs) || (t0 < 0) || (t0 >= p.T);
   unsigned* status = &p.hdr->status;
   if (bad) {
-    if (threadIdx.x == 0 && sp == 0) flag_status(status, PATTN_DEV_BAD_METADATA);
+    if (threadIdx.x == 0 && sp == 0) {
+      if (p.pdl_wait) grid_dep_wait();
+      flag_status(status, PATTN_DEV_BAD_METADATA);
+    }
     if (t0 < 0 || t0 >= p.T) return;
     s = 0;  // treat as empty: the rows become zero
   }
@@ -283,6 +289,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         const int key0 = (u_begin + gu) * UNIT;
         blk = bt[p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs)];
         if (blk < 0 || blk >= p.NB) {
+          if (p.pdl_wait) grid_dep_wait();
           flag_status(status, PATTN_DEV_BAD_METADATA);
           blk = min(max(blk, 0), p.NB - 1);
         }
@@ -651,6 +658,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     // CTA's, and the second barrier hands that on to this CTA's warps.
     named_bar_sync(2, C::NW * 32);
     if (threadIdx.x == 0) {
+      // the counters are cleared by the kernel this one may overlap
+      if (p.pdl_wait) grid_dep_wait();
       unsigned* cnt = p.counters + static_cast<int64_t>(r) * p.Hkv + grp;
       unsigned prev;
       asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
@@ -685,6 +694,20 @@ cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
   const float out_scale = FP8 ? p.v_scale * 256.f : 1.f;
   const long long items = static_cast<long long>(p.B) * (p.Hkv / HG) * p.splits;
   if (items == 0) return cudaSuccess;
+  if (p.pdl_launch) {
+    // programmatic dependent of the previous kernel in the stream
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(items));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = p.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, kvmap, sl2, out_scale);
+  }
   kern<<<static_cast<unsigned>(items), C::THREADS, C::SMEM, p.stream>>>(p, kvmap, sl2, out_scale);
   return cudaGetLastError();
 }

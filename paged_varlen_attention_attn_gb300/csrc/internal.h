@@ -54,6 +54,15 @@ struct Problem {
   float* o_part;     // [B][H][splits][D]  (splits > 1)
   float* lse_part;   // [B][H][splits]     (log2 domain)
   cudaStream_t stream;
+  // Programmatic dependent launch (host-side choices):
+  int pdl_launch;   // the decode kernel may start before the previous kernel in
+                    // the stream has finished
+  int pdl_wait;     // ...and waits for it (griddepcontrol.wait) before it touches
+                    // the status word or the partition counters, which that
+                    // kernel clears
+  int pdl_trigger;  // the prefill kernel lets its dependent start once all of
+                    // its CTAs are running (decode CTAs then take the SMs that
+                    // finished prefill CTAs leave)
 };
 
 // Workspace layout for a problem (offsets in bytes, 256-byte aligned).
@@ -67,6 +76,10 @@ WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int sp
 
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const Problem& p);
+// Decode-only calls: clears the first `bytes` bytes of the workspace (status
+// word and partition counters) in a kernel that the decode kernel may follow
+// as a programmatic dependent.
+cudaError_t launch_decode_prep(void* ws, size_t bytes, cudaStream_t stream);
 cudaError_t launch_decode(const Problem& p, const CUtensorMap& kv_map);
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
 // TMA tensor map over the KV cache [2 * NB][bs][Hkv][D] with boxes of

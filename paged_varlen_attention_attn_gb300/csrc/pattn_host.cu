@@ -445,8 +445,17 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   } else {
     // Decode only: nothing to plan (the decode kernel validates its own
     // rows); clear the status word and the partition counters.
-    if (cudaMemsetAsync(ws, 0, L.counters_end, p.stream) != cudaSuccess) return PATTN_ERR_CUDA;
+    if (launch_decode_prep(ws, L.counters_end, p.stream) != cudaSuccess) return PATTN_ERR_CUDA;
   }
+  // The decode kernel is a programmatic dependent of the kernel before it,
+  // unless per-phase events sit between them.  After the prep kernel it
+  // waits for it before touching the words it clears; after the prefill
+  // kernel (which starts only once the plan kernel's writes are done) it has
+  // nothing to wait for, and it may take the SMs of finished prefill CTAs.
+  const bool timed = ext->timing_events != nullptr;
+  p.pdl_launch = timed ? 0 : 1;
+  p.pdl_wait = (ext->max_query_len > 1) ? 0 : 1;
+  p.pdl_trigger = (!timed && ext->max_query_len > 1) ? 1 : 0;
   mark(1);
   mark(2);
 

@@ -128,10 +128,24 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   }
 }
 
+// Decode-only calls: clear the status word and the partition counters.  The
+// decode kernel follows as a programmatic dependent, so it starts streaming the
+// cache while this runs and waits for it only where it touches these words.
+__global__ void __launch_bounds__(PLAN_THREADS) decode_prep_kernel(unsigned* words, int n) {
+  grid_dep_trigger();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) words[i] = 0u;
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const Problem& p) {
   plan_kernel<<<1, PLAN_THREADS, 0, p.stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_prep(void* ws, size_t bytes, cudaStream_t stream) {
+  const int n = static_cast<int>(bytes / sizeof(unsigned));
+  decode_prep_kernel<<<1, PLAN_THREADS, 0, stream>>>(static_cast<unsigned*>(ws), n);
   return cudaGetLastError();
 }
 

@@ -224,6 +224,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int KC = p.kv_chunks;
   const int n_items = p.hdr->num_prefill_tiles * NP * KC;
   const int GS = gridDim.x;
+  // The decode kernel of the same call reads nothing this kernel writes.
+  if (p.pdl_trigger && threadIdx.x == 0) grid_dep_trigger();
   if (static_cast<int>(blockIdx.x) >= n_items) return;
   auto item_at = [&](int k) {
     return k * GS + ((k & 1) ? GS - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
