@@ -24,9 +24,10 @@
 // far below what HBM allows either way.  At G <= 8 two warps serve each KV
 // head, taking the partition's units in turn, and merge their (o, m, l) at the
 // end, which doubles the warps that hide load latency.  e4m3 K and V
-// fragments are widened to f16 in registers with integer operations (exact:
-// every e4m3 value times 2^-8 is an f16 value); the per-tensor scales (times
-// 2^8) are folded into the softmax scale (K) and the final normalisation (V).
+// fragments are widened to f16 in registers, two codes per conversion
+// instruction (exact: every e4m3 value is an f16 value); the per-tensor
+// scales are folded into the softmax scale (K) and the final normalisation
+// (V).
 #include "../../include/pattn.h"
 #include "common.cuh"
 #include "internal.h"
@@ -75,25 +76,21 @@ struct DecodeCfg {
   static constexpr int THREADS = (NW + 1) * 32;
 };
 
-// e4m3 -> f16 widening, exact: a code s.eeee.mmm shifted left by 7 is the
-// f16 pattern 0.seeee.mmm0000000, and moving the sign from bit 14 to bit 15
-// (t + (t & bit 14): the bit doubles into the next position) gives
-// s.0eeee.mmm0000000, the f16 equal to the code's value times 2^-8 -- f16's
-// exponent bias (15) exceeds e4m3's (7) by 8, and e4m3 subnormals land on f16
-// subnormals the same way.  The two NaN codes (S.1111.111) become +-480 *
-// 2^-8 instead of NaN.  The 2^8 is folded into the per-tensor scales.  The
-// shift and the add are integer multiply-adds, which can run on the FMA pipe;
-// only the two masks need the integer ALU.
-//
+// e4m3 -> f16 widening with the hardware pair conversion: exact (every e4m3
+// value, subnormals included, is an f16 value) and NaN codes stay NaN.  The
+// two codes of the low 16 bits of v become the (lo, hi) halves of the result.
+__device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
+  unsigned r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
+  return r;
+}
 // Codes in bytes 0 and 2 of x (bytes 1 and 3 ignored) -> f16x2 (lo, hi).
 __device__ __forceinline__ unsigned e4m3_b02_to_f16x2(unsigned x) {
-  const unsigned t = (x & 0x00FF00FFu) * 128u;
-  return t + (t & 0x40004000u);
+  return e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0020u));
 }
 // Codes in bytes 1 and 3 of x (bytes 0 and 2 ignored) -> f16x2 (lo, hi).
 __device__ __forceinline__ unsigned e4m3_b13_to_f16x2(unsigned x) {
-  const unsigned t = __umulhi(x & 0xFF00FF00u, 0x80000000u);  // >> 1
-  return t + (t & 0x40004000u);
+  return e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0031u));
 }
 
 // Byte offset of 16-byte chunk c of row j of head hh in a K (or V) unit as
@@ -689,9 +686,9 @@ cudaError_t launch_decode_t(const Problem& p, const CUtensorMap& kvmap) {
   auto kern = decode_split_kernel<D, FP8, NT, HG, WPH, HALF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  // e4m3 data is widened to f16 as value * 2^-8; the 2^8 goes into the scales.
-  const float sl2 = p.scale * LOG2E * (FP8 ? p.k_scale * 256.f : 1.f);
-  const float out_scale = FP8 ? p.v_scale * 256.f : 1.f;
+  // e4m3 data is widened to its f16 value; the per-tensor scales go here.
+  const float sl2 = p.scale * LOG2E * (FP8 ? p.k_scale : 1.f);
+  const float out_scale = FP8 ? p.v_scale : 1.f;
   const long long items = static_cast<long long>(p.B) * (p.Hkv / HG) * p.splits;
   if (items == 0) return cudaSuccess;
   if (p.pdl_launch) {
