@@ -34,7 +34,7 @@ def bind(path):
         ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.pattn_ref_e4m3_to_double.restype = ctypes.c_double
     lib.pattn_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.pattn_ref_bf16_to_double.restype = ctypes.c_double
@@ -115,7 +115,7 @@ def _c(a, dtype):
 def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
              num_heads, num_kv_heads, head_size, block_size, window=0, causal=1,
              kv_dtype=0, kv_scale=(1.0, 1.0), rows=None, num_splits=0,
-             num_threads=None, lib=None):
+             num_threads=None, sinks=None, lib=None):
     """Oracle output for selected (token, head) rows.
 
     q_bits        uint16 [T, H, d]   (bf16 bit patterns)
@@ -123,6 +123,7 @@ def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
     block_table   int32 [B, max_blocks_per_seq]
     seq_lens      int32 [B];  query_start_loc int32 [B + 1]
     rows          int array [n, 2] of (token, head); None = every row
+    sinks         float32 [H] attention-sink logits, or None
     lib           another oracle library opened with ``bind`` (tests only)
     Returns (out float64 [n, d], lse float64 [n]).
     """
@@ -147,13 +148,17 @@ def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
     ks = _c(np.asarray(kv_scale, dtype=np.float32).reshape(2), np.float32)
     if num_threads is None:
         num_threads = os.cpu_count() or 1
+    sk = None
+    if sinks is not None:
+        sk = _c(np.asarray(sinks, dtype=np.float32).reshape(num_heads), np.float32)
     rc = lib.pattn_ref_rows(
         q_bits.ctypes.data, kv.ctypes.data, bt.ctypes.data, sl.ctypes.data,
         qsl.ctypes.data, int(sl.shape[0]), int(bt.shape[1]), int(kv.shape[1]),
         float(scale), int(num_heads), int(num_kv_heads), int(head_size),
         int(block_size), int(window), int(causal), int(kv_dtype), ks.ctypes.data,
         rt.ctypes.data, rh.ctypes.data, int(n), int(num_splits),
-        int(num_threads), out.ctypes.data, lse.ctypes.data)
+        int(num_threads), out.ctypes.data, lse.ctypes.data,
+        sk.ctypes.data if sk is not None else None)
     if rc != 0:
         raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
     return out, lse

@@ -23,6 +23,16 @@
  *   score_k = scale * sum_j q_j K_kj, m = max score, w_k = exp(score_k - m),
  *   out = sum_k w_k V_k / sum_k w_k, lse = m + ln(sum_k w_k).
  *
+ * Attention sinks (optional, one logit per query head): the pages name them
+ * only in the RBLN kernel-selection rule ("Full Attention", choice between
+ * naive and flash attention) and give no formula.  The reading taken here is
+ * a learned logit sink_h that joins the softmax normaliser as one more term
+ * with no value: with m = max(max_k score_k, sink_h),
+ *   out = sum_k w_k V_k / (exp(sink_h - m) + sum_k w_k),
+ *   lse = m + ln(exp(sink_h - m) + sum_k w_k).
+ * sink_h is in the units of score (natural log, not multiplied by scale).
+ * sink_h = -inf is the same as no sink.
+ *
  * This is the "naive attention" of the RBLN overview: scores over the valid
  * tokens, softmax, product with V -- with the causal mask of its Full
  * Attention section and the window of its SWA section.  The FlashAttention
@@ -108,6 +118,7 @@ typedef struct {
   int num_splits;
   double* out;
   double* lse;
+  const float* sinks; /* [num_heads] or NULL */
   atomic_llong next_row;
   atomic_int error;
   int max_seq;
@@ -136,12 +147,13 @@ static int key_visible(const job_t* jb, int k, int p) {
 }
 
 /*
- * Attention of one query row over the visible keys in [k_begin, k_end).
- * Writes the normalised output to o[d] and returns lse (-inf if no key is
- * visible, with o = 0).  scores[] has room for s doubles.
+ * Attention of one query row over the visible keys in [k_begin, k_end), with
+ * the sink logit `sink` in the normaliser (-inf: none).  Writes the
+ * normalised output to o[d] and returns lse (-inf if no key is visible and
+ * there is no sink, with o = 0).  scores[] has room for s doubles.
  */
 static double attend_range(const job_t* jb, int r, const double* qv, int g, int p,
-                           int k_begin, int k_end, double* scores, double* o) {
+                           int k_begin, int k_end, double sink, double* scores, double* o) {
   const int d = jb->head_size, bs = jb->block_size;
   const int32_t* bt = jb->block_table + (int64_t)r * jb->max_blocks_per_seq;
   double m = -INFINITY;
@@ -156,8 +168,10 @@ static double attend_range(const job_t* jb, int r, const double* qv, int g, int 
     if (!any || scores[k] > m) m = scores[k];
     any = 1;
   }
-  if (!any) return -INFINITY;
-  double denom = 0.0;
+  const int has_sink = sink > -INFINITY;
+  if (!any && !has_sink) return -INFINITY;
+  if (has_sink && (!any || sink > m)) m = sink;
+  double denom = has_sink ? exp(sink - m) : 0.0;
   for (int k = k_begin; k < k_end; ++k) {
     if (!key_visible(jb, k, p)) continue;
     int blk = bt[k / bs], slot = k % bs;
@@ -190,9 +204,10 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
     qv[j] = jb->kv_dtype == 2 ? pattn_ref_f16_to_double(bits) : pattn_ref_bf16_to_double(bits);
   }
   double* o = jb->out + row * d;
+  const double sink = jb->sinks ? (double)jb->sinks[h] : -INFINITY;
 
   if (jb->num_splits <= 1) {
-    jb->lse[row] = attend_range(jb, r, qv, g, p, 0, s, scores, o);
+    jb->lse[row] = attend_range(jb, r, qv, g, p, 0, s, sink, scores, o);
     return REF_OK;
   }
 
@@ -206,25 +221,29 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
     }
   for (int j = 0; j < d; ++j) o[j] = 0.0;
   if (k_lo < 0) {
-    jb->lse[row] = -INFINITY;
+    jb->lse[row] = sink;  /* the sink alone (or -inf) */
     return REF_OK;
   }
   int b_lo = k_lo / bs, b_hi = (k_hi + bs - 1) / bs, nblk = b_hi - b_lo;
   int per = (nblk + jb->num_splits - 1) / jb->num_splits;
-  /* Each partition gives (o_p, lse_p) by the plain definition; then merge. */
+  /* Each partition gives (o_p, lse_p) by the plain definition (no sink); then
+     merge, the sink entering the merge as one more term with no output. */
   double* lse_p = part + (int64_t)jb->num_splits * d;
   double lse_max = -INFINITY;
   for (int sp = 0; sp < jb->num_splits; ++sp) {
     int kb = (b_lo + sp * per) * bs, ke = (b_lo + (sp + 1) * per) * bs;
     if (kb > s) kb = s;
     if (ke > s) ke = s;
-    lse_p[sp] = (kb < ke) ? attend_range(jb, r, qv, g, p, kb, ke, scores, part + (int64_t)sp * d)
+    lse_p[sp] = (kb < ke) ? attend_range(jb, r, qv, g, p, kb, ke, -INFINITY, scores,
+                                         part + (int64_t)sp * d)
                           : -INFINITY;
     if (lse_p[sp] > lse_max) lse_max = lse_p[sp];
   }
+  if (sink > lse_max) lse_max = sink;
   double sum = 0.0;
   for (int sp = 0; sp < jb->num_splits; ++sp)
     if (lse_p[sp] > -INFINITY) sum += exp(lse_p[sp] - lse_max);
+  if (sink > -INFINITY) sum += exp(sink - lse_max);
   double lse = lse_max + log(sum);
   for (int sp = 0; sp < jb->num_splits; ++sp) {
     if (!(lse_p[sp] > -INFINITY)) continue;
@@ -265,6 +284,7 @@ static void* worker(void* arg) {
  *              (kv_dtype 2, where q is f16 too; else q is bf16)
  *   kv_scale   {k_scale, v_scale}; read only for kv_dtype 1
  *   out        [n_rows][head_size] doubles, lse [n_rows] doubles
+ *   sinks      [num_heads] sink logits, or NULL for none
  * Returns 0, or REF_ERR_* (bad arguments, metadata, or memory).
  */
 int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_table,
@@ -273,7 +293,7 @@ int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_tab
                    int num_kv_heads, int head_size, int block_size, int window, int causal,
                    int kv_dtype, const float* kv_scale, const int32_t* row_token,
                    const int32_t* row_head, int64_t n_rows, int num_splits, int num_threads,
-                   double* out, double* lse) {
+                   double* out, double* lse, const float* sinks) {
   if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !out || !lse)
     return REF_ERR_ARG;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size <= 0 ||
@@ -307,6 +327,7 @@ int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_tab
   jb.num_splits = num_splits;
   jb.out = out;
   jb.lse = lse;
+  jb.sinks = sinks;
   atomic_init(&jb.next_row, 0);
   atomic_init(&jb.error, 0);
   jb.max_seq = 0;

@@ -36,9 +36,10 @@ def to_f64_kv(kv, kv_dtype, kv_scale):
 
 def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
                     num_heads, num_kv_heads, head_size, block_size, window=0,
-                    causal=1, kv_dtype=0, kv_scale=(1.0, 1.0)):
+                    causal=1, kv_dtype=0, kv_scale=(1.0, 1.0), sinks=None):
     """Returns (out [T, H, d], lse [T, H]) in float64; rows of tokens outside
-    every request stay NaN."""
+    every request stay NaN.  sinks: per-head sink logits, taken here as one
+    more key column whose score is the sink and whose value row is zero."""
     Q = to_f64_q(q)
     KV = to_f64_kv(kv_cache, kv_dtype, kv_scale)
     bt = np.asarray(block_table.cpu() if torch.is_tensor(block_table) else block_table)
@@ -70,9 +71,13 @@ def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
             g = h // G
             S = float(np.float32(scale)) * (Q[t0:t1, h, :] @ K[:, g, :].T)
             S = np.where(mask, S, -np.inf)
+            Vh = V[:, g, :]
+            if sinks is not None:
+                S = np.concatenate([S, np.full((ql, 1), float(sinks[h]))], axis=1)
+                Vh = np.concatenate([Vh, np.zeros((1, head_size))], axis=0)
             m = S.max(axis=1, keepdims=True)
             W = np.exp(S - m)
             den = W.sum(axis=1, keepdims=True)
-            out[t0:t1, h, :] = (W @ V[:, g, :]) / den
+            out[t0:t1, h, :] = (W @ Vh) / den
             lse[t0:t1, h] = (m + np.log(den))[:, 0]
     return out, lse
