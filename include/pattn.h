@@ -93,6 +93,18 @@ typedef struct {
                              1 prefill, 2 decode, 3 combine (a phase that does
                              not run records both back to back).  For
                              profiling; the caller owns the events.          */
+  const float* sinks;     /* [device] fp32 [num_heads] attention-sink logits, or
+                             NULL for none.  Head h's sink joins the softmax
+                             normaliser as a term with no value:
+                               out = sum_k e^{s_k} V_k / (e^{sinks[h]} + sum_k e^{s_k}),
+                             s_k = scale * q . k (the sink is not scaled).  A
+                             sink of -inf is no sink; values must be finite or
+                             -inf.  The pages ("RBLN Attention modes", Full
+                             Attention: flash attention serves layers with
+                             attention sinks) give no formula; this is the
+                             reading taken.  A caller built against the
+                             header without this field passes the smaller
+                             struct_size and gets no sinks.                  */
 } pattn_ext_t;
 
 #define PATTN_MAX_SPLITS 64

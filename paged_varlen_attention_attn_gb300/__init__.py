@@ -46,7 +46,8 @@ class Ext(ctypes.Structure):
                 ("max_seq_len", ctypes.c_int), ("num_splits", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("stream", ctypes.c_void_p),
-                ("timing_events", ctypes.POINTER(ctypes.c_void_p))]
+                ("timing_events", ctypes.POINTER(ctypes.c_void_p)),
+                ("sinks", ctypes.c_void_p)]
 
 PHASES = ("plan", "prefill", "decode", "combine")
 
@@ -141,9 +142,10 @@ def pattn_cascade_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block
 def cascade_forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_heads,
                     num_kv_heads, head_size, block_size, common_prefix_len, window=0, causal=1,
                     kv_dtype=KV_BF16, kv_scale=None, max_query_len, max_seq_len, num_splits=0,
-                    out=None, workspace=None, stream=None):
+                    out=None, workspace=None, stream=None, sinks=None):
     """pattn_cascade_fwd on torch tensors: pattn_varlen_fwd for a batch whose
     requests share their first common_prefix_len keys (same blocks).
+    ``sinks``: optional fp32 [num_heads] device tensor of attention-sink logits.
     Returns ``out``; raises PattnError."""
     import torch
     dev = q.device
@@ -156,7 +158,8 @@ def cascade_forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
     ext = make_ext(num_seqs=seq_lens.shape[0], num_tokens=T,
                    max_blocks_per_seq=block_table.shape[1], num_blocks=kv_cache.shape[1],
                    max_query_len=max_query_len, max_seq_len=max_seq_len,
-                   num_splits=num_splits, stream=stream.cuda_stream)
+                   num_splits=num_splits, stream=stream.cuda_stream,
+                   sinks=_sinks_ptr(sinks, num_heads, dev))
     need = pattn_cascade_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size,
                                          common_prefix_len)
     if need == 0:
@@ -180,7 +183,7 @@ def cascade_forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
 
 def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_len,
              max_seq_len, num_splits=0, workspace=0, workspace_bytes=0, stream=0,
-             timing_events=None):
+             timing_events=None, sinks=0):
     e = Ext()
     e.struct_size = ctypes.sizeof(Ext)
     e.num_seqs, e.num_tokens = int(num_seqs), int(num_tokens)
@@ -190,6 +193,7 @@ def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_
     e.workspace = int(workspace) or None
     e.workspace_bytes = int(workspace_bytes)
     e.stream = int(stream) or None
+    e.sinks = int(sinks) or None
     if timing_events is not None:
         arr = (ctypes.c_void_p * 8)(*[int(x) for x in timing_events])
         e._events_keepalive = arr
@@ -269,15 +273,27 @@ class Workspace:
 _default_ws = Workspace()
 
 
+def _sinks_ptr(sinks, num_heads, device):
+    """Device pointer of an fp32 [num_heads] sink tensor (0 for None)."""
+    if sinks is None:
+        return 0
+    import torch
+    if (sinks.dtype != torch.float32 or sinks.device != torch.device(device) or
+            sinks.numel() != num_heads or not sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous fp32 [num_heads] tensor on q's device")
+    return sinks.data_ptr()
+
+
 def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_heads,
             num_kv_heads, head_size, block_size, window=0, causal=1, kv_dtype=KV_BF16,
             kv_scale=None, max_query_len, max_seq_len, num_splits=0, out=None,
-            workspace=None, stream=None, timing_events=None, check=True):
+            workspace=None, stream=None, timing_events=None, sinks=None, check=True):
     """pattn_varlen_fwd on torch tensors (all on one CUDA device).
 
     max_query_len / max_seq_len are host ints (as in FlashAttentionMetadata):
     the library never reads device memory on the host.  ``timing_events``:
-    optional 8 raw cudaEvent_t handles (see pattn_ext_t).  Returns ``out``.
+    optional 8 raw cudaEvent_t handles (see pattn_ext_t).  ``sinks``: optional
+    fp32 [num_heads] device tensor of attention-sink logits.  Returns ``out``.
     """
     import torch
     dev = q.device
@@ -291,7 +307,7 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
                    max_blocks_per_seq=block_table.shape[1], num_blocks=kv_cache.shape[1],
                    max_query_len=max_query_len, max_seq_len=max_seq_len,
                    num_splits=num_splits, stream=stream.cuda_stream,
-                   timing_events=timing_events)
+                   timing_events=timing_events, sinks=_sinks_ptr(sinks, num_heads, dev))
     need = pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size)
     if need == 0:
         raise PattnError(1, "pattn_workspace_bytes")

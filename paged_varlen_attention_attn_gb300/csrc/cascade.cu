@@ -41,12 +41,14 @@ __global__ void __launch_bounds__(256)
 // One warp per (token, head) row of the batch: out = sum_i 2^(l_i - M) o_i /
 // sum_i 2^(l_i - M) over the prefix pass's KA key chunks and the suffix
 // pass, l_i their log2-domain lse, M the largest; a partial that saw no key
-// (lse = -inf) weighs 0.  Rows of tokens outside [qsl[0], qsl[B]) are left
-// untouched.
+// (lse = -inf) weighs 0.  A head's attention sink, if any, adds its term to
+// the denominator here, once (the passes' partials leave it out).  Rows of
+// tokens outside [qsl[0], qsl[B]) are left untouched.
 template <int D, bool HALF>
 __global__ void __launch_bounds__(256)
     cascade_merge_kernel(const float* o_a, const float* lse_a, int KA, const float* o_b,
-                         const float* lse_b, void* out, const int* qsl, int B, int T, int H) {
+                         const float* lse_b, void* out, const int* qsl, int B, int T, int H,
+                         const float* sinks) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<int64_t>(T) * H) return;
@@ -72,6 +74,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] += wa * src[e];
   }
+  L += sink_term(sinks, static_cast<int>(row % H), Mu);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
   for (int e = 0; e < PER; e += 2)
@@ -90,20 +93,21 @@ cudaError_t launch_cascade_setup(WsHeader* hdr, const int* qsl, const int* seq_l
 
 cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, int chunks_a,
                                  const float* o_b, const float* lse_b, void* out, const int* qsl,
-                                 int B, int T, int H, int D, bool half, cudaStream_t stream) {
+                                 int B, int T, int H, int D, bool half, const float* sinks,
+                                 cudaStream_t stream) {
   const long long rows = static_cast<long long>(T) * H;
   if (rows == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
   if (D == 128) {
     if (half)
-      cascade_merge_kernel<128, true><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<128, true><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H, sinks);
     else
-      cascade_merge_kernel<128, false><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<128, false><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H, sinks);
   } else {
     if (half)
-      cascade_merge_kernel<64, true><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<64, true><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H, sinks);
     else
-      cascade_merge_kernel<64, false><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H);
+      cascade_merge_kernel<64, false><<<grid, 256, 0, stream>>>(o_a, lse_a, chunks_a, o_b, lse_b, out, qsl, B, T, H, sinks);
   }
   return cudaGetLastError();
 }

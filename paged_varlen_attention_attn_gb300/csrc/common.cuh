@@ -92,6 +92,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
   }
 }
 
+// ------------------------------------------------------------ attention sinks
+
+// The normaliser term of head h's attention sink against a row whose
+// log2-domain reference max is M: 2^(sink_h * log2(e) - M), or 0 without a
+// sink (a null array or a sink of -inf).  A sink far above M gives +inf, which
+// drives the row to 0, its limit.
+__device__ __forceinline__ float sink_term(const float* sinks, int h, float M) {
+  if (sinks == nullptr) return 0.f;
+  const float s2 = sinks[h] * 1.4426950408889634f;
+  return (s2 == -INFINITY) ? 0.f : exp2f(s2 - M);
+}
+
 // ------------------------------------------------- programmatic dependent launch
 
 // Block until the kernel this one depends on (launched before it in the

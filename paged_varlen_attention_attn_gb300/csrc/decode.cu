@@ -153,6 +153,8 @@ __device__ __forceinline__ void merge_partitions(const Problem& p, int r, int h,
     float L = w0[k] + w1[k];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    // a final output (not a partial for a later merge) includes the sink
+    if (!p.o32) L += sink_term(p.sinks, h + k, Mu);
     inv[k] = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[k][e] = 0.f;
@@ -617,7 +619,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
       if (head >= G) continue;
       const float L = l_run[nt][e & 1];
       const float M = m_run[nt][e & 1];
-      const float inv = (L > 0.f) ? out_scale / L : 0.f;
+      // an unsplit final row includes the head's sink in its normaliser
+      const float Ls = (S == 1 && !p.o32) ? L + sink_term(p.sinks, h0 + head, M) : L;
+      const float inv = (Ls > 0.f) ? out_scale / Ls : 0.f;
 #pragma unroll
       for (int m = 0; m < D / 16; ++m) {
         const int d = FP8 ? (quad * (D / 8) + 2 * m + (e >> 1)) : (16 * m + quad + ((e & 2) ? 8 : 0));

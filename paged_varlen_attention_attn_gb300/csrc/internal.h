@@ -42,6 +42,8 @@ struct Problem {
   // normalised fp32 o [T][H][D] and lse [T][H] (log2 units) instead of out.
   float* o32;
   float* lse32;
+  const float* sinks;  // [H] attention-sink logits (natural-log units) or null; used
+                       // only where a final output row is normalised
   int kv_chunks;     // prefill in partial-result mode: each row item's key
                      // tiles are cut into this many contiguous chunks, one CTA
                      // and one (o, lse) partial each ([T][H][kv_chunks])
@@ -105,7 +107,8 @@ cudaError_t launch_cascade_setup(WsHeader* hdr, const int* qsl, const int* seq_l
                                  cudaStream_t stream);
 cudaError_t launch_cascade_merge(const float* o_a, const float* lse_a, int chunks_a,
                                  const float* o_b, const float* lse_b, void* out, const int* qsl,
-                                 int B, int T, int H, int D, bool half, cudaStream_t stream);
+                                 int B, int T, int H, int D, bool half, const float* sinks,
+                                 cudaStream_t stream);
 
 // Query rows one prefill CTA covers: two heads x 128 rows when the GQA group
 // size is even, else one head x 256 rows.

@@ -5,6 +5,7 @@
 // maps, and enqueue plan -> prefill -> decode -> combine on the caller's
 // stream.  Nothing here synchronises or allocates.
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -51,8 +52,16 @@ int sm_count() {
   return counts[dev];
 }
 
+// The struct grows at its end: a struct_size that reaches the field before
+// `sinks` is a complete older struct.
 bool ext_ok(const pattn_ext_t* ext) {
-  return ext && ext->struct_size >= sizeof(pattn_ext_t);
+  return ext && ext->struct_size >= offsetof(pattn_ext_t, sinks);
+}
+
+// ext->sinks if the caller's struct has the field, else null.
+const float* ext_sinks(const pattn_ext_t* ext) {
+  return ext->struct_size >= offsetof(pattn_ext_t, sinks) + sizeof(ext->sinks) ? ext->sinks
+                                                                               : nullptr;
 }
 
 // Decode partition count.  A forced count is used as given; otherwise enough
@@ -417,6 +426,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.clear_status = 1;
   p.o32 = nullptr;
   p.lse32 = nullptr;
+  p.sinks = ext_sinks(ext);
   p.NB = ext->num_blocks;
   p.max_q = ext->max_query_len;
   p.max_s = ext->max_seq_len;
@@ -593,7 +603,7 @@ pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache, const int3
   if (launch_cascade_merge(pre.o32, pre.lse32, pre.kv_chunks, suf.o32, suf.lse32, out,
                            query_start_loc,
                            ext->num_seqs, ext->num_tokens, num_heads, head_size,
-                           kv_dtype == PATTN_KV_F16, st) != cudaSuccess)
+                           kv_dtype == PATTN_KV_F16, ext_sinks(ext), st) != cudaSuccess)
     return PATTN_ERR_CUDA;
   return PATTN_OK;
 }

@@ -645,7 +645,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
       if (have_o) {
         tc_fence_after();
-        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        // a final output row includes its head's sink in the normaliser
+        const float l_tot = p.o32 ? l_run : l_run + sink_term(p.sinks, u.h, m_run);
+        const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           float ov[32];

@@ -36,10 +36,10 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_ext_struct_layout_matches_c():
-    # size_t + 7 ints (padded) + void* + size_t + void* + void**
-    assert ctypes.sizeof(pa.Ext) == 72
+    # size_t + 7 ints (padded) + void* + size_t + void* + void** + float*
+    assert ctypes.sizeof(pa.Ext) == 80
     assert pa.Ext.workspace.offset == 40 and pa.Ext.stream.offset == 56
-    assert pa.Ext.timing_events.offset == 64
+    assert pa.Ext.timing_events.offset == 64 and pa.Ext.sinks.offset == 72
 
 
 def _ext(**kw):
@@ -103,6 +103,16 @@ def test_bad_struct_size_is_rejected(lib):
     ext.struct_size = 8
     assert _call(lib, ext) == 1
     assert pa.pattn_workspace_bytes(ext, 4, 2, 64, 16, lib=lib) == 0
+    ext.struct_size = 71  # one byte short of the struct before `sinks`
+    assert pa.pattn_workspace_bytes(ext, 4, 2, 64, 16, lib=lib) == 0
+
+
+def test_struct_without_the_sinks_field_is_accepted(lib):
+    # a caller built against the header before `sinks` passes 72 bytes
+    ext = _ext()
+    full = pa.pattn_workspace_bytes(ext, 4, 2, 64, 16, lib=lib)
+    ext.struct_size = 72
+    assert pa.pattn_workspace_bytes(ext, 4, 2, 64, 16, lib=lib) == full > 0
 
 
 def test_split_choice(lib):
