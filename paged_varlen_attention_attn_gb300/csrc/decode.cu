@@ -207,7 +207,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   const int item = blockIdx.x;
   const int sp = item % S;
   const int grp = (item / S) % n_groups;
-  const int r = item / (S * n_groups);
+  // Requests are taken longest first (the order the kernel before this one
+  // wrote), so the grid's ragged end holds the short partitions.  In a
+  // decode-only call that kernel may still be running: wait for it (it also
+  // clears the status word and the counters).
+  if (p.pdl_wait) grid_dep_wait();
+  const int rank = item / (S * n_groups);
+  const int r = p.decode_order ? p.decode_order[rank] : rank;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   const int hh = warp % HG, wslot = warp / HG;  // consumer: head in the group, unit slot
@@ -221,10 +227,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     // over its requests: a longer one is bad metadata, reported and zeroed
     // here (once, clamped to the output).
     if (p.max_q <= 1 && q_len != 0 && grp == 0 && sp == 0) {
-      if (threadIdx.x == 0) {
-        if (p.pdl_wait) grid_dep_wait();
-        flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
-      }
+      if (threadIdx.x == 0) flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
       const int64_t a = static_cast<int64_t>(max(0, t0)) * p.H * D;
       const int64_t b = static_cast<int64_t>(min(p.T, t0 + max(q_len, 0))) * p.H * D;
       if (p.o32) {
@@ -241,10 +244,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   bool bad = (s < 1) || (s > p.mbps * p.bs) || (t0 < 0) || (t0 >= p.T);
   unsigned* status = &p.hdr->status;
   if (bad) {
-    if (threadIdx.x == 0 && sp == 0) {
-      if (p.pdl_wait) grid_dep_wait();
-      flag_status(status, PATTN_DEV_BAD_METADATA);
-    }
+    if (threadIdx.x == 0 && sp == 0) flag_status(status, PATTN_DEV_BAD_METADATA);
     if (t0 < 0 || t0 >= p.T) return;
     s = 0;  // treat as empty: the rows become zero
   }
@@ -288,7 +288,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         const int key0 = (u_begin + gu) * UNIT;
         blk = bt[p.bs_shift >= 0 ? (key0 >> p.bs_shift) : (key0 / p.bs)];
         if (blk < 0 || blk >= p.NB) {
-          if (p.pdl_wait) grid_dep_wait();
           flag_status(status, PATTN_DEV_BAD_METADATA);
           blk = min(max(blk, 0), p.NB - 1);
         }
@@ -659,8 +658,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     // CTA's, and the second barrier hands that on to this CTA's warps.
     named_bar_sync(2, C::NW * 32);
     if (threadIdx.x == 0) {
-      // the counters are cleared by the kernel this one may overlap
-      if (p.pdl_wait) grid_dep_wait();
       unsigned* cnt = p.counters + static_cast<int64_t>(r) * p.Hkv + grp;
       unsigned prev;
       asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"

@@ -50,6 +50,8 @@ struct Problem {
   // workspace views
   WsHeader* hdr;
   int2* tiles;       // (request, row-item) pairs sorted by cost, descending
+  int* decode_order; // [B] requests by decreasing visible decode length (decode
+                     // rows first); null: request order
   int max_tiles;     // capacity of tiles[]
   int rows_per_item; // query rows of one prefill work item (128 or 256)
   unsigned* counters;  // [B][Hkv]: partitions of a (request, KV-head group) done
@@ -71,17 +73,17 @@ struct Problem {
 // The header and the counters come first, so one memset of counters_end
 // bytes clears both.
 struct WsLayout {
-  size_t counters_off, counters_end, tiles_off, o_part_off, lse_off, total;
+  size_t counters_off, counters_end, tiles_off, order_off, o_part_off, lse_off, total;
   int max_tiles;
 };
 WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int splits);
 
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const Problem& p);
-// Decode-only calls: clears the first `bytes` bytes of the workspace (status
-// word and partition counters) in a kernel that the decode kernel may follow
-// as a programmatic dependent.
-cudaError_t launch_decode_prep(void* ws, size_t bytes, cudaStream_t stream);
+// Decode-only calls: clears the status word and the partition counters and
+// writes p.decode_order, in a kernel that the decode kernel may follow as a
+// programmatic dependent.
+cudaError_t launch_decode_prep(const Problem& p);
 cudaError_t launch_decode(const Problem& p, const CUtensorMap& kv_map);
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
 // TMA tensor map over the KV cache [2 * NB][bs][Hkv][D] with boxes of

@@ -316,6 +316,8 @@ WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int sp
   L.max_tiles = (max_q > 1) ? (T + BLOCK_M - 1) / BLOCK_M + B : 0;
   L.tiles_off = off;
   off = align_up(off + static_cast<size_t>(L.max_tiles) * sizeof(int2), 256);
+  L.order_off = off;
+  off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
   L.o_part_off = off;
   if (splits > 1) {
     off = align_up(off + static_cast<size_t>(B) * H * splits * D * sizeof(float), 256);
@@ -434,6 +436,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   unsigned char* ws = static_cast<unsigned char*>(ext->workspace);
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.tiles = reinterpret_cast<int2*>(ws + L.tiles_off);
+  p.decode_order = reinterpret_cast<int*>(ws + L.order_off);
   p.max_tiles = L.max_tiles;
   p.rows_per_item = prefill_rows_per_item(p.G);
   p.counters = reinterpret_cast<unsigned*>(ws + L.counters_off);
@@ -454,14 +457,16 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
     if (launch_plan(p) != cudaSuccess) return PATTN_ERR_CUDA;
   } else {
     // Decode only: nothing to plan (the decode kernel validates its own
-    // rows); clear the status word and the partition counters.
-    if (launch_decode_prep(ws, L.counters_end, p.stream) != cudaSuccess) return PATTN_ERR_CUDA;
+    // rows); clear the status word and the partition counters and order the
+    // requests longest first.
+    if (launch_decode_prep(p) != cudaSuccess) return PATTN_ERR_CUDA;
   }
   // The decode kernel is a programmatic dependent of the kernel before it,
   // unless per-phase events sit between them.  After the prep kernel it
-  // waits for it before touching the words it clears; after the prefill
-  // kernel (which starts only once the plan kernel's writes are done) it has
-  // nothing to wait for, and it may take the SMs of finished prefill CTAs.
+  // waits for it before it starts (it reads the order that kernel writes);
+  // after the prefill kernel (which starts only once the plan kernel's writes
+  // are done) it has nothing to wait for, and it may take the SMs of finished
+  // prefill CTAs.
   const bool timed = ext->timing_events != nullptr;
   p.pdl_launch = timed ? 0 : 1;
   p.pdl_wait = (ext->max_query_len > 1) ? 0 : 1;

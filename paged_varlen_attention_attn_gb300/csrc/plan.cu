@@ -7,7 +7,8 @@
 // query-row item) ordered by their number of key tiles, largest first, so the
 // heaviest tiles start first (longest-processing-time order).  It also clears
 // the status word, so later kernels of the same call report into a clean one,
-// and the decode kernel's partition counters.
+// and the decode kernel's partition counters, and orders the decode requests
+// by their visible length, longest first, for the decode grid.
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,9 +36,78 @@ __device__ __forceinline__ int tile_cost(const Problem& p, int q_len, int s, int
   return min(max(c, 0), NBUCKET - 1);
 }
 
+// Visible KV blocks of request r's decode row (its partitions' total work), or
+// 0 for a request that is not a valid decode (it does no decode work).
+__device__ __forceinline__ int decode_cost(const Problem& p, int r) {
+  const int q_len = p.qsl[r + 1] - p.qsl[r];
+  const int s = p.seq_lens[r];
+  if (q_len != 1 || s < 1 || s > p.mbps * p.bs) return 0;
+  const int k_lo = (p.window > 0) ? max(0, s - p.window) : 0;
+  return min((s + p.bs - 1) / p.bs - k_lo / p.bs, NBUCKET - 1);
+}
+
+// Turns hist[] (counts per cost bucket) into cursors in descending cost
+// order: bucket b starts at the number of items with a larger cost.  Returns
+// the total count (in every thread).  Each thread owns NBUCKET / PLAN_THREADS
+// buckets; warp_sums has a slot per warp.
+__device__ int scan_descending(int* hist, int* warp_sums) {
+  constexpr int PER = NBUCKET / PLAN_THREADS;
+  const int tid = threadIdx.x;
+  int local[PER];
+  int sum = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    local[e] = hist[NBUCKET - 1 - (tid * PER + e)];
+    sum += local[e];
+  }
+  int incl = sum;
+  const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sums[lane] = wi - w;  // exclusive prefix of warps
+    if (lane == 31) warp_sums[32] = wi;
+  }
+  __syncthreads();
+  int run = warp_sums[wid] + incl - sum;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    hist[NBUCKET - 1 - (tid * PER + e)] = run;  // cursor: first slot of the bucket
+    run += local[e];
+  }
+  const int total = warp_sums[32];
+  __syncthreads();
+  return total;
+}
+
+// Writes p.decode_order: every request, by decreasing decode cost (a counting
+// sort; the order within one cost is whatever the atomics give).
+__device__ void order_decodes(const Problem& p, int* hist, int* warp_sums) {
+  const int tid = threadIdx.x;
+  for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
+  __syncthreads();
+  for (int r = tid; r < p.B; r += PLAN_THREADS) atomicAdd(&hist[decode_cost(p, r)], 1);
+  __syncthreads();
+  scan_descending(hist, warp_sums);
+  for (int r = tid; r < p.B; r += PLAN_THREADS)
+    p.decode_order[atomicAdd(&hist[decode_cost(p, r)], 1)] = r;
+}
+
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __shared__ int hist[NBUCKET];
-  __shared__ int warp_sums[PLAN_THREADS / 32];
+  __shared__ int warp_sums[PLAN_THREADS / 32 + 1];
   const int tid = threadIdx.x;
   if (tid == 0 && p.clear_status) p.hdr->status = 0u;
   for (int i = tid; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
@@ -71,50 +141,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   }
   __syncthreads();
 
-  // Exclusive scan over buckets in descending cost order: bucket b starts at
-  // the number of tiles with a larger cost.  Each thread owns 4 buckets.
-  constexpr int PER = NBUCKET / PLAN_THREADS;
-  int local[PER];
-  int sum = 0;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int b = NBUCKET - 1 - (tid * PER + e);
-    local[e] = hist[b];
-    sum += local[e];
-  }
-  int incl = sum;
-  const int lane = tid & 31, wid = tid >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sums[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    int w = warp_sums[lane];
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += v;
-    }
-    warp_sums[lane] = wi - w;  // exclusive prefix of warps
-  }
-  __syncthreads();
-  int run = warp_sums[wid] + incl - sum;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int b = NBUCKET - 1 - (tid * PER + e);
-    const int c = local[e];
-    hist[b] = run;  // cursor: first slot of bucket b
-    run += c;
-  }
-  if (tid == PLAN_THREADS - 1) {
+  // Bucket b's tiles start at the number of tiles with a larger cost.
+  const int run = scan_descending(hist, warp_sums);
+  if (tid == 0) {
     if (run > p.max_tiles) flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
     p.hdr->num_prefill_tiles = min(run, p.max_tiles);
   }
-  __syncthreads();
 
   // Pass 2: scatter (request, q-tile) pairs to their slots.
   for (int r = tid; r < p.B; r += PLAN_THREADS) {
@@ -126,14 +158,26 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
       if (slot < p.max_tiles) p.tiles[slot] = make_int2(r, qt);
     }
   }
+  __syncthreads();
+
+  // Pass 3: the decode grid's request order.
+  if (p.decode_order) order_decodes(p, hist, warp_sums);
 }
 
-// Decode-only calls: clear the status word and the partition counters.  The
-// decode kernel follows as a programmatic dependent, so it starts streaming the
-// cache while this runs and waits for it only where it touches these words.
-__global__ void __launch_bounds__(PLAN_THREADS) decode_prep_kernel(unsigned* words, int n) {
+// Decode-only calls: clear the status word and the partition counters and
+// write the decode order.  The decode kernel follows as a programmatic
+// dependent: its CTAs are resident when this finishes, which saves the launch
+// gap.
+__global__ void __launch_bounds__(PLAN_THREADS) decode_prep_kernel(const Problem p) {
+  __shared__ int hist[NBUCKET];
+  __shared__ int warp_sums[PLAN_THREADS / 32 + 1];
   grid_dep_trigger();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) words[i] = 0u;
+  if (threadIdx.x == 0) {
+    p.hdr->status = 0u;
+    p.hdr->num_prefill_tiles = 0;
+  }
+  for (int i = threadIdx.x; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
+  order_decodes(p, hist, warp_sums);
 }
 
 }  // namespace
@@ -143,9 +187,8 @@ cudaError_t launch_plan(const Problem& p) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_prep(void* ws, size_t bytes, cudaStream_t stream) {
-  const int n = static_cast<int>(bytes / sizeof(unsigned));
-  decode_prep_kernel<<<1, PLAN_THREADS, 0, stream>>>(static_cast<unsigned*>(ws), n);
+cudaError_t launch_decode_prep(const Problem& p) {
+  decode_prep_kernel<<<1, PLAN_THREADS, 0, p.stream>>>(p);
   return cudaGetLastError();
 }
 
