@@ -656,6 +656,9 @@ def main():
                     help="--op cascade: shared prefix length in keys (multiple of 16)")
     ap.add_argument("--f16", action="store_true",
                     help="run the workload with f16 q, cache and output (16-bit workloads only)")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="force the decode partition count (default: the workload's own, "
+                         "0 = the library's choice)")
     ap.add_argument("--op", choices=["attention", "cache_write", "cascade"], default="attention",
                     help="cache_write: time pattn_reshape_and_cache on the workload's new "
                          "tokens instead of the attention step")
@@ -672,6 +675,8 @@ def main():
         if spec.kv_dtype != W.KV_BF16:
             raise SystemExit("--f16 needs a 16-bit workload")
         spec = dataclasses.replace(spec, kv_dtype=W.KV_F16, name=spec.name + "_f16")
+    if args.splits is not None:
+        spec = dataclasses.replace(spec, num_splits=args.splits)
     world, rank, local = dist_info()
 
     if args.impl == "reference":

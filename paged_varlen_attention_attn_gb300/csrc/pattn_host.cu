@@ -67,9 +67,13 @@ const float* ext_sinks(const pattn_ext_t* ext) {
 // Decode partition count.  A forced count is used as given; otherwise enough
 // partitions that there are about 8 (request, KV head, partition) items per
 // SM (2 to 4 decode CTAs, depending on how many KV heads one CTA serves), and
-// that no partition is longer than ~1024 keys, bounded by the block count a
-// row can see and by PATTN_MAX_SPLITS.  It depends on neither dtype nor head
-// size, so pattn_workspace_bytes can size the partials without them.
+// that no partition is longer than ~8192 keys, bounded by the block count a
+// row can see and by PATTN_MAX_SPLITS.  The decode grid runs the requests
+// longest first, so its ragged end is short partitions and few, long
+// partitions beat many short ones (each CTA has a fixed set-up and merge
+// cost); the length bound only keeps one very long request from becoming the
+// tail.  It depends on neither dtype nor head size, so pattn_workspace_bytes
+// can size the partials without them.
 int choose_splits(const pattn_ext_t* ext, int num_kv_heads, int block_size, int window) {
   if (ext->num_splits > 0) return ext->num_splits;
   const int visible = (window > 0) ? std::min(ext->max_seq_len, window + block_size)
@@ -78,7 +82,7 @@ int choose_splits(const pattn_ext_t* ext, int num_kv_heads, int block_size, int 
   const long long items = static_cast<long long>(std::max(1, ext->num_seqs)) * num_kv_heads;
   const int sms = sm_count();
   int by_grid = static_cast<int>((8LL * sms + items - 1) / items);
-  int by_len = (visible + 1023) / 1024;
+  int by_len = (visible + 8191) / 8192;
   int s = std::max(1, std::max(by_grid, by_len));
   s = std::min(s, max_blocks);
   s = std::min(s, PATTN_MAX_SPLITS);
