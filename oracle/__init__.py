@@ -34,7 +34,8 @@ def bind(path):
         ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int]
     lib.pattn_ref_e4m3_to_double.restype = ctypes.c_double
     lib.pattn_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.pattn_ref_bf16_to_double.restype = ctypes.c_double
@@ -115,17 +116,18 @@ def _c(a, dtype):
 def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
              num_heads, num_kv_heads, head_size, block_size, window=0, causal=1,
              kv_dtype=0, kv_scale=(1.0, 1.0), rows=None, num_splits=0,
-             num_threads=None, sinks=None, lib=None):
+             num_threads=None, sinks=None, head_size_v=0, lib=None):
     """Oracle output for selected (token, head) rows.
 
     q_bits        uint16 [T, H, d]   (bf16 bit patterns)
-    kv_cache      uint16 (bf16 bits) or uint8 (e4m3 bytes) [2, NB, bs, Hkv, d]
+    kv_cache      uint16 (bf16 bits) or uint8 (e4m3 bytes) [2, NB, bs, Hkv, d];
+                  with head_size_v > 0 the DiffKV layout [NB, bs, Hkv, d + head_size_v]
     block_table   int32 [B, max_blocks_per_seq]
     seq_lens      int32 [B];  query_start_loc int32 [B + 1]
     rows          int array [n, 2] of (token, head); None = every row
     sinks         float32 [H] attention-sink logits, or None
     lib           another oracle library opened with ``bind`` (tests only)
-    Returns (out float64 [n, d], lse float64 [n]).
+    Returns (out float64 [n, head_size_v or d], lse float64 [n]).
     """
     lib = lib or _load()
     q_bits = _c(q_bits, np.uint16)
@@ -143,7 +145,9 @@ def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
     rt = _c(rows[:, 0], np.int32)
     rh = _c(rows[:, 1], np.int32)
     n = rows.shape[0]
-    out = np.zeros((n, head_size), dtype=np.float64)
+    dv = head_size_v if head_size_v > 0 else head_size
+    nb = int(kv.shape[0]) if head_size_v > 0 else int(kv.shape[1])
+    out = np.zeros((n, dv), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     ks = _c(np.asarray(kv_scale, dtype=np.float32).reshape(2), np.float32)
     if num_threads is None:
@@ -153,12 +157,12 @@ def ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
         sk = _c(np.asarray(sinks, dtype=np.float32).reshape(num_heads), np.float32)
     rc = lib.pattn_ref_rows(
         q_bits.ctypes.data, kv.ctypes.data, bt.ctypes.data, sl.ctypes.data,
-        qsl.ctypes.data, int(sl.shape[0]), int(bt.shape[1]), int(kv.shape[1]),
+        qsl.ctypes.data, int(sl.shape[0]), int(bt.shape[1]), nb,
         float(scale), int(num_heads), int(num_kv_heads), int(head_size),
         int(block_size), int(window), int(causal), int(kv_dtype), ks.ctypes.data,
         rt.ctypes.data, rh.ctypes.data, int(n), int(num_splits),
         int(num_threads), out.ctypes.data, lse.ctypes.data,
-        sk.ctypes.data if sk is not None else None)
+        sk.ctypes.data if sk is not None else None, int(head_size_v))
     if rc != 0:
         raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
     return out, lse
@@ -173,8 +177,9 @@ def ref_varlen(q_bits, kv_cache, block_table, seq_lens, query_start_loc, **kw):
     t0, t1 = int(qsl[0]), int(qsl[-1])
     o, l = ref_rows(q_bits, kv_cache, block_table, seq_lens, query_start_loc,
                     rows=None, **kw)
-    out = np.full((T, H, d), np.nan)
+    dv = o.shape[1]
+    out = np.full((T, H, dv), np.nan)
     lse = np.full((T, H), np.nan)
-    out[t0:t1] = o.reshape(t1 - t0, H, d)
+    out[t0:t1] = o.reshape(t1 - t0, H, dv)
     lse[t0:t1] = l.reshape(t1 - t0, H)
     return out, lse

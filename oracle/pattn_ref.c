@@ -39,6 +39,14 @@
  * page states that the tiled online-softmax method is exact, so the tiled
  * CUDA kernels must reach this result up to rounding.
  *
+ * DiffKV layout (head_size_v > 0): "[vLLM] other attention backends",
+ * FlashAttention DiffKV, lets V have its own head size head_size_v and says
+ * the cache is then asymmetric, without giving its shape.  The reading taken:
+ * one tensor [num_blocks][block_size][num_kv_heads][head_size + head_size_v],
+ * each row holding the token's K (head_size elements) then its V (head_size_v
+ * elements); scores use the head_size elements of q and K, the output has
+ * head_size_v elements.
+ *
  * Split mode (num_splits > 1) is the RBLN "flash attention" reading: the
  * visible keys are cut into partitions of whole KV blocks, each partition
  * gives (o_p, lse_p) by the same definition, and the partitions are merged
@@ -110,6 +118,8 @@ typedef struct {
   int num_seqs, max_blocks_per_seq, num_blocks;
   double scale;
   int num_heads, num_kv_heads, head_size, block_size;
+  int head_size_v; /* elements of a V row (== head_size unless diffkv) */
+  int diffkv;      /* cache in the DiffKV layout */
   int window, causal, kv_dtype;
   double k_scale, v_scale;
   const int32_t* row_token;
@@ -126,8 +136,13 @@ typedef struct {
 
 /* Element (kv_index, block, slot, g, j) of the cache, as double. */
 static double cache_elem(const job_t* jb, int kv_index, int block, int slot, int g, int j) {
-  int64_t idx = ((((int64_t)kv_index * jb->num_blocks + block) * jb->block_size + slot) *
-                     jb->num_kv_heads + g) * jb->head_size + j;
+  int64_t idx;
+  if (jb->diffkv)
+    idx = (((int64_t)block * jb->block_size + slot) * jb->num_kv_heads + g) *
+              (jb->head_size + jb->head_size_v) + (kv_index ? jb->head_size + j : j);
+  else
+    idx = ((((int64_t)kv_index * jb->num_blocks + block) * jb->block_size + slot) *
+               jb->num_kv_heads + g) * jb->head_size + j;
   if (jb->kv_dtype == 0) return pattn_ref_bf16_to_double(((const uint16_t*)jb->kv)[idx]);
   if (jb->kv_dtype == 2) return pattn_ref_f16_to_double(((const uint16_t*)jb->kv)[idx]);
   return pattn_ref_e4m3_to_double(((const uint8_t*)jb->kv)[idx]) *
@@ -154,11 +169,11 @@ static int key_visible(const job_t* jb, int k, int p) {
  */
 static double attend_range(const job_t* jb, int r, const double* qv, int g, int p,
                            int k_begin, int k_end, double sink, double* scores, double* o) {
-  const int d = jb->head_size, bs = jb->block_size;
+  const int d = jb->head_size, dv = jb->head_size_v, bs = jb->block_size;
   const int32_t* bt = jb->block_table + (int64_t)r * jb->max_blocks_per_seq;
   double m = -INFINITY;
   int any = 0;
-  for (int j = 0; j < d; ++j) o[j] = 0.0;
+  for (int j = 0; j < dv; ++j) o[j] = 0.0;
   for (int k = k_begin; k < k_end; ++k) {
     if (!key_visible(jb, k, p)) continue;
     int blk = bt[k / bs], slot = k % bs;
@@ -177,14 +192,14 @@ static double attend_range(const job_t* jb, int r, const double* qv, int g, int 
     int blk = bt[k / bs], slot = k % bs;
     double w = exp(scores[k] - m);
     denom += w;
-    for (int j = 0; j < d; ++j) o[j] += w * cache_elem(jb, 1, blk, slot, g, j);
+    for (int j = 0; j < dv; ++j) o[j] += w * cache_elem(jb, 1, blk, slot, g, j);
   }
-  for (int j = 0; j < d; ++j) o[j] /= denom;
+  for (int j = 0; j < dv; ++j) o[j] /= denom;
   return m + log(denom);
 }
 
 static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, double* part) {
-  const int d = jb->head_size, bs = jb->block_size;
+  const int d = jb->head_size, dv = jb->head_size_v, bs = jb->block_size;
   int t = jb->row_token[row], h = jb->row_head[row];
   if (h < 0 || h >= jb->num_heads) return REF_ERR_ARG;
   int r = find_request(jb, t);
@@ -203,7 +218,7 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
     const uint16_t bits = jb->q[((int64_t)t * jb->num_heads + h) * d + j];
     qv[j] = jb->kv_dtype == 2 ? pattn_ref_f16_to_double(bits) : pattn_ref_bf16_to_double(bits);
   }
-  double* o = jb->out + row * d;
+  double* o = jb->out + row * dv;
   const double sink = jb->sinks ? (double)jb->sinks[h] : -INFINITY;
 
   if (jb->num_splits <= 1) {
@@ -219,7 +234,7 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
       if (k_lo < 0) k_lo = k;
       k_hi = k + 1;
     }
-  for (int j = 0; j < d; ++j) o[j] = 0.0;
+  for (int j = 0; j < dv; ++j) o[j] = 0.0;
   if (k_lo < 0) {
     jb->lse[row] = sink;  /* the sink alone (or -inf) */
     return REF_OK;
@@ -228,14 +243,14 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
   int per = (nblk + jb->num_splits - 1) / jb->num_splits;
   /* Each partition gives (o_p, lse_p) by the plain definition (no sink); then
      merge, the sink entering the merge as one more term with no output. */
-  double* lse_p = part + (int64_t)jb->num_splits * d;
+  double* lse_p = part + (int64_t)jb->num_splits * dv;
   double lse_max = -INFINITY;
   for (int sp = 0; sp < jb->num_splits; ++sp) {
     int kb = (b_lo + sp * per) * bs, ke = (b_lo + (sp + 1) * per) * bs;
     if (kb > s) kb = s;
     if (ke > s) ke = s;
     lse_p[sp] = (kb < ke) ? attend_range(jb, r, qv, g, p, kb, ke, -INFINITY, scores,
-                                         part + (int64_t)sp * d)
+                                         part + (int64_t)sp * dv)
                           : -INFINITY;
     if (lse_p[sp] > lse_max) lse_max = lse_p[sp];
   }
@@ -248,7 +263,7 @@ static int row_compute(job_t* jb, int64_t row, double* scores, double* qv, doubl
   for (int sp = 0; sp < jb->num_splits; ++sp) {
     if (!(lse_p[sp] > -INFINITY)) continue;
     double wgt = exp(lse_p[sp] - lse);
-    for (int j = 0; j < d; ++j) o[j] += wgt * part[(int64_t)sp * d + j];
+    for (int j = 0; j < dv; ++j) o[j] += wgt * part[(int64_t)sp * dv + j];
   }
   jb->lse[row] = lse;
   return REF_OK;
@@ -259,7 +274,7 @@ static void* worker(void* arg) {
   int nsp = jb->num_splits > 1 ? jb->num_splits : 1;
   double* scores = (double*)malloc(sizeof(double) * (size_t)(jb->max_seq + 1));
   double* qv = (double*)malloc(sizeof(double) * (size_t)jb->head_size);
-  double* part = (double*)malloc(sizeof(double) * (size_t)(jb->head_size + 1) * (size_t)nsp);
+  double* part = (double*)malloc(sizeof(double) * (size_t)(jb->head_size_v + 1) * (size_t)nsp);
   if (!scores || !qv || !part) {
     atomic_store(&jb->error, REF_ERR_NOMEM);
   } else {
@@ -279,12 +294,15 @@ static void* worker(void* arg) {
 /*
  * Attention for an explicit list of (token, head) rows.
  *   q          bf16 bits [num_tokens][num_heads][head_size]
- *   kv_cache   [2][num_blocks][block_size][num_kv_heads][head_size],
+ *   kv_cache   [2][num_blocks][block_size][num_kv_heads][head_size], or with
+ *              head_size_v > 0 the DiffKV layout
+ *              [num_blocks][block_size][num_kv_heads][head_size + head_size_v],
  *              bf16 bits (kv_dtype 0), e4m3 bytes (kv_dtype 1) or f16 bits
  *              (kv_dtype 2, where q is f16 too; else q is bf16)
  *   kv_scale   {k_scale, v_scale}; read only for kv_dtype 1
- *   out        [n_rows][head_size] doubles, lse [n_rows] doubles
+ *   out        [n_rows][head_size_v, or head_size] doubles, lse [n_rows] doubles
  *   sinks      [num_heads] sink logits, or NULL for none
+ *   head_size_v  0: the standard layout; > 0: the DiffKV layout (16-bit K/V)
  * Returns 0, or REF_ERR_* (bad arguments, metadata, or memory).
  */
 int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_table,
@@ -293,12 +311,12 @@ int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_tab
                    int num_kv_heads, int head_size, int block_size, int window, int causal,
                    int kv_dtype, const float* kv_scale, const int32_t* row_token,
                    const int32_t* row_head, int64_t n_rows, int num_splits, int num_threads,
-                   double* out, double* lse, const float* sinks) {
+                   double* out, double* lse, const float* sinks, int head_size_v) {
   if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !out || !lse)
     return REF_ERR_ARG;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size <= 0 ||
       block_size <= 0 || num_seqs < 0 || kv_dtype < 0 || kv_dtype > 2 ||
-      (kv_dtype == 1 && !kv_scale))
+      (kv_dtype == 1 && !kv_scale) || head_size_v < 0 || (head_size_v > 0 && kv_dtype == 1))
     return REF_ERR_ARG;
   if (n_rows == 0) return REF_OK;
   job_t jb;
@@ -315,6 +333,8 @@ int pattn_ref_rows(const void* q, const void* kv_cache, const int32_t* block_tab
   jb.num_heads = num_heads;
   jb.num_kv_heads = num_kv_heads;
   jb.head_size = head_size;
+  jb.diffkv = head_size_v > 0;
+  jb.head_size_v = head_size_v > 0 ? head_size_v : head_size;
   jb.block_size = block_size;
   jb.window = window;
   jb.causal = causal;

@@ -36,10 +36,12 @@ def to_f64_kv(kv, kv_dtype, kv_scale):
 
 def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale,
                     num_heads, num_kv_heads, head_size, block_size, window=0,
-                    causal=1, kv_dtype=0, kv_scale=(1.0, 1.0), sinks=None):
+                    causal=1, kv_dtype=0, kv_scale=(1.0, 1.0), sinks=None, head_size_v=0):
     """Returns (out [T, H, d], lse [T, H]) in float64; rows of tokens outside
     every request stay NaN.  sinks: per-head sink logits, taken here as one
-    more key column whose score is the sink and whose value row is zero."""
+    more key column whose score is the sink and whose value row is zero.
+    head_size_v > 0: kv_cache is [NB, bs, Hkv, head_size + head_size_v], each
+    row K then V."""
     Q = to_f64_q(q)
     KV = to_f64_kv(kv_cache, kv_dtype, kv_scale)
     bt = np.asarray(block_table.cpu() if torch.is_tensor(block_table) else block_table)
@@ -48,7 +50,8 @@ def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
                      else query_start_loc)
     T = Q.shape[0]
     G = num_heads // num_kv_heads
-    out = np.full((T, num_heads, head_size), np.nan)
+    dv = head_size_v or head_size
+    out = np.full((T, num_heads, dv), np.nan)
     lse = np.full((T, num_heads), np.nan)
     bs = block_size
     for r in range(len(sl)):
@@ -58,8 +61,12 @@ def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
             continue
         nb = (s + bs - 1) // bs
         blocks = bt[r, :nb]
-        K = KV[0][blocks].reshape(nb * bs, num_kv_heads, head_size)[:s]
-        V = KV[1][blocks].reshape(nb * bs, num_kv_heads, head_size)[:s]
+        if head_size_v:
+            rows = KV[blocks].reshape(nb * bs, num_kv_heads, head_size + dv)[:s]
+            K, V = rows[:, :, :head_size], rows[:, :, head_size:]
+        else:
+            K = KV[0][blocks].reshape(nb * bs, num_kv_heads, head_size)[:s]
+            V = KV[1][blocks].reshape(nb * bs, num_kv_heads, head_size)[:s]
         pos = (s - ql) + np.arange(ql)[:, None]
         key = np.arange(s)[None, :]
         mask = np.ones((ql, s), dtype=bool)
@@ -74,7 +81,7 @@ def brute_attention(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
             Vh = V[:, g, :]
             if sinks is not None:
                 S = np.concatenate([S, np.full((ql, 1), float(sinks[h]))], axis=1)
-                Vh = np.concatenate([Vh, np.zeros((1, head_size))], axis=0)
+                Vh = np.concatenate([Vh, np.zeros((1, dv))], axis=0)
             m = S.max(axis=1, keepdims=True)
             W = np.exp(S - m)
             den = W.sum(axis=1, keepdims=True)

@@ -72,3 +72,26 @@ def shuffle_blocks(case, seed):
                   block_table=bt.to(case.block_table.device),
                   seq_lens=case.seq_lens, query_start_loc=case.query_start_loc,
                   scale=case.scale, kv_scale=case.kv_scale)
+
+
+class DiffKVCase:
+    """A varlen batch over a cache in the DiffKV layout
+    [num_blocks][block_size][num_kv_heads][dk + dv] (each row: K then V)."""
+
+    def __init__(self, case, cache, dv):
+        self.case, self.cache, self.dv = case, cache, dv
+        self.spec = case.spec
+
+
+def diffkv_case(seed, *, H=4, Hkv=2, dk=32, dv=64, bs=16, n_req=3, max_s=70, window=0,
+                kv_dtype=W.KV_BF16, kinds=("prefill", "decode", "chunk"), device="cpu"):
+    """Metadata and q (head size dk) from small_spec; a seeded N(0,1) cache in
+    the DiffKV layout.  The standard-layout cache of the case is not used."""
+    sp = small_spec(seed, H=H, Hkv=Hkv, d=dk, bs=bs, n_req=n_req, max_s=max_s,
+                    window=window, kv_dtype=kv_dtype, kinds=kinds)
+    case = W.make_case(sp, device=device)
+    g = torch.Generator().manual_seed(seed + 7919)
+    nb = case.kv_cache.shape[1]
+    dt = torch.float16 if kv_dtype == W.KV_F16 else torch.bfloat16
+    cache = torch.randn(nb, bs, Hkv, dk + dv, generator=g).to(dt).to(device)
+    return DiffKVCase(case, cache, dv)
