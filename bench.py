@@ -565,6 +565,91 @@ def run_cascade(args, world, rank, local, prefix):
         print(json.dumps(line), flush=True)
 
 
+def run_diffkv(args, spec, world, rank, local):
+    """Time pattn_varlen_fwd over a DiffKV cache (head_size_v != head_size):
+    the workload's request lengths, heads and blocks, K head size 192 and V
+    head size 128 in the layout [num_blocks, block_size, Hkv, 192 + 128].
+    Decode batches report KV GB/s (visible keys x Hkv x (192 + 128) x 2
+    bytes) against HBM; the kernel is the generic SIMT one."""
+    import dataclasses
+    import torch
+    import paged_varlen_attention_attn_gb300 as pa
+    import workloads as W
+    pa.load()
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    dk, dv = 192, 128
+    case = W.make_case(dataclasses.replace(spec, head_size=dk), device=dev)
+    nb = case.kv_cache.shape[1]
+    g = torch.Generator(device=dev).manual_seed(spec.seed + 11)
+    cache = torch.randn(nb, spec.block_size, spec.num_kv_heads, dk + dv, generator=g,
+                        device=dev).to(torch.bfloat16)
+    del case.kv_cache
+    vis = 0
+    for q, s in zip(spec.q_lens, spec.seq_lens):
+        for i in range(q):
+            p = s - q + i
+            lo = max(0, p - spec.window + 1) if spec.window > 0 else 0
+            vis += p + 1 - lo
+    nbytes = vis * spec.num_kv_heads * (dk + dv) * 2
+    out = torch.empty(case.q.shape[0], spec.num_heads, dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ws = pa.Workspace()
+
+    def step():
+        pa.forward(case.q, cache, case.block_table, case.seq_lens, case.query_start_loc,
+                   scale=case.scale, num_heads=spec.num_heads, num_kv_heads=spec.num_kv_heads,
+                   head_size=dk, block_size=spec.block_size, window=spec.window,
+                   causal=spec.causal, max_query_len=case.max_query_len,
+                   max_seq_len=case.max_seq_len, out=out, workspace=ws, stream=stream,
+                   head_size_v=dv)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush_w.zero_(); flush_r.sum(); step()
+    torch.cuda.synchronize()
+    st = pa.pattn_read_device_status(pa.forward.last_ext)
+    if st != 0:
+        raise RuntimeError("device status: " + pa.pattn_status_string(st))
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush_w.zero_(); flush_r.sum()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms = max_over_ranks(ms, device=dev)
+    pk, pk_src = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    value, _ = aggregate(gbs * (ms / 1e3), ms / 1e3, device=dev)
+    line = {"metric": "DiffKV attention, KV GB/s", "value": round(value, 1),
+            "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic (seeded N(0,1), the workload's block tables)",
+            "config": {"workload": f"{spec.name} lengths and heads, K head {dk}, V head {dv}, "
+                                   f"DiffKV layout, block {spec.block_size}",
+                       "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "kernel": "diffkv_kernel", "peak_source": pk_src, "traffic": None},
+            "gpu_launches": K, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_cache_write(args, spec, world, rank, local):
     """Time pattn_reshape_and_cache on the workload's new tokens: request r's
     query tokens (positions ctx .. s-1) are written through its block table,
@@ -659,9 +744,11 @@ def main():
     ap.add_argument("--splits", type=int, default=None,
                     help="force the decode partition count (default: the workload's own, "
                          "0 = the library's choice)")
-    ap.add_argument("--op", choices=["attention", "cache_write", "cascade"], default="attention",
+    ap.add_argument("--op", choices=["attention", "cache_write", "cascade", "diffkv"],
+                    default="attention",
                     help="cache_write: time pattn_reshape_and_cache on the workload's new "
-                         "tokens instead of the attention step")
+                         "tokens instead of the attention step; diffkv: the attention step "
+                         "over a DiffKV cache (K head 192, V head 128)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 400}.get(args.config, 100)
@@ -688,6 +775,8 @@ def main():
         return run_cache_write(args, spec, world, rank, local)
     if args.op == "cascade":
         return run_cascade(args, world, rank, local, args.cascade_prefix)
+    if args.op == "diffkv":
+        return run_diffkv(args, spec, world, rank, local)
     res = run_ours(args, spec, world, rank, local)
     pk, pk_src = peaks()
     counts = res["counts"]

@@ -105,6 +105,20 @@ typedef struct {
                              reading taken.  A caller built against the
                              header without this field passes the smaller
                              struct_size and gets no sinks.                  */
+  int head_size_v;        /* 0: K and V share head_size and the cache is
+                             [2, num_blocks, block_size, num_kv_heads, head_size].
+                             > 0: the DiffKV layout ("[vLLM] other attention
+                             backends", FlashAttention DiffKV: V has its own
+                             head size and the cache is asymmetric; the page
+                             gives no shape, this is the reading taken): the
+                             cache is [num_blocks, block_size, num_kv_heads,
+                             head_size + head_size_v], each row the token's K
+                             then its V, and out is [num_tokens, num_heads,
+                             head_size_v].  head_size and head_size_v are then
+                             multiples of 32 up to 256, the cache is bf16 or
+                             f16 (PATTN_KV_F16), and a generic (not tensor-core)
+                             kernel serves every row.  A caller built against
+                             the header without this field gets 0.           */
 } pattn_ext_t;
 
 #define PATTN_MAX_SPLITS 64
@@ -127,7 +141,8 @@ typedef struct {
  *   scale           multiplies q . k; finite and >= 0
  *   num_heads, num_kv_heads   num_heads % num_kv_heads == 0 and
  *                   num_heads / num_kv_heads <= 16
- *   head_size       64 or 128
+ *   head_size       64 or 128 (with ext->head_size_v > 0: the K head size, a
+ *                   multiple of 32 up to 256; see pattn_ext_t.head_size_v)
  *   block_size      a multiple of 16 (the ValueError of get_kv_cache_shape)
  *   window          <= 0: no window; > 0: keys with p - k < window are visible
  *   causal          1: k <= p; 0: every key < seq_len (then window must be <= 0)
@@ -286,6 +301,32 @@ pattn_status_t pattn_reshape_and_cache(const void* key, const void* value, void*
                                        int num_kv_heads, int head_size, int block_size,
                                        int num_blocks, int kv_dtype, const float* kv_scale,
                                        unsigned* device_status, void* stream);
+
+/*
+ * pattn_reshape_and_cache_diffkv -- pattn_reshape_and_cache for the DiffKV
+ * layout (pattn_ext_t.head_size_v; the DiffKV backend of "[vLLM] other
+ * attention backends" has its own cache-write kernel for its asymmetric
+ * cache).
+ *
+ *   key             [device] 16-bit [num_tokens, num_kv_heads, head_size]
+ *   value           [device] 16-bit [num_tokens, num_kv_heads, head_size_v]
+ *   kv_cache        [device] [num_blocks, block_size, num_kv_heads,
+ *                   head_size + head_size_v], updated in place: token t's key
+ *                   row then its value row go to row [s / block_size]
+ *                   [s % block_size][h], s = slot_mapping[t]
+ *   head_size, head_size_v   multiples of 8; block_size a multiple of 16
+ *   kv_dtype        PATTN_KV_BF16 or PATTN_KV_F16 (the bits are copied)
+ *   slot_mapping, device_status, stream   as for pattn_reshape_and_cache
+ *
+ * All buffers 16-B aligned.  Returns PATTN_OK once enqueued; argument errors
+ * before any CUDA call.  Allocates nothing, never synchronises.
+ */
+pattn_status_t pattn_reshape_and_cache_diffkv(const void* key, const void* value,
+                                              void* kv_cache, const int64_t* slot_mapping,
+                                              int num_tokens, int num_kv_heads, int head_size,
+                                              int head_size_v, int block_size, int num_blocks,
+                                              int kv_dtype, unsigned* device_status,
+                                              void* stream);
 
 /* A static, human-readable name for a status code. */
 const char* pattn_status_string(int status);

@@ -44,6 +44,10 @@ def bind(path):
     lib.pattn_ref_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.pattn_ref_e4m3_encode.restype = ctypes.c_uint8
     lib.pattn_ref_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.pattn_ref_reshape_and_cache_diffkv.restype = ctypes.c_int
+    lib.pattn_ref_reshape_and_cache_diffkv.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.pattn_ref_reshape_and_cache.restype = ctypes.c_int
     lib.pattn_ref_reshape_and_cache.argtypes = [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
@@ -104,6 +108,25 @@ def reshape_and_cache(key_bits, value_bits, kv_cache, slot_mapping, *, num_kv_he
         key_bits.ctypes.data, value_bits.ctypes.data, kv_cache.ctypes.data, slots.ctypes.data,
         int(slots.shape[0]), num_kv_heads, head_size, block_size, int(kv_cache.shape[1]),
         kv_dtype, ks, vs)
+    if rc != 0:
+        raise OracleError(_ERRORS.get(rc, f"error {rc}"))
+    return kv_cache
+
+
+def reshape_and_cache_diffkv(key_bits, value_bits, kv_cache, slot_mapping, *, num_kv_heads,
+                             head_size, head_size_v, block_size, lib=None):
+    """Oracle cache write into the DiffKV layout: key_bits uint16 [T, Hkv,
+    head_size], value_bits uint16 [T, Hkv, head_size_v], kv_cache uint16 [NB,
+    bs, Hkv, head_size + head_size_v] updated in place and returned."""
+    lib = lib or _load()
+    key_bits = _c(key_bits, np.uint16)
+    value_bits = _c(value_bits, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    assert kv_cache.dtype == np.uint16 and kv_cache.flags["C_CONTIGUOUS"]
+    rc = lib.pattn_ref_reshape_and_cache_diffkv(
+        key_bits.ctypes.data, value_bits.ctypes.data, kv_cache.ctypes.data, slots.ctypes.data,
+        int(slots.shape[0]), num_kv_heads, head_size, head_size_v, block_size,
+        int(kv_cache.shape[0]))
     if rc != 0:
         raise OracleError(_ERRORS.get(rc, f"error {rc}"))
     return kv_cache

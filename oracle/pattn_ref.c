@@ -448,3 +448,43 @@ int pattn_ref_reshape_and_cache(const uint16_t* key, const uint16_t* value, void
   }
   return err;
 }
+
+/*
+ * KV-cache write for the DiffKV layout ("[vLLM] other attention backends",
+ * FlashAttention DiffKV, which has its own cache-write kernel for its
+ * asymmetric cache).  Token t with slot s = slot_mapping[t] >= 0 writes, for
+ * every KV head h, its key row (head_size elements) and then its value row
+ * (head_size_v elements) to cache row [s / bs][s % bs][h] of
+ * [num_blocks][block_size][num_kv_heads][head_size + head_size_v]: 16-bit
+ * bits as they are.  A negative slot writes nothing; a slot at or beyond
+ * num_blocks * bs writes nothing and makes the call return REF_ERR_METADATA.
+ * key is [T][Hkv][head_size] and value [T][Hkv][head_size_v], 16-bit bits.
+ */
+int pattn_ref_reshape_and_cache_diffkv(const uint16_t* key, const uint16_t* value,
+                                       uint16_t* kv_cache, const int64_t* slot_mapping,
+                                       int num_tokens, int num_kv_heads, int head_size,
+                                       int head_size_v, int block_size, int num_blocks) {
+  if (!key || !value || !kv_cache || !slot_mapping || num_tokens < 0 || num_kv_heads <= 0 ||
+      head_size <= 0 || head_size_v <= 0 || block_size <= 0 || num_blocks < 0)
+    return REF_ERR_ARG;
+  int err = REF_OK;
+  const int64_t pool = (int64_t)num_blocks * block_size;
+  const int width = head_size + head_size_v;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t sl = slot_mapping[t];
+    if (sl < 0) continue;
+    if (sl >= pool) {
+      err = REF_ERR_METADATA;
+      continue;
+    }
+    for (int h = 0; h < num_kv_heads; ++h) {
+      uint16_t* row = kv_cache + ((sl / block_size * block_size + sl % block_size) *
+                                      num_kv_heads + h) * (int64_t)width;
+      for (int j = 0; j < head_size; ++j)
+        row[j] = key[((int64_t)t * num_kv_heads + h) * head_size + j];
+      for (int j = 0; j < head_size_v; ++j)
+        row[head_size + j] = value[((int64_t)t * num_kv_heads + h) * head_size_v + j];
+    }
+  }
+  return err;
+}

@@ -27,7 +27,8 @@ STATUS = {0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARGUMENT", 2: "PATTN_ERR_UNSUPPOR
 
 EXPORTS = ("pattn_varlen_fwd", "pattn_workspace_bytes", "pattn_decode_splits",
            "pattn_read_device_status", "pattn_status_string", "pattn_version",
-           "pattn_decode_fwd_static", "pattn_reshape_and_cache", "pattn_cascade_fwd",
+           "pattn_decode_fwd_static", "pattn_reshape_and_cache",
+           "pattn_reshape_and_cache_diffkv", "pattn_cascade_fwd",
            "pattn_cascade_workspace_bytes")
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -47,7 +48,7 @@ class Ext(ctypes.Structure):
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("stream", ctypes.c_void_p),
                 ("timing_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("head_size_v", ctypes.c_int)]
 
 PHASES = ("plan", "prefill", "decode", "combine")
 
@@ -92,6 +93,8 @@ def load(path=None):
     lib.pattn_cascade_workspace_bytes.argtypes = [ctypes.POINTER(Ext), i, i, i, i, i]
     lib.pattn_reshape_and_cache.restype = i
     lib.pattn_reshape_and_cache.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
+    lib.pattn_reshape_and_cache_diffkv.restype = i
+    lib.pattn_reshape_and_cache_diffkv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
     if path is None:
         _lib = lib
     return lib
@@ -128,6 +131,24 @@ def reshape_and_cache(key, value, kv_cache, slot_mapping, *, block_size, kv_dtyp
                                  stream.cuda_stream)
     if st != 0:
         raise PattnError(st, "pattn_reshape_and_cache")
+    return kv_cache
+
+
+def reshape_and_cache_diffkv(key, value, kv_cache, slot_mapping, *, block_size,
+                             kv_dtype=KV_BF16, device_status=None, stream=None):
+    """pattn_reshape_and_cache_diffkv on torch tensors: key 16-bit [T, Hkv, dk],
+    value [T, Hkv, dv], kv_cache [num_blocks, block_size, Hkv, dk + dv],
+    slot_mapping int64 [T].  Raises PattnError."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(key.device)
+    st = load().pattn_reshape_and_cache_diffkv(
+        key.data_ptr(), value.data_ptr(), kv_cache.data_ptr(), slot_mapping.data_ptr(),
+        int(key.shape[0]), int(key.shape[1]), int(key.shape[2]), int(value.shape[2]),
+        int(block_size), int(kv_cache.shape[0]), int(kv_dtype),
+        None if device_status is None else device_status.data_ptr(), stream.cuda_stream)
+    if st != 0:
+        raise PattnError(st, "pattn_reshape_and_cache_diffkv")
     return kv_cache
 
 
@@ -183,7 +204,7 @@ def cascade_forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scal
 
 def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_len,
              max_seq_len, num_splits=0, workspace=0, workspace_bytes=0, stream=0,
-             timing_events=None, sinks=0):
+             timing_events=None, sinks=0, head_size_v=0):
     e = Ext()
     e.struct_size = ctypes.sizeof(Ext)
     e.num_seqs, e.num_tokens = int(num_seqs), int(num_tokens)
@@ -194,6 +215,7 @@ def make_ext(*, num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_query_
     e.workspace_bytes = int(workspace_bytes)
     e.stream = int(stream) or None
     e.sinks = int(sinks) or None
+    e.head_size_v = int(head_size_v)
     if timing_events is not None:
         arr = (ctypes.c_void_p * 8)(*[int(x) for x in timing_events])
         e._events_keepalive = arr
@@ -287,27 +309,33 @@ def _sinks_ptr(sinks, num_heads, device):
 def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_heads,
             num_kv_heads, head_size, block_size, window=0, causal=1, kv_dtype=KV_BF16,
             kv_scale=None, max_query_len, max_seq_len, num_splits=0, out=None,
-            workspace=None, stream=None, timing_events=None, sinks=None, check=True):
+            workspace=None, stream=None, timing_events=None, sinks=None, head_size_v=0,
+            check=True):
     """pattn_varlen_fwd on torch tensors (all on one CUDA device).
 
     max_query_len / max_seq_len are host ints (as in FlashAttentionMetadata):
     the library never reads device memory on the host.  ``timing_events``:
     optional 8 raw cudaEvent_t handles (see pattn_ext_t).  ``sinks``: optional
-    fp32 [num_heads] device tensor of attention-sink logits.  Returns ``out``.
+    fp32 [num_heads] device tensor of attention-sink logits.  ``head_size_v``:
+    > 0 selects the DiffKV cache layout [num_blocks, block_size, num_kv_heads,
+    head_size + head_size_v] and an output of head size head_size_v (see
+    pattn_ext_t).  Returns ``out``.
     """
     import torch
     dev = q.device
     T = q.shape[0]
     if out is None:
         odt = torch.float16 if kv_dtype == KV_F16 else torch.bfloat16
-        out = torch.empty((T, num_heads, head_size), dtype=odt, device=dev)
+        out = torch.empty((T, num_heads, head_size_v or head_size), dtype=odt, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
+    num_blocks = kv_cache.shape[0] if head_size_v else kv_cache.shape[1]
     ext = make_ext(num_seqs=seq_lens.shape[0], num_tokens=T,
-                   max_blocks_per_seq=block_table.shape[1], num_blocks=kv_cache.shape[1],
+                   max_blocks_per_seq=block_table.shape[1], num_blocks=num_blocks,
                    max_query_len=max_query_len, max_seq_len=max_seq_len,
                    num_splits=num_splits, stream=stream.cuda_stream,
-                   timing_events=timing_events, sinks=_sinks_ptr(sinks, num_heads, dev))
+                   timing_events=timing_events, sinks=_sinks_ptr(sinks, num_heads, dev),
+                   head_size_v=head_size_v)
     need = pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size)
     if need == 0:
         raise PattnError(1, "pattn_workspace_bytes")

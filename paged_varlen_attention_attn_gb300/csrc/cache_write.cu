@@ -63,10 +63,62 @@ __global__ void __launch_bounds__(CW_THREADS)
   }
 }
 
+// DiffKV layout [NB][bs][Hkv][dk + dv]: token t's key row (dk elements) then
+// its value row (dv) go to cache row [s / bs][s % bs][h].  16-bit data only;
+// each thread moves 16 bytes (8 elements) of one key or value row.
+__global__ void __launch_bounds__(CW_THREADS)
+    reshape_and_cache_diffkv_kernel(const uint16_t* __restrict__ key,
+                                    const uint16_t* __restrict__ value, uint16_t* __restrict__ cache,
+                                    const int64_t* __restrict__ slots, int T, int Hkv, int dk,
+                                    int dv, int bs, int NB, unsigned* status) {
+  const int ck = dk / 8, cv = dv / 8;                  // 16-byte pieces of a K / V row
+  const int64_t per_token = static_cast<int64_t>(Hkv) * (ck + cv);
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * CW_THREADS + threadIdx.x;
+  if (idx >= per_token * T) return;
+  const int t = static_cast<int>(idx / per_token);
+  const int rem = static_cast<int>(idx - static_cast<int64_t>(t) * per_token);
+  const int h = rem / (ck + cv), c = rem - h * (ck + cv);
+  const int64_t s = slots[t];
+  if (s < 0) return;
+  if (s >= static_cast<int64_t>(NB) * bs) {
+    if (h == 0 && c == 0 && status) atomicOr(status, PATTN_DEV_BAD_METADATA);
+    return;
+  }
+  const bool is_v = c >= ck;
+  const uint16_t* src = is_v ? value + (static_cast<int64_t>(t) * Hkv + h) * dv + (c - ck) * 8
+                             : key + (static_cast<int64_t>(t) * Hkv + h) * dk + c * 8;
+  const int64_t dst = (s * Hkv + h) * static_cast<int64_t>(dk + dv) + c * 8;
+  *reinterpret_cast<uint4*>(cache + dst) = *reinterpret_cast<const uint4*>(src);
+}
+
 }  // namespace
 }  // namespace pattn
 
 using namespace pattn;
+
+extern "C" pattn_status_t pattn_reshape_and_cache_diffkv(
+    const void* key, const void* value, void* kv_cache, const int64_t* slot_mapping,
+    int num_tokens, int num_kv_heads, int head_size, int head_size_v, int block_size,
+    int num_blocks, int kv_dtype, unsigned* device_status, void* stream) {
+  if (!key || !value || !kv_cache || !slot_mapping) return PATTN_ERR_INVALID_ARGUMENT;
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PATTN_ERR_INVALID_ARGUMENT;
+  if (block_size <= 0 || block_size % 16 != 0) return PATTN_ERR_INVALID_ARGUMENT;
+  if (head_size <= 0 || head_size % 8 != 0 || head_size_v <= 0 || head_size_v % 8 != 0)
+    return PATTN_ERR_UNSUPPORTED;
+  if (kv_dtype != PATTN_KV_BF16 && kv_dtype != PATTN_KV_F16) return PATTN_ERR_UNSUPPORTED;
+  const uintptr_t align = reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value) |
+                          reinterpret_cast<uintptr_t>(kv_cache);
+  if (align & 15) return PATTN_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return PATTN_OK;
+  const long long n =
+      static_cast<long long>(num_tokens) * num_kv_heads * ((head_size + head_size_v) / 8);
+  const unsigned grid = static_cast<unsigned>((n + CW_THREADS - 1) / CW_THREADS);
+  reshape_and_cache_diffkv_kernel<<<grid, CW_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(key), static_cast<const uint16_t*>(value),
+      static_cast<uint16_t*>(kv_cache), slot_mapping, num_tokens, num_kv_heads, head_size,
+      head_size_v, block_size, num_blocks, device_status);
+  return cudaGetLastError() == cudaSuccess ? PATTN_OK : PATTN_ERR_CUDA;
+}
 
 extern "C" pattn_status_t pattn_reshape_and_cache(const void* key, const void* value,
                                                   void* kv_cache, const int64_t* slot_mapping,

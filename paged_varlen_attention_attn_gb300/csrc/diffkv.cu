@@ -1,0 +1,219 @@
+// diffkv.cu -- attention over a DiffKV cache, where V has its own head size
+// (sm_103a).
+//
+// "[vLLM] other attention backends", FlashAttention DiffKV: the head size of V
+// (head_size_v) may differ from that of K, and the KV cache is then
+// asymmetric.  The page gives no shape; the layout read here is one tensor
+// [num_blocks][block_size][num_kv_heads][dk + dv], each row holding the
+// token's K (dk elements) and then its V (dv elements).  The attention is
+// pattn_varlen_fwd's (causal or not, sliding window, GQA, sinks); out is
+// [T][H][dv].
+//
+// A generic SIMT kernel for any dk, dv that are multiples of 32 up to 256,
+// not a tensor-core one.  One CTA per (query token, KV head): its four warps
+// share the KV head's G query heads (warp w takes heads w, w + 4, ...).  Key
+// tiles of 32 rows (K and V together) are staged in shared memory with each
+// row padded by one 32-bit word, so lane k reading word c of row k hits bank
+// (c + k * odd) mod 32: no conflicts.  Lane k scores key k of the tile; the
+// online softmax runs in log2 units; lane j accumulates output columns
+// j, j + 32, ... of each of its heads.
+#include "../../include/pattn.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace pattn {
+namespace {
+
+constexpr int DKV_THREADS = 128;
+constexpr int DKV_KEYS = 32;   // keys per staged tile
+constexpr int DKV_MAXH = 4;    // query heads per warp: G <= 16
+constexpr int DKV_MAXC = 8;    // output columns per lane: dv <= 256
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+template <bool HALF>
+__device__ __forceinline__ float2 unpack2(unsigned w) {
+  if constexpr (HALF) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  } else {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  }
+}
+
+template <bool HALF>
+__device__ __forceinline__ float elem(const void* base, int64_t i) {
+  if constexpr (HALF)
+    return __half2float(static_cast<const __half*>(base)[i]);
+  else
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+}
+
+template <bool HALF>
+__device__ __forceinline__ void store(void* base, int64_t i, float v) {
+  if constexpr (HALF)
+    static_cast<__half*>(base)[i] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  return v;
+}
+
+template <bool HALF>
+__global__ void __launch_bounds__(DKV_THREADS)
+    diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2) {
+  extern __shared__ unsigned kv_s[];           // [DKV_KEYS][rw] words, then q
+  const int rw = (dk + dv) / 2 + 1;            // words per staged row (padded)
+  float* q_s = reinterpret_cast<float*>(kv_s + DKV_KEYS * rw);   // [G][dk]
+  const int t = blockIdx.x, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  unsigned* status = &p.hdr->status;
+
+  // The request holding token t: the largest r with qsl[r] <= t.
+  if (t < p.qsl[0] || t >= p.qsl[p.B]) return;
+  int rl = 0, rh = p.B - 1;
+  while (rl < rh) {
+    const int mid = (rl + rh + 1) >> 1;
+    if (p.qsl[mid] <= t) rl = mid;
+    else rh = mid - 1;
+  }
+  const int r = rl;
+  const int t0 = p.qsl[r], q_len = p.qsl[r + 1] - t0, s = p.seq_lens[r];
+  const int64_t orow = (static_cast<int64_t>(t) * p.H + static_cast<int64_t>(g) * G) * dv;
+  if (t >= t0 + q_len || q_len > s || s > p.mbps * p.bs) {
+    // bad metadata: reported, the row's heads written as zeros
+    if (threadIdx.x == 0) flag_status(status, PATTN_DEV_BAD_METADATA);
+    for (int e = threadIdx.x; e < G * dv; e += DKV_THREADS) store<HALF>(p.out, orow + e, 0.f);
+    return;
+  }
+  const int pos = s - q_len + (t - t0);
+  const int hi = p.causal ? pos + 1 : s;
+  const int lo = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
+
+  // q of the G heads, as floats
+  const int64_t qrow = (static_cast<int64_t>(t) * p.H + static_cast<int64_t>(g) * G) * dk;
+  for (int e = threadIdx.x; e < G * dk; e += DKV_THREADS) q_s[e] = elem<HALF>(p.q, qrow + e);
+
+  float m_run[DKV_MAXH], l_run[DKV_MAXH], o[DKV_MAXH][DKV_MAXC];
+#pragma unroll
+  for (int jh = 0; jh < DKV_MAXH; ++jh) {
+    m_run[jh] = -INFINITY;
+    l_run[jh] = 0.f;
+#pragma unroll
+    for (int c = 0; c < DKV_MAXC; ++c) o[jh][c] = 0.f;
+  }
+  const int nc = dv / 32;
+  const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
+  const int row_words = (dk + dv) / 2;
+
+  for (int k0 = lo; k0 < hi; k0 += DKV_KEYS) {
+    __syncthreads();  // the previous tile is consumed (and q is staged)
+    // Stage keys k0 .. k0 + 31 (those below hi): K and V words of head g.
+    for (int e = threadIdx.x; e < DKV_KEYS * row_words; e += DKV_THREADS) {
+      const int kk = e / row_words, w = e - kk * row_words;
+      const int k = k0 + kk;
+      unsigned v = 0u;
+      if (k < hi) {
+        int blk = bt[k / p.bs];
+        if (blk < 0 || blk >= p.NB) {
+          flag_status(status, PATTN_DEV_BAD_METADATA);
+          blk = min(max(blk, 0), p.NB - 1);
+        }
+        const unsigned* row = reinterpret_cast<const unsigned*>(p.kv) +
+                              ((static_cast<int64_t>(blk) * p.bs + k % p.bs) * p.Hkv + g) * row_words;
+        v = row[w];
+      }
+      kv_s[kk * rw + w] = v;
+    }
+    __syncthreads();
+
+    const bool key_ok = k0 + lane < hi;
+#pragma unroll
+    for (int jh = 0; jh < DKV_MAXH; ++jh) {
+      const int hh = warp + 4 * jh;  // query head within the group
+      if (hh >= G) continue;
+      // score of key k0 + lane
+      const float* q = q_s + hh * dk;
+      const unsigned* krow = kv_s + lane * rw;
+      float dot0 = 0.f, dot1 = 0.f;
+      for (int c = 0; c < dk / 2; ++c) {
+        const float2 kf = unpack2<HALF>(krow[c]);
+        dot0 = fmaf(q[2 * c], kf.x, dot0);
+        dot1 = fmaf(q[2 * c + 1], kf.y, dot1);
+      }
+      const float s2 = key_ok ? (dot0 + dot1) * sl2 : -INFINITY;
+      const float m_new = fmaxf(m_run[jh], warp_max(s2));
+      if (m_new == -INFINITY) continue;  // nothing visible yet
+      const float alpha = exp2f(m_run[jh] - m_new);
+      const float pk = exp2f(s2 - m_new);
+      l_run[jh] = l_run[jh] * alpha + warp_sum(pk);
+      m_run[jh] = m_new;
+#pragma unroll
+      for (int c = 0; c < DKV_MAXC; ++c) o[jh][c] *= alpha;
+      // o += sum_k p_k V_k, lane owning columns lane + 32 c
+      for (int kk = 0; kk < DKV_KEYS; ++kk) {
+        const float pb = __shfl_sync(FULL_MASK, pk, kk);
+        const unsigned* vrow = kv_s + kk * rw + dk / 2;
+#pragma unroll
+        for (int c = 0; c < DKV_MAXC; ++c) {
+          if (c < nc) {
+            const int col = lane + 32 * c;
+            const float2 vf = unpack2<HALF>(vrow[col >> 1]);
+            o[jh][c] = fmaf(pb, (col & 1) ? vf.y : vf.x, o[jh][c]);
+          }
+        }
+      }
+    }
+  }
+
+  // normalise (with the head's sink) and write
+#pragma unroll
+  for (int jh = 0; jh < DKV_MAXH; ++jh) {
+    const int hh = warp + 4 * jh;
+    if (hh >= G) continue;
+    const float l_tot = l_run[jh] + sink_term(p.sinks, g * G + hh, m_run[jh]);
+    const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+#pragma unroll
+    for (int c = 0; c < DKV_MAXC; ++c)
+      if (c < nc) store<HALF>(p.out, orow + static_cast<int64_t>(hh) * dv + lane + 32 * c, o[jh][c] * inv);
+  }
+}
+
+}  // namespace
+
+size_t diffkv_smem_bytes(int G, int dk, int dv) {
+  return (static_cast<size_t>(DKV_KEYS) * ((dk + dv) / 2 + 1) + static_cast<size_t>(G) * dk) *
+         sizeof(float);
+}
+
+cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {
+  if (p.T == 0 || p.B == 0) return cudaSuccess;
+  const size_t smem = diffkv_smem_bytes(p.G, dk, dv);
+  const float sl2 = fmaxf(p.scale * LOG2E, 1e-30f);
+  const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>(p.Hkv));
+  if (p.kv_dtype == PATTN_KV_F16) {
+    cudaError_t e = cudaFuncSetAttribute(diffkv_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    diffkv_kernel<true><<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(diffkv_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    diffkv_kernel<false><<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pattn

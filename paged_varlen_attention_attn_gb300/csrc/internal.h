@@ -78,6 +78,10 @@ struct WsLayout {
 };
 WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int splits);
 
+// Attention over a DiffKV cache ([NB][bs][Hkv][dk + dv], K then V per row):
+// p.D is dk; out is [T][H][dv].
+cudaError_t launch_diffkv(const Problem& p, int dk, int dv);
+
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const Problem& p);
 // Decode-only calls: clears the status word and the partition counters and

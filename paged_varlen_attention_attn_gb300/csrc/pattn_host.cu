@@ -64,6 +64,13 @@ const float* ext_sinks(const pattn_ext_t* ext) {
                                                                                : nullptr;
 }
 
+// ext->head_size_v if the caller's struct has the field, else 0.
+int ext_head_size_v(const pattn_ext_t* ext) {
+  return ext->struct_size >= offsetof(pattn_ext_t, head_size_v) + sizeof(ext->head_size_v)
+             ? ext->head_size_v
+             : 0;
+}
+
 // Decode partition count.  A forced count is used as given; otherwise enough
 // partitions that there are about 8 (request, KV head, partition) items per
 // SM (2 to 4 decode CTAs, depending on how many KV heads one CTA serves), and
@@ -102,7 +109,14 @@ pattn_status_t validate(const pattn_ext_t* ext, int num_heads, int num_kv_heads,
       ext->num_blocks < 0 || ext->max_query_len < 0 || ext->max_seq_len < 0 ||
       ext->num_splits < 0 || ext->num_splits > PATTN_MAX_SPLITS)
     return PATTN_ERR_INVALID_ARGUMENT;
-  if (head_size != 64 && head_size != 128) return PATTN_ERR_UNSUPPORTED;
+  const int hv = ext_head_size_v(ext);
+  if (hv < 0) return PATTN_ERR_INVALID_ARGUMENT;
+  if (hv > 0) {  // DiffKV: the generic kernel's sizes
+    if (head_size % 32 || head_size < 32 || head_size > 256 || hv % 32 || hv > 256)
+      return PATTN_ERR_UNSUPPORTED;
+  } else if (head_size != 64 && head_size != 128) {
+    return PATTN_ERR_UNSUPPORTED;
+  }
   if (num_heads / num_kv_heads > 16) return PATTN_ERR_UNSUPPORTED;
   return PATTN_OK;
 }
@@ -129,6 +143,7 @@ pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* bl
   }
   if (!causal && window > 0) return PATTN_ERR_UNSUPPORTED;
   if (kv_dtype == PATTN_KV_FP8_E4M3 && ext->max_query_len > 1) return PATTN_ERR_UNSUPPORTED;
+  if (ext_head_size_v(ext) > 0 && kv_dtype == PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;
   // Prefill key tiles are 128 keys: a page must divide the tile or be a whole
   // number of tiles.
   if (ext->max_query_len > 1 && !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
@@ -334,6 +349,47 @@ WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int sp
   return L;
 }
 
+// pattn_varlen_fwd on a DiffKV cache: the status word is cleared, then one
+// generic kernel serves every row.
+pattn_status_t diffkv_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
+                          const int32_t* seq_lens, const int32_t* query_start_loc, void* out,
+                          float scale, int num_heads, int num_kv_heads, int head_size,
+                          int block_size, int window, int causal, int kv_dtype,
+                          const pattn_ext_t* ext) {
+  if (ext->workspace_bytes < sizeof(WsHeader)) return PATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (ext->num_seqs == 0 || ext->num_tokens == 0) return PATTN_OK;
+  if (ext->num_blocks == 0 || ext->max_blocks_per_seq == 0) return PATTN_ERR_INVALID_ARGUMENT;
+  Problem p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.kv = kv_cache;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.out = out;
+  p.scale = scale;
+  p.H = num_heads;
+  p.Hkv = num_kv_heads;
+  p.G = num_heads / num_kv_heads;
+  p.D = head_size;
+  p.bs = block_size;
+  p.window = window;
+  p.causal = causal;
+  p.kv_dtype = kv_dtype;
+  p.B = ext->num_seqs;
+  p.T = ext->num_tokens;
+  p.mbps = ext->max_blocks_per_seq;
+  p.bt_stride = p.mbps;
+  p.NB = ext->num_blocks;
+  p.sinks = ext_sinks(ext);
+  p.hdr = static_cast<WsHeader*>(ext->workspace);
+  p.stream = static_cast<cudaStream_t>(ext->stream);
+  if (cudaMemsetAsync(&p.hdr->status, 0, sizeof(unsigned), p.stream) != cudaSuccess)
+    return PATTN_ERR_CUDA;
+  if (launch_diffkv(p, head_size, ext_head_size_v(ext)) != cudaSuccess) return PATTN_ERR_CUDA;
+  return PATTN_OK;
+}
+
 }  // namespace pattn
 
 using namespace pattn;
@@ -396,6 +452,9 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
                                 kv_dtype, kv_scale, ext);
   if (v != PATTN_OK) return v;
   if (window < 0) window = 0;
+  if (ext_head_size_v(ext) > 0)
+    return diffkv_fwd(q, kv_cache, block_table, seq_lens, query_start_loc, out, scale, num_heads,
+                      num_kv_heads, head_size, block_size, window, causal, kv_dtype, ext);
 
   const int splits = choose_splits(ext, num_kv_heads, block_size, window);
   const WsLayout L = workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads, head_size,
@@ -519,6 +578,7 @@ pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache, const int3
                                 num_heads, num_kv_heads, head_size, block_size, window, causal,
                                 kv_dtype, kv_scale, ext);
   if (v != PATTN_OK) return v;
+  if (ext_head_size_v(ext) > 0) return PATTN_ERR_UNSUPPORTED;  // DiffKV: pattn_varlen_fwd only
   const int P = common_prefix_len;
   if (P <= 0 || P % block_size != 0) return PATTN_ERR_INVALID_ARGUMENT;
   if (causal != 1 || window > 0) return PATTN_ERR_UNSUPPORTED;

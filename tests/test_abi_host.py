@@ -36,10 +36,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_ext_struct_layout_matches_c():
-    # size_t + 7 ints (padded) + void* + size_t + void* + void** + float*
-    assert ctypes.sizeof(pa.Ext) == 80
+    # size_t + 7 ints (padded) + void* + size_t + void* + void** + float* + int
+    assert ctypes.sizeof(pa.Ext) == 88
     assert pa.Ext.workspace.offset == 40 and pa.Ext.stream.offset == 56
     assert pa.Ext.timing_events.offset == 64 and pa.Ext.sinks.offset == 72
+    assert pa.Ext.head_size_v.offset == 80
 
 
 def _ext(**kw):
@@ -209,3 +210,19 @@ def test_cascade_workspace_covers_partials(lib):
     casc = pa.pattn_cascade_workspace_bytes(e, 8, 2, 128, 16, 512, lib=lib)
     assert casc >= plain + 2 * 100 * 8 * (128 + 1) * 4
     assert pa.pattn_cascade_workspace_bytes(e, 8, 2, 128, 16, 20, lib=lib) == 0
+
+
+def test_diffkv_argument_checks(lib):
+    # the DiffKV layout takes head sizes that are multiples of 32 up to 256
+    ext = _ext(workspace=FAKE, workspace_bytes=1 << 30, head_size_v=96)
+    assert pa.pattn_workspace_bytes(ext, 4, 2, 160, 16, lib=lib) > 0
+    assert pa.pattn_workspace_bytes(ext, 4, 2, 48, 16, lib=lib) == 0   # head_size % 32
+    ext.head_size_v = 288
+    assert pa.pattn_workspace_bytes(ext, 4, 2, 64, 16, lib=lib) == 0
+    ext.head_size_v = -1
+    assert pa.pattn_workspace_bytes(ext, 4, 2, 64, 16, lib=lib) == 0
+    # e4m3 caches are not served in the DiffKV layout (a decode-only call,
+    # which e4m3 supports in the standard layout)
+    ext.head_size_v = 64
+    ext.max_query_len = 1
+    assert _call(lib, ext, kv_dtype=1, kv_scale=(1.0, 1.0)) == 2

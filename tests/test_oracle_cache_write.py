@@ -110,6 +110,39 @@ def cache_write_failures(lib):
     return bad
 
 
+def diffkv_write_failures(lib):
+    """DiffKV layout: a numpy scatter of [K | V] rows to their slots."""
+    bad = []
+    rng = np.random.default_rng(17)
+    T, Hkv, dk, dv, bs, nb = 29, 2, 16, 40, 16, 5
+    key = rng.integers(0, 1 << 16, (T, Hkv, dk), dtype=np.uint16)
+    val = rng.integers(0, 1 << 16, (T, Hkv, dv), dtype=np.uint16)
+    cache = rng.integers(0, 1 << 16, (nb, bs, Hkv, dk + dv), dtype=np.uint16)
+    slots = rng.permutation(nb * bs)[:T].astype(np.int64)
+    slots[::6] = -1
+    exp = cache.copy()
+    flat = exp.reshape(nb * bs, Hkv, dk + dv)
+    ok = slots >= 0
+    flat[slots[ok], :, :dk] = key[ok]
+    flat[slots[ok], :, dk:] = val[ok]
+    got = oracle.reshape_and_cache_diffkv(key, val, cache.copy(), slots, num_kv_heads=Hkv,
+                                          head_size=dk, head_size_v=dv, block_size=bs, lib=lib)
+    if not np.array_equal(got, exp):
+        bad.append("diffkv-scatter")
+    slots[1] = nb * bs
+    try:
+        oracle.reshape_and_cache_diffkv(key, val, cache.copy(), slots, num_kv_heads=Hkv,
+                                        head_size=dk, head_size_v=dv, block_size=bs, lib=lib)
+        bad.append("diffkv-slot-range")
+    except oracle.OracleError:
+        pass
+    return bad
+
+
+def test_diffkv_write_pins():
+    assert diffkv_write_failures(None) == []
+
+
 def test_encoder_pins():
     assert encoder_failures(None) == []
 
@@ -138,6 +171,10 @@ MUTATIONS = {
     "k_and_v_swapped": ("const uint16_t* src = kv ? value : key;",
                         "const uint16_t* src = kv ? key : value;"),
     "negative_slot_written": ("if (s < 0) continue;", "if (s < 0) s = 0;"),
+    "diffkv_v_at_row_start": ("row[head_size + j] = value[", "row[j] = value["),
+    "diffkv_row_width_k": ("* (int64_t)width;", "* (int64_t)head_size;"),
+    "diffkv_value_stride_k": ("value[((int64_t)t * num_kv_heads + h) * head_size_v + j]",
+                              "value[((int64_t)t * num_kv_heads + h) * head_size + j]"),
 }
 
 
@@ -148,10 +185,11 @@ def test_planted_mistakes_are_caught(name, tmp_path):
     assert src.count(old) == 1, f"mutation anchor for {name} not found once"
     src = src.replace(old, new)
     if name == "negative_slot_written":
-        src = src.replace("const int64_t s = slot_mapping[t];", "int64_t s = slot_mapping[t];")
+        src = src.replace("const int64_t s = slot_mapping[t];", "int64_t s = slot_mapping[t];", 1)
     (tmp_path / "mut.c").write_text(src)
     so = tmp_path / "libmut.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so),
                     str(tmp_path / "mut.c"), "-lm"], check=True)
     lib = oracle.bind(str(so))
-    assert encoder_failures(lib) + cache_write_failures(lib), f"{name} went unnoticed"
+    assert (encoder_failures(lib) + cache_write_failures(lib) + diffkv_write_failures(lib)), \
+        f"{name} went unnoticed"
