@@ -12,11 +12,13 @@
 // A generic SIMT kernel for any dk, dv that are multiples of 32 up to 256,
 // not a tensor-core one.  One CTA per (query token, KV head): its four warps
 // share the KV head's G query heads (warp w takes heads w, w + 4, ...).  Key
-// tiles of 32 rows (K and V together) are staged in shared memory with each
-// row padded by one 32-bit word, so lane k reading word c of row k hits bank
-// (c + k * odd) mod 32: no conflicts.  Lane k scores key k of the tile; the
-// online softmax runs in log2 units; lane j accumulates output columns
-// j, j + 32, ... of each of its heads.
+// tiles of 32 rows (K and V together) are copied into shared memory with
+// 16-byte cp.async (rows past the visible range zero-filled), double
+// buffered so the next tile streams in while the current one is used.  Each
+// staged row is padded by 16 bytes, so the 16-byte reads of lane k in row k
+// fall on distinct banks within every quarter warp.  Lane k scores key k of
+// the tile; the online softmax runs in log2 units; lane j accumulates output
+// columns j, j + 32, ... of each of its heads.
 #include "../../include/pattn.h"
 #include "common.cuh"
 #include "internal.h"
@@ -67,12 +69,34 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, bool valid) {
+  // src-size 0 fills the 16 bytes with zeros and reads nothing
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <bool HALF>
+__device__ __forceinline__ float half_bits_to_float(unsigned short b) {
+  if constexpr (HALF)
+    return __half2float(__ushort_as_half(b));
+  else
+    return __bfloat162float(__ushort_as_bfloat16(b));
+}
+
 template <bool HALF>
 __global__ void __launch_bounds__(DKV_THREADS)
     diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2) {
-  extern __shared__ unsigned kv_s[];           // [DKV_KEYS][rw] words, then q
-  const int rw = (dk + dv) / 2 + 1;            // words per staged row (padded)
-  float* q_s = reinterpret_cast<float*>(kv_s + DKV_KEYS * rw);   // [G][dk]
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int rbytes = (dk + dv) * 2;   // a cache row: K then V
+  const int rs = rbytes + 16;         // staged row stride
+  const int cpr = rbytes / 16;        // 16-byte pieces of a row
+  float* q_s = reinterpret_cast<float*>(smem + 2 * DKV_KEYS * rs);   // [G][dk]
   const int t = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
@@ -98,6 +122,36 @@ __global__ void __launch_bounds__(DKV_THREADS)
   const int pos = s - q_len + (t - t0);
   const int hi = p.causal ? pos + 1 : s;
   const int lo = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
+  const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
+  const unsigned char* cache = static_cast<const unsigned char*>(p.kv);
+
+  // Copy keys k0 .. k0 + 31 into buffer b: warp w copies rows w, w + 4, ...
+  // The 32 keys' row offsets come from one coalesced block-table load (lane
+  // = key) and reach each row's copy through a shuffle.
+  auto stage = [&](int b, int k0) {
+    unsigned char* dst = smem + b * DKV_KEYS * rs;
+    const int kl = k0 + lane;
+    int64_t row_off = -1;  // byte offset of key kl's row, or -1 past the range
+    if (kl < hi) {
+      int blk = bt[kl / p.bs];
+      if (blk < 0 || blk >= p.NB) {
+        flag_status(status, PATTN_DEV_BAD_METADATA);
+        blk = min(max(blk, 0), p.NB - 1);
+      }
+      row_off = ((static_cast<int64_t>(blk) * p.bs + kl % p.bs) * p.Hkv + g) * rbytes;
+    }
+#pragma unroll
+    for (int kk = warp; kk < DKV_KEYS; kk += 4) {
+      const int64_t off = __shfl_sync(FULL_MASK, row_off, kk);
+      const bool ok = off >= 0;
+      const unsigned char* src = cache + (ok ? off : 0);
+      for (int c = lane; c < cpr; c += 32) cp_async16(dst + kk * rs + c * 16, src + (ok ? c * 16 : 0), ok);
+    }
+    cp_async_commit();
+  };
+
+  const int ntiles = (hi > lo) ? (hi - lo + DKV_KEYS - 1) / DKV_KEYS : 0;
+  if (ntiles > 0) stage(0, lo);
 
   // q of the G heads, as floats
   const int64_t qrow = (static_cast<int64_t>(t) * p.H + static_cast<int64_t>(g) * G) * dk;
@@ -112,67 +166,64 @@ __global__ void __launch_bounds__(DKV_THREADS)
     for (int c = 0; c < DKV_MAXC; ++c) o[jh][c] = 0.f;
   }
   const int nc = dv / 32;
-  const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
-  const int row_words = (dk + dv) / 2;
 
-  for (int k0 = lo; k0 < hi; k0 += DKV_KEYS) {
-    __syncthreads();  // the previous tile is consumed (and q is staged)
-    // Stage keys k0 .. k0 + 31 (those below hi): K and V words of head g.
-    for (int e = threadIdx.x; e < DKV_KEYS * row_words; e += DKV_THREADS) {
-      const int kk = e / row_words, w = e - kk * row_words;
-      const int k = k0 + kk;
-      unsigned v = 0u;
-      if (k < hi) {
-        int blk = bt[k / p.bs];
-        if (blk < 0 || blk >= p.NB) {
-          flag_status(status, PATTN_DEV_BAD_METADATA);
-          blk = min(max(blk, 0), p.NB - 1);
-        }
-        const unsigned* row = reinterpret_cast<const unsigned*>(p.kv) +
-                              ((static_cast<int64_t>(blk) * p.bs + k % p.bs) * p.Hkv + g) * row_words;
-        v = row[w];
-      }
-      kv_s[kk * rw + w] = v;
+  for (int j = 0; j < ntiles; ++j) {
+    const int k0 = lo + j * DKV_KEYS;
+    if (j + 1 < ntiles) {
+      stage((j + 1) & 1, k0 + DKV_KEYS);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    __syncthreads();
-
+    __syncthreads();  // tile j (and q) in shared memory for every thread
+    const unsigned char* tb = smem + (j & 1) * DKV_KEYS * rs;
     const bool key_ok = k0 + lane < hi;
 #pragma unroll
     for (int jh = 0; jh < DKV_MAXH; ++jh) {
       const int hh = warp + 4 * jh;  // query head within the group
       if (hh >= G) continue;
       // score of key k0 + lane
-      const float* q = q_s + hh * dk;
-      const unsigned* krow = kv_s + lane * rw;
+      const float4* q4 = reinterpret_cast<const float4*>(q_s + hh * dk);
+      const uint4* krow = reinterpret_cast<const uint4*>(tb + lane * rs);
       float dot0 = 0.f, dot1 = 0.f;
-      for (int c = 0; c < dk / 2; ++c) {
-        const float2 kf = unpack2<HALF>(krow[c]);
-        dot0 = fmaf(q[2 * c], kf.x, dot0);
-        dot1 = fmaf(q[2 * c + 1], kf.y, dot1);
+#pragma unroll 4
+      for (int c = 0; c < dk / 8; ++c) {
+        const uint4 w = krow[c];
+        const float4 qa = q4[2 * c], qb = q4[2 * c + 1];
+        float2 f = unpack2<HALF>(w.x);
+        dot0 = fmaf(qa.x, f.x, dot0);
+        dot1 = fmaf(qa.y, f.y, dot1);
+        f = unpack2<HALF>(w.y);
+        dot0 = fmaf(qa.z, f.x, dot0);
+        dot1 = fmaf(qa.w, f.y, dot1);
+        f = unpack2<HALF>(w.z);
+        dot0 = fmaf(qb.x, f.x, dot0);
+        dot1 = fmaf(qb.y, f.y, dot1);
+        f = unpack2<HALF>(w.w);
+        dot0 = fmaf(qb.z, f.x, dot0);
+        dot1 = fmaf(qb.w, f.y, dot1);
       }
       const float s2 = key_ok ? (dot0 + dot1) * sl2 : -INFINITY;
       const float m_new = fmaxf(m_run[jh], warp_max(s2));
       if (m_new == -INFINITY) continue;  // nothing visible yet
-      const float alpha = exp2f(m_run[jh] - m_new);
-      const float pk = exp2f(s2 - m_new);
+      const float alpha = fast_exp2(m_run[jh] - m_new);
+      const float pk = fast_exp2(s2 - m_new);
       l_run[jh] = l_run[jh] * alpha + warp_sum(pk);
       m_run[jh] = m_new;
 #pragma unroll
       for (int c = 0; c < DKV_MAXC; ++c) o[jh][c] *= alpha;
       // o += sum_k p_k V_k, lane owning columns lane + 32 c
+#pragma unroll 8
       for (int kk = 0; kk < DKV_KEYS; ++kk) {
         const float pb = __shfl_sync(FULL_MASK, pk, kk);
-        const unsigned* vrow = kv_s + kk * rw + dk / 2;
+        const unsigned short* vrow =
+            reinterpret_cast<const unsigned short*>(tb + kk * rs + dk * 2) + lane;
 #pragma unroll
-        for (int c = 0; c < DKV_MAXC; ++c) {
-          if (c < nc) {
-            const int col = lane + 32 * c;
-            const float2 vf = unpack2<HALF>(vrow[col >> 1]);
-            o[jh][c] = fmaf(pb, (col & 1) ? vf.y : vf.x, o[jh][c]);
-          }
-        }
+        for (int c = 0; c < DKV_MAXC; ++c)
+          if (c < nc) o[jh][c] = fmaf(pb, half_bits_to_float<HALF>(vrow[32 * c]), o[jh][c]);
       }
     }
+    __syncthreads();  // tile j used: its buffer may be refilled
   }
 
   // normalise (with the head's sink) and write
@@ -191,8 +242,8 @@ __global__ void __launch_bounds__(DKV_THREADS)
 }  // namespace
 
 size_t diffkv_smem_bytes(int G, int dk, int dv) {
-  return (static_cast<size_t>(DKV_KEYS) * ((dk + dv) / 2 + 1) + static_cast<size_t>(G) * dk) *
-         sizeof(float);
+  return 2 * static_cast<size_t>(DKV_KEYS) * ((dk + dv) * 2 + 16) +
+         static_cast<size_t>(G) * dk * sizeof(float);
 }
 
 cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {
