@@ -146,8 +146,9 @@ typedef struct {
  *   block_size      a multiple of 16 (the ValueError of get_kv_cache_shape)
  *   window          <= 0: no window; > 0: keys with p - k < window are visible
  *   causal          1: k <= p; 0: every key < seq_len (then window must be <= 0)
- *   kv_dtype        a pattn_kv_dtype_t.  e4m3 runs decode rows only
- *                   (a batch with max_query_len > 1 returns UNSUPPORTED)
+ *   kv_dtype        a pattn_kv_dtype_t.  With e4m3, decode rows run on the
+ *                   bandwidth-bound decode kernel and prefill rows on a
+ *                   generic (SIMT, not tensor-core) kernel
  *   kv_scale        host float[2] {k_scale, v_scale}; required for e4m3, ignored
  *                   for bf16 (may be NULL)
  *   ext             host sizes, workspace and stream (see pattn_ext_t)

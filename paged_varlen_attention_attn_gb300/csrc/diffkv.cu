@@ -9,6 +9,11 @@
 // pattn_varlen_fwd's (causal or not, sliding window, GQA, sinks); out is
 // [T][H][dv].
 //
+// The same generic kernel serves the prefill rows of an e4m3 cache in the
+// standard layout ([2][num_blocks][block_size][num_kv_heads][d]: K and V rows
+// are fetched from their two planes into one staged row), widening the codes
+// with the hardware pair conversion and applying the per-tensor scales.
+//
 // A generic SIMT kernel for any dk, dv that are multiples of 32 up to 256,
 // not a tensor-core one.  One CTA per (query token, KV head): its four warps
 // share the KV head's G query heads (warp w takes heads w, w + 4, ...).  Key
@@ -89,13 +94,60 @@ __device__ __forceinline__ float half_bits_to_float(unsigned short b) {
     return __bfloat162float(__ushort_as_bfloat16(b));
 }
 
+// Two e4m3 codes (the low 16 bits of v) as floats, exactly (the pair
+// conversion widens to f16; every e4m3 value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(unsigned v) {
+  unsigned r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
+  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+}
+
+// Cache element types of the generic kernel.
+constexpr int GK_BF16 = 0, GK_E4M3 = 1, GK_F16 = 2;
+
+// dot(q[0..7], 8 16-bit values in w) into (d0, d1)
 template <bool HALF>
+__device__ __forceinline__ void dot8(const float4 qa, const float4 qb, const uint4 w, float& d0,
+                                     float& d1) {
+  float2 f = unpack2<HALF>(w.x);
+  d0 = fmaf(qa.x, f.x, d0);
+  d1 = fmaf(qa.y, f.y, d1);
+  f = unpack2<HALF>(w.y);
+  d0 = fmaf(qa.z, f.x, d0);
+  d1 = fmaf(qa.w, f.y, d1);
+  f = unpack2<HALF>(w.z);
+  d0 = fmaf(qb.x, f.x, d0);
+  d1 = fmaf(qb.y, f.y, d1);
+  f = unpack2<HALF>(w.w);
+  d0 = fmaf(qb.z, f.x, d0);
+  d1 = fmaf(qb.w, f.y, d1);
+}
+
+// dot(q[0..3], 4 e4m3 codes in w) into (d0, d1)
+__device__ __forceinline__ void dot4_e4m3(const float4 q, unsigned w, float& d0, float& d1) {
+  float2 f = e4m3x2_to_float2(w);
+  d0 = fmaf(q.x, f.x, d0);
+  d1 = fmaf(q.y, f.y, d1);
+  f = e4m3x2_to_float2(w >> 16);
+  d0 = fmaf(q.z, f.x, d0);
+  d1 = fmaf(q.w, f.y, d1);
+}
+
+// KV: GK_BF16, GK_E4M3 (with bf16 q and out) or GK_F16 (f16 q and out).
+// split: the standard layout (K and V planes); else the DiffKV layout.
+// skip_decode: rows of requests with query_len 1 are left to the decode kernel.
+template <int KV>
 __global__ void __launch_bounds__(DKV_THREADS)
-    diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2) {
+    diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2, float out_scale,
+                  int split, int skip_decode) {
+  constexpr bool HALF = KV == GK_F16;       // q, out (and a 16-bit cache) are f16
+  constexpr int ES = (KV == GK_E4M3) ? 1 : 2;
   extern __shared__ __align__(16) unsigned char smem[];
-  const int rbytes = (dk + dv) * 2;   // a cache row: K then V
+  const int kbytes = dk * ES;
+  const int rbytes = (dk + dv) * ES;  // a staged row: K then V
   const int rs = rbytes + 16;         // staged row stride
   const int cpr = rbytes / 16;        // 16-byte pieces of a row
+  const int ck = kbytes / 16;         // ... of its K part
   float* q_s = reinterpret_cast<float*>(smem + 2 * DKV_KEYS * rs);   // [G][dk]
   const int t = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -112,6 +164,7 @@ __global__ void __launch_bounds__(DKV_THREADS)
   }
   const int r = rl;
   const int t0 = p.qsl[r], q_len = p.qsl[r + 1] - t0, s = p.seq_lens[r];
+  if (skip_decode && q_len == 1) return;
   const int64_t orow = (static_cast<int64_t>(t) * p.H + static_cast<int64_t>(g) * G) * dv;
   if (t >= t0 + q_len || q_len > s || s > p.mbps * p.bs) {
     // bad metadata: reported, the row's heads written as zeros
@@ -124,6 +177,12 @@ __global__ void __launch_bounds__(DKV_THREADS)
   const int lo = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
   const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
   const unsigned char* cache = static_cast<const unsigned char*>(p.kv);
+  // Source bytes of a row (the DiffKV row, or the K row of the standard
+  // layout) and the extra offset of the V pieces (the V plane lies
+  // NB * bs * Hkv rows after the K plane; a DiffKV row continues in place).
+  const int64_t src_row = split ? kbytes : rbytes;
+  const int64_t v_extra =
+      split ? static_cast<int64_t>(p.NB) * p.bs * p.Hkv * kbytes - kbytes : 0;
 
   // Copy keys k0 .. k0 + 31 into buffer b: warp w copies rows w, w + 4, ...
   // The 32 keys' row offsets come from one coalesced block-table load (lane
@@ -138,14 +197,15 @@ __global__ void __launch_bounds__(DKV_THREADS)
         flag_status(status, PATTN_DEV_BAD_METADATA);
         blk = min(max(blk, 0), p.NB - 1);
       }
-      row_off = ((static_cast<int64_t>(blk) * p.bs + kl % p.bs) * p.Hkv + g) * rbytes;
+      row_off = ((static_cast<int64_t>(blk) * p.bs + kl % p.bs) * p.Hkv + g) * src_row;
     }
 #pragma unroll
     for (int kk = warp; kk < DKV_KEYS; kk += 4) {
       const int64_t off = __shfl_sync(FULL_MASK, row_off, kk);
       const bool ok = off >= 0;
       const unsigned char* src = cache + (ok ? off : 0);
-      for (int c = lane; c < cpr; c += 32) cp_async16(dst + kk * rs + c * 16, src + (ok ? c * 16 : 0), ok);
+      for (int c = lane; c < cpr; c += 32)
+        cp_async16(dst + kk * rs + c * 16, src + (ok ? c * 16 + (c >= ck ? v_extra : 0) : 0), ok);
     }
     cp_async_commit();
   };
@@ -187,21 +247,16 @@ __global__ void __launch_bounds__(DKV_THREADS)
       const uint4* krow = reinterpret_cast<const uint4*>(tb + lane * rs);
       float dot0 = 0.f, dot1 = 0.f;
 #pragma unroll 4
-      for (int c = 0; c < dk / 8; ++c) {
+      for (int c = 0; c < ck; ++c) {
         const uint4 w = krow[c];
-        const float4 qa = q4[2 * c], qb = q4[2 * c + 1];
-        float2 f = unpack2<HALF>(w.x);
-        dot0 = fmaf(qa.x, f.x, dot0);
-        dot1 = fmaf(qa.y, f.y, dot1);
-        f = unpack2<HALF>(w.y);
-        dot0 = fmaf(qa.z, f.x, dot0);
-        dot1 = fmaf(qa.w, f.y, dot1);
-        f = unpack2<HALF>(w.z);
-        dot0 = fmaf(qb.x, f.x, dot0);
-        dot1 = fmaf(qb.y, f.y, dot1);
-        f = unpack2<HALF>(w.w);
-        dot0 = fmaf(qb.z, f.x, dot0);
-        dot1 = fmaf(qb.w, f.y, dot1);
+        if constexpr (KV == GK_E4M3) {  // 16 codes
+          dot4_e4m3(q4[4 * c], w.x, dot0, dot1);
+          dot4_e4m3(q4[4 * c + 1], w.y, dot0, dot1);
+          dot4_e4m3(q4[4 * c + 2], w.z, dot0, dot1);
+          dot4_e4m3(q4[4 * c + 3], w.w, dot0, dot1);
+        } else {                         // 8 16-bit values
+          dot8<HALF>(q4[2 * c], q4[2 * c + 1], w, dot0, dot1);
+        }
       }
       const float s2 = key_ok ? (dot0 + dot1) * sl2 : -INFINITY;
       const float m_new = fmaxf(m_run[jh], warp_max(s2));
@@ -216,11 +271,18 @@ __global__ void __launch_bounds__(DKV_THREADS)
 #pragma unroll 8
       for (int kk = 0; kk < DKV_KEYS; ++kk) {
         const float pb = __shfl_sync(FULL_MASK, pk, kk);
-        const unsigned short* vrow =
-            reinterpret_cast<const unsigned short*>(tb + kk * rs + dk * 2) + lane;
+        if constexpr (KV == GK_E4M3) {
+          const unsigned char* vrow = tb + kk * rs + kbytes + lane;
 #pragma unroll
-        for (int c = 0; c < DKV_MAXC; ++c)
-          if (c < nc) o[jh][c] = fmaf(pb, half_bits_to_float<HALF>(vrow[32 * c]), o[jh][c]);
+          for (int c = 0; c < DKV_MAXC; ++c)
+            if (c < nc) o[jh][c] = fmaf(pb, e4m3x2_to_float2(vrow[32 * c]).x, o[jh][c]);
+        } else {
+          const unsigned short* vrow =
+              reinterpret_cast<const unsigned short*>(tb + kk * rs + kbytes) + lane;
+#pragma unroll
+          for (int c = 0; c < DKV_MAXC; ++c)
+            if (c < nc) o[jh][c] = fmaf(pb, half_bits_to_float<HALF>(vrow[32 * c]), o[jh][c]);
+        }
       }
     }
     __syncthreads();  // tile j used: its buffer may be refilled
@@ -232,7 +294,7 @@ __global__ void __launch_bounds__(DKV_THREADS)
     const int hh = warp + 4 * jh;
     if (hh >= G) continue;
     const float l_tot = l_run[jh] + sink_term(p.sinks, g * G + hh, m_run[jh]);
-    const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+    const float inv = (l_tot > 0.f) ? out_scale / l_tot : 0.f;
 #pragma unroll
     for (int c = 0; c < DKV_MAXC; ++c)
       if (c < nc) store<HALF>(p.out, orow + static_cast<int64_t>(hh) * dv + lane + 32 * c, o[jh][c] * inv);
@@ -241,30 +303,35 @@ __global__ void __launch_bounds__(DKV_THREADS)
 
 }  // namespace
 
-size_t diffkv_smem_bytes(int G, int dk, int dv) {
-  return 2 * static_cast<size_t>(DKV_KEYS) * ((dk + dv) * 2 + 16) +
+size_t generic_smem_bytes(int G, int dk, int dv, int es) {
+  return 2 * static_cast<size_t>(DKV_KEYS) * ((dk + dv) * es + 16) +
          static_cast<size_t>(G) * dk * sizeof(float);
 }
 
-cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {
-  if (p.T == 0 || p.B == 0) return cudaSuccess;
-  const size_t smem = diffkv_smem_bytes(p.G, dk, dv);
-  const float sl2 = fmaxf(p.scale * LOG2E, 1e-30f);
+template <int KV>
+cudaError_t launch_generic_t(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
+  const size_t smem = generic_smem_bytes(p.G, dk, dv, KV == GK_E4M3 ? 1 : 2);
+  const float sl2 = fmaxf(p.scale * LOG2E * (KV == GK_E4M3 ? p.k_scale : 1.f), 1e-30f);
+  const float out_scale = (KV == GK_E4M3) ? p.v_scale : 1.f;
   const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>(p.Hkv));
-  if (p.kv_dtype == PATTN_KV_F16) {
-    cudaError_t e = cudaFuncSetAttribute(diffkv_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    diffkv_kernel<true><<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(diffkv_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    diffkv_kernel<false><<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2);
-  }
+  cudaError_t e = cudaFuncSetAttribute(diffkv_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  diffkv_kernel<KV><<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2, out_scale,
+                                                          split ? 1 : 0, skip_decode ? 1 : 0);
   return cudaGetLastError();
+}
+
+cudaError_t launch_generic(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
+  if (p.T == 0 || p.B == 0) return cudaSuccess;
+  if (p.kv_dtype == PATTN_KV_F16) return launch_generic_t<GK_F16>(p, dk, dv, split, skip_decode);
+  if (p.kv_dtype == PATTN_KV_FP8_E4M3)
+    return launch_generic_t<GK_E4M3>(p, dk, dv, split, skip_decode);
+  return launch_generic_t<GK_BF16>(p, dk, dv, split, skip_decode);
+}
+
+cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {
+  return launch_generic(p, dk, dv, false, false);
 }
 
 }  // namespace pattn

@@ -142,11 +142,12 @@ pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* bl
       return PATTN_ERR_INVALID_ARGUMENT;
   }
   if (!causal && window > 0) return PATTN_ERR_UNSUPPORTED;
-  if (kv_dtype == PATTN_KV_FP8_E4M3 && ext->max_query_len > 1) return PATTN_ERR_UNSUPPORTED;
   if (ext_head_size_v(ext) > 0 && kv_dtype == PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;
-  // Prefill key tiles are 128 keys: a page must divide the tile or be a whole
-  // number of tiles.
-  if (ext->max_query_len > 1 && !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
+  // Prefill key tiles of the tensor-core kernel are 128 keys: a page must
+  // divide the tile or be a whole number of tiles.  (e4m3 prefill rows go to
+  // the generic kernel, which takes any block size.)
+  if (ext->max_query_len > 1 && kv_dtype != PATTN_KV_FP8_E4M3 &&
+      !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
     return PATTN_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(kv_cache) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
       (reinterpret_cast<uintptr_t>(out) & 15) ||
@@ -513,15 +514,20 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
       cudaEventRecord(static_cast<cudaEvent_t>(ext->timing_events[idx]), p.stream);
   };
 
+  // Prefill rows run on the tensor-core kernel, except over an e4m3 cache,
+  // where the generic kernel serves them after the decode kernel.
+  const bool tc_prefill = ext->max_query_len > 1 && kv_dtype != PATTN_KV_FP8_E4M3;
+  const bool generic_prefill = ext->max_query_len > 1 && kv_dtype == PATTN_KV_FP8_E4M3;
   mark(0);
-  if (ext->max_query_len > 1) {
+  if (tc_prefill) {
     // The plan kernel clears the header and the counters and builds the
     // prefill work list.
     if (launch_plan(p) != cudaSuccess) return PATTN_ERR_CUDA;
   } else {
-    // Decode only: nothing to plan (the decode kernel validates its own
-    // rows); clear the status word and the partition counters and order the
-    // requests longest first.
+    // No tensor-core prefill (decode only, or an e4m3 cache): nothing to plan
+    // (the decode and generic kernels validate their own rows); clear the
+    // status word and the partition counters and order the requests longest
+    // first.
     if (launch_decode_prep(p) != cudaSuccess) return PATTN_ERR_CUDA;
   }
   // The decode kernel is a programmatic dependent of the kernel before it,
@@ -532,12 +538,12 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   // prefill CTAs.
   const bool timed = ext->timing_events != nullptr;
   p.pdl_launch = timed ? 0 : 1;
-  p.pdl_wait = (ext->max_query_len > 1) ? 0 : 1;
-  p.pdl_trigger = (!timed && ext->max_query_len > 1) ? 1 : 0;
+  p.pdl_wait = tc_prefill ? 0 : 1;
+  p.pdl_trigger = (!timed && tc_prefill) ? 1 : 0;
   mark(1);
   mark(2);
 
-  if (ext->max_query_len > 1) {
+  if (tc_prefill) {
     CUtensorMap qmap, kvmap;
     if (!encode_q_map(&qmap, q, kv_dtype, num_heads, head_size, ext->num_tokens))
       return PATTN_ERR_CUDA;
@@ -553,6 +559,9 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
                          ext->num_blocks, decode_heads_per_cta(num_kv_heads, head_size, kv_dtype)))
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
+  if (generic_prefill &&
+      launch_generic(p, head_size, head_size, /*split=*/true, /*skip_decode=*/true) != cudaSuccess)
+    return PATTN_ERR_CUDA;
   mark(5);
   // The partitions are merged inside the decode kernel (its last CTA of each
   // request and KV-head group); the combine phase is empty.
