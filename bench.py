@@ -348,8 +348,9 @@ def run_ours(args, spec, world, rank, local_rank):
 def run_e2e(args, case, spec, counts, dev, stream, ca, ws):
     """One serving step through the public API, from host memory: the KV pool
     stays resident on the GPU (it is the cache earlier steps filled); every
-    step copies from pinned host memory the queries, the new tokens' key and
-    value rows and their slots, and the metadata, writes the new rows into
+    step copies from pinned host memory (one packed buffer, one copy) the
+    queries, the new tokens' key and value rows and their slots, and the
+    metadata, writes the new rows into
     the cache (pattn_reshape_and_cache), runs attention (pattn_varlen_fwd)
     and reads the output back.  The new tokens are each request's query
     positions ctx .. s-1, so the cache write touches exactly the slots the
@@ -368,14 +369,26 @@ def run_e2e(args, case, spec, counts, dev, stream, ca, ws):
     kv_dt = torch.float16 if spec.kv_dtype == 2 else torch.bfloat16
     new_k = torch.randn(T, Hkv, d, generator=g).to(kv_dt)
     new_v = torch.randn(T, Hkv, d, generator=g).to(kv_dt)
-    host = {"q": case.q.cpu(), "new_k": new_k, "new_v": new_v, "slots": slots,
-            "block_table": case.block_table.cpu(), "seq_lens": case.seq_lens.cpu(),
-            "query_start_loc": case.query_start_loc.cpu()}
-    host = {k: v.pin_memory() for k, v in host.items()}
-    dev_bufs = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    parts = {"q": case.q.cpu(), "new_k": new_k, "new_v": new_v, "slots": slots,
+             "block_table": case.block_table.cpu(), "seq_lens": case.seq_lens.cpu(),
+             "query_start_loc": case.query_start_loc.cpu()}
+    # The inputs of a step travel in one pinned buffer and one copy, as a
+    # serving engine packs them, each part at a 256-byte aligned offset; the
+    # device side holds views into one device buffer.
+    offs, total = {}, 0
+    for k, v in parts.items():
+        offs[k] = total
+        total += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_all = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_all = torch.empty(total, dtype=torch.uint8, device=dev)
+    dev_bufs = {}
+    for k, v in parts.items():
+        n = v.numel() * v.element_size()
+        host_all[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
+        dev_bufs[k] = dev_all[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
     out_dev = torch.empty_like(case.q)
     out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d = sum(v.numel() * v.element_size() for v in parts.values())
     d2h = out_host.numel() * out_host.element_size()
     ks = case.kv_scale if spec.kv_dtype == 1 else None
     K = max(3, min(args.steps, args.e2e_steps))
@@ -385,8 +398,7 @@ def run_e2e(args, case, spec, counts, dev, stream, ca, ws):
         for i in range(K + 2):
             if i >= 2:
                 ev[i - 2][0].record()
-            for k, v in host.items():
-                dev_bufs[k].copy_(v, non_blocking=True)
+            dev_all.copy_(host_all, non_blocking=True)
             pa.reshape_and_cache(dev_bufs["new_k"], dev_bufs["new_v"], case.kv_cache,
                                  dev_bufs["slots"], block_size=bs, kv_dtype=spec.kv_dtype,
                                  kv_scale=ks, stream=stream)
@@ -399,7 +411,7 @@ def run_e2e(args, case, spec, counts, dev, stream, ca, ws):
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     ms = max_over_ranks(ms, device=dev)
-    del dev_bufs, host
+    del dev_bufs, dev_all, host_all
     return dict(ms=ms, h2d=h2d, d2h=d2h)
 
 
@@ -834,7 +846,8 @@ def main():
                        "ms_per_step": round(e["ms"], 4),
                        "note": "serving step through the public API: q, the new tokens' K/V "
                                "rows and slots, block table and lengths copied from pinned "
-                               "host memory; the new rows written into the resident cache "
+                               "host memory in one packed copy; the new rows written into "
+                               "the resident cache "
                                "(pattn_reshape_and_cache); attention; output read back"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         max_rows = args.oracle_rows or {1: 10**9, 2: 2048, 3: 2048, 4: 512, 5: 128}.get(args.config, 256)
