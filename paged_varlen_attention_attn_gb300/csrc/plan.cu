@@ -93,16 +93,20 @@ __device__ int scan_descending(int* hist, int* warp_sums) {
 }
 
 // Writes p.decode_order: every request, by decreasing decode cost (a counting
-// sort; the order within one cost is whatever the atomics give).
+// sort; the order within one cost is whatever the atomics give).  A thread's
+// first request keeps its cost in a register between the two passes, so the
+// metadata is read once (the decode kernel waits for this).
 __device__ void order_decodes(const Problem& p, int* hist, int* warp_sums) {
   const int tid = threadIdx.x;
+  const int cost0 = (tid < p.B) ? decode_cost(p, tid) : 0;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
-  for (int r = tid; r < p.B; r += PLAN_THREADS) atomicAdd(&hist[decode_cost(p, r)], 1);
+  for (int r = tid; r < p.B; r += PLAN_THREADS)
+    atomicAdd(&hist[r == tid ? cost0 : decode_cost(p, r)], 1);
   __syncthreads();
   scan_descending(hist, warp_sums);
   for (int r = tid; r < p.B; r += PLAN_THREADS)
-    p.decode_order[atomicAdd(&hist[decode_cost(p, r)], 1)] = r;
+    p.decode_order[atomicAdd(&hist[r == tid ? cost0 : decode_cost(p, r)], 1)] = r;
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
