@@ -753,6 +753,9 @@ def main():
                     help="--op cascade: shared prefix length in keys (multiple of 16)")
     ap.add_argument("--f16", action="store_true",
                     help="run the workload with f16 q, cache and output (16-bit workloads only)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="run the workload over an e4m3 cache (per-tensor scales); prefill "
+                         "rows then run on the generic kernel")
     ap.add_argument("--splits", type=int, default=None,
                     help="force the decode partition count (default: the workload's own, "
                          "0 = the library's choice)")
@@ -774,6 +777,10 @@ def main():
         if spec.kv_dtype != W.KV_BF16:
             raise SystemExit("--f16 needs a 16-bit workload")
         spec = dataclasses.replace(spec, kv_dtype=W.KV_F16, name=spec.name + "_f16")
+    if args.fp8:
+        if spec.kv_dtype != W.KV_BF16:
+            raise SystemExit("--fp8 needs a bf16 workload")
+        spec = dataclasses.replace(spec, kv_dtype=W.KV_FP8_E4M3, name=spec.name + "_fp8")
     if args.splits is not None:
         spec = dataclasses.replace(spec, num_splits=args.splits)
     world, rank, local = dist_info()
@@ -810,7 +817,12 @@ def main():
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4)}
-    roof["kernel"] = f"{kind}_split_kernel" if kind == "decode" else "prefill_kernel"
+    if kind == "decode":
+        roof["kernel"] = "decode_split_kernel"
+    elif spec.kv_dtype == 1:  # e4m3 prefill rows run on the generic SIMT kernel
+        roof["kernel"] = "diffkv_kernel (generic, e4m3 prefill rows)"
+    else:
+        roof["kernel"] = "prefill_kernel"
     roof["kernel_ms"] = round(ph[kind], 4)
     roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)" if pk_src == "measured" else pk_src
     roof["traffic"] = profiled_traffic(kind, spec.name)

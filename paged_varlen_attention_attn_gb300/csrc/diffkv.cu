@@ -34,7 +34,6 @@ namespace {
 constexpr int DKV_THREADS = 128;
 constexpr int DKV_KEYS = 32;   // keys per staged tile
 constexpr int DKV_MAXH = 4;    // query heads per warp: G <= 16
-constexpr int DKV_MAXC = 8;    // output columns per lane: dv <= 256
 constexpr unsigned FULL_MASK = 0xffffffffu;
 
 template <bool HALF>
@@ -105,38 +104,47 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(unsigned v) {
 // Cache element types of the generic kernel.
 constexpr int GK_BF16 = 0, GK_E4M3 = 1, GK_F16 = 2;
 
+// (d0, d1) += (a0, a1) * (b0, b1) on the paired fp32 pipe
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // dot(q[0..7], 8 16-bit values in w) into (d0, d1)
 template <bool HALF>
 __device__ __forceinline__ void dot8(const float4 qa, const float4 qb, const uint4 w, float& d0,
                                      float& d1) {
   float2 f = unpack2<HALF>(w.x);
-  d0 = fmaf(qa.x, f.x, d0);
-  d1 = fmaf(qa.y, f.y, d1);
+  fma2(d0, d1, qa.x, qa.y, f.x, f.y);
   f = unpack2<HALF>(w.y);
-  d0 = fmaf(qa.z, f.x, d0);
-  d1 = fmaf(qa.w, f.y, d1);
+  fma2(d0, d1, qa.z, qa.w, f.x, f.y);
   f = unpack2<HALF>(w.z);
-  d0 = fmaf(qb.x, f.x, d0);
-  d1 = fmaf(qb.y, f.y, d1);
+  fma2(d0, d1, qb.x, qb.y, f.x, f.y);
   f = unpack2<HALF>(w.w);
-  d0 = fmaf(qb.z, f.x, d0);
-  d1 = fmaf(qb.w, f.y, d1);
+  fma2(d0, d1, qb.z, qb.w, f.x, f.y);
 }
 
 // dot(q[0..3], 4 e4m3 codes in w) into (d0, d1)
 __device__ __forceinline__ void dot4_e4m3(const float4 q, unsigned w, float& d0, float& d1) {
   float2 f = e4m3x2_to_float2(w);
-  d0 = fmaf(q.x, f.x, d0);
-  d1 = fmaf(q.y, f.y, d1);
+  fma2(d0, d1, q.x, q.y, f.x, f.y);
   f = e4m3x2_to_float2(w >> 16);
-  d0 = fmaf(q.z, f.x, d0);
-  d1 = fmaf(q.w, f.y, d1);
+  fma2(d0, d1, q.z, q.w, f.x, f.y);
 }
 
 // KV: GK_BF16, GK_E4M3 (with bf16 q and out) or GK_F16 (f16 q and out).
+// NC: dv / 32, the output columns per lane.  With NC even a lane owns pairs of
+// adjacent columns (2 lane + 64 c, + 1), read as one 32-bit (16-bit for e4m3)
+// word per key and stored together; with NC odd, columns lane + 32 c.
 // split: the standard layout (K and V planes); else the DiffKV layout.
 // skip_decode: rows of requests with query_len 1 are left to the decode kernel.
-template <int KV>
+template <int KV, int NC>
 __global__ void __launch_bounds__(DKV_THREADS)
     diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2, float out_scale,
                   int split, int skip_decode) {
@@ -217,15 +225,15 @@ __global__ void __launch_bounds__(DKV_THREADS)
   const int64_t qrow = (static_cast<int64_t>(t) * p.H + static_cast<int64_t>(g) * G) * dk;
   for (int e = threadIdx.x; e < G * dk; e += DKV_THREADS) q_s[e] = elem<HALF>(p.q, qrow + e);
 
-  float m_run[DKV_MAXH], l_run[DKV_MAXH], o[DKV_MAXH][DKV_MAXC];
+  constexpr bool PAIRS = (NC % 2) == 0;
+  float m_run[DKV_MAXH], l_run[DKV_MAXH], o[DKV_MAXH][NC];
 #pragma unroll
   for (int jh = 0; jh < DKV_MAXH; ++jh) {
     m_run[jh] = -INFINITY;
     l_run[jh] = 0.f;
 #pragma unroll
-    for (int c = 0; c < DKV_MAXC; ++c) o[jh][c] = 0.f;
+    for (int c = 0; c < NC; ++c) o[jh][c] = 0.f;
   }
-  const int nc = dv / 32;
 
   for (int j = 0; j < ntiles; ++j) {
     const int k0 = lo + j * DKV_KEYS;
@@ -266,22 +274,32 @@ __global__ void __launch_bounds__(DKV_THREADS)
       l_run[jh] = l_run[jh] * alpha + warp_sum(pk);
       m_run[jh] = m_new;
 #pragma unroll
-      for (int c = 0; c < DKV_MAXC; ++c) o[jh][c] *= alpha;
-      // o += sum_k p_k V_k, lane owning columns lane + 32 c
+      for (int c = 0; c < NC; ++c) o[jh][c] *= alpha;
+      // o += sum_k p_k V_k over this lane's columns
 #pragma unroll 8
       for (int kk = 0; kk < DKV_KEYS; ++kk) {
         const float pb = __shfl_sync(FULL_MASK, pk, kk);
-        if constexpr (KV == GK_E4M3) {
-          const unsigned char* vrow = tb + kk * rs + kbytes + lane;
+        const unsigned char* vbase = tb + kk * rs + kbytes;
+        if constexpr (PAIRS) {
 #pragma unroll
-          for (int c = 0; c < DKV_MAXC; ++c)
-            if (c < nc) o[jh][c] = fmaf(pb, e4m3x2_to_float2(vrow[32 * c]).x, o[jh][c]);
+          for (int c2 = 0; c2 < NC / 2; ++c2) {
+            float2 v;
+            if constexpr (KV == GK_E4M3)
+              v = e4m3x2_to_float2(reinterpret_cast<const unsigned short*>(vbase)[lane + 32 * c2]);
+            else
+              v = unpack2<HALF>(reinterpret_cast<const unsigned*>(vbase)[lane + 32 * c2]);
+            fma2(o[jh][2 * c2], o[jh][2 * c2 + 1], pb, pb, v.x, v.y);
+          }
         } else {
-          const unsigned short* vrow =
-              reinterpret_cast<const unsigned short*>(tb + kk * rs + kbytes) + lane;
 #pragma unroll
-          for (int c = 0; c < DKV_MAXC; ++c)
-            if (c < nc) o[jh][c] = fmaf(pb, half_bits_to_float<HALF>(vrow[32 * c]), o[jh][c]);
+          for (int c = 0; c < NC; ++c) {
+            float v;
+            if constexpr (KV == GK_E4M3)
+              v = e4m3x2_to_float2(vbase[lane + 32 * c]).x;
+            else
+              v = half_bits_to_float<HALF>(reinterpret_cast<const unsigned short*>(vbase)[lane + 32 * c]);
+            o[jh][c] = fmaf(pb, v, o[jh][c]);
+          }
         }
       }
     }
@@ -295,9 +313,16 @@ __global__ void __launch_bounds__(DKV_THREADS)
     if (hh >= G) continue;
     const float l_tot = l_run[jh] + sink_term(p.sinks, g * G + hh, m_run[jh]);
     const float inv = (l_tot > 0.f) ? out_scale / l_tot : 0.f;
+    const int64_t ob = orow + static_cast<int64_t>(hh) * dv;
+    if constexpr (PAIRS) {
 #pragma unroll
-    for (int c = 0; c < DKV_MAXC; ++c)
-      if (c < nc) store<HALF>(p.out, orow + static_cast<int64_t>(hh) * dv + lane + 32 * c, o[jh][c] * inv);
+      for (int c2 = 0; c2 < NC / 2; ++c2)
+        reinterpret_cast<unsigned*>(p.out)[(ob >> 1) + lane + 32 * c2] =
+            pack2<HALF>(o[jh][2 * c2] * inv, o[jh][2 * c2 + 1] * inv);
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) store<HALF>(p.out, ob + lane + 32 * c, o[jh][c] * inv);
+    }
   }
 }
 
@@ -308,26 +333,42 @@ size_t generic_smem_bytes(int G, int dk, int dv, int es) {
          static_cast<size_t>(G) * dk * sizeof(float);
 }
 
-template <int KV>
+template <int KV, int NC>
 cudaError_t launch_generic_t(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
   const size_t smem = generic_smem_bytes(p.G, dk, dv, KV == GK_E4M3 ? 1 : 2);
   const float sl2 = fmaxf(p.scale * LOG2E * (KV == GK_E4M3 ? p.k_scale : 1.f), 1e-30f);
   const float out_scale = (KV == GK_E4M3) ? p.v_scale : 1.f;
   const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>(p.Hkv));
-  cudaError_t e = cudaFuncSetAttribute(diffkv_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = diffkv_kernel<KV, NC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  diffkv_kernel<KV><<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2, out_scale,
-                                                          split ? 1 : 0, skip_decode ? 1 : 0);
+  kern<<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2, out_scale, split ? 1 : 0,
+                                              skip_decode ? 1 : 0);
   return cudaGetLastError();
+}
+
+template <int KV>
+cudaError_t launch_generic_kv(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
+  switch (dv / 32) {
+    case 1: return launch_generic_t<KV, 1>(p, dk, dv, split, skip_decode);
+    case 2: return launch_generic_t<KV, 2>(p, dk, dv, split, skip_decode);
+    case 3: return launch_generic_t<KV, 3>(p, dk, dv, split, skip_decode);
+    case 4: return launch_generic_t<KV, 4>(p, dk, dv, split, skip_decode);
+    case 5: return launch_generic_t<KV, 5>(p, dk, dv, split, skip_decode);
+    case 6: return launch_generic_t<KV, 6>(p, dk, dv, split, skip_decode);
+    case 7: return launch_generic_t<KV, 7>(p, dk, dv, split, skip_decode);
+    case 8: return launch_generic_t<KV, 8>(p, dk, dv, split, skip_decode);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_generic(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
   if (p.T == 0 || p.B == 0) return cudaSuccess;
-  if (p.kv_dtype == PATTN_KV_F16) return launch_generic_t<GK_F16>(p, dk, dv, split, skip_decode);
+  if (p.kv_dtype == PATTN_KV_F16) return launch_generic_kv<GK_F16>(p, dk, dv, split, skip_decode);
   if (p.kv_dtype == PATTN_KV_FP8_E4M3)
-    return launch_generic_t<GK_E4M3>(p, dk, dv, split, skip_decode);
-  return launch_generic_t<GK_BF16>(p, dk, dv, split, skip_decode);
+    return launch_generic_kv<GK_E4M3>(p, dk, dv, split, skip_decode);
+  return launch_generic_kv<GK_BF16>(p, dk, dv, split, skip_decode);
 }
 
 cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {

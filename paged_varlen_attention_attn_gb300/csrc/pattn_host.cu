@@ -559,10 +559,16 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
                          ext->num_blocks, decode_heads_per_cta(num_kv_heads, head_size, kv_dtype)))
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
-  if (generic_prefill &&
-      launch_generic(p, head_size, head_size, /*split=*/true, /*skip_decode=*/true) != cudaSuccess)
-    return PATTN_ERR_CUDA;
   mark(5);
+  if (generic_prefill) {
+    // the prefill phase's events move here (their earlier records are
+    // overwritten)
+    mark(2);
+    if (launch_generic(p, head_size, head_size, /*split=*/true, /*skip_decode=*/true) !=
+        cudaSuccess)
+      return PATTN_ERR_CUDA;
+    mark(3);
+  }
   // The partitions are merged inside the decode kernel (its last CTA of each
   // request and KV-head group); the combine phase is empty.
   mark(6);
