@@ -144,10 +144,8 @@ pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* bl
   if (!causal && window > 0) return PATTN_ERR_UNSUPPORTED;
   if (ext_head_size_v(ext) > 0 && kv_dtype == PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;
   // Prefill key tiles of the tensor-core kernel are 128 keys: a page must
-  // divide the tile or be a whole number of tiles.  (e4m3 prefill rows go to
-  // the generic kernel, which takes any block size.)
-  if (ext->max_query_len > 1 && kv_dtype != PATTN_KV_FP8_E4M3 &&
-      !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
+  // divide the tile or be a whole number of tiles.
+  if (ext->max_query_len > 1 && !(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0))
     return PATTN_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(kv_cache) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
       (reinterpret_cast<uintptr_t>(out) & 15) ||
@@ -287,8 +285,9 @@ bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, 
   cuuint32_t box[4] = {static_cast<cuuint32_t>(fp8 ? D : 64), 1,
                        static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapSwizzle sw =
-      (fp8 && D == 64) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  // e4m3 rows land unswizzled in the prefill kernel's staging buffer (its
+  // producers widen them into the swizzled f16 layout).
+  const CUtensorMapSwizzle sw = fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   return enc(map,
              fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                  : (kv_dtype == PATTN_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -514,20 +513,18 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
       cudaEventRecord(static_cast<cudaEvent_t>(ext->timing_events[idx]), p.stream);
   };
 
-  // Prefill rows run on the tensor-core kernel, except over an e4m3 cache,
-  // where the generic kernel serves them after the decode kernel.
-  const bool tc_prefill = ext->max_query_len > 1 && kv_dtype != PATTN_KV_FP8_E4M3;
-  const bool generic_prefill = ext->max_query_len > 1 && kv_dtype == PATTN_KV_FP8_E4M3;
+  // Prefill rows run on the tensor-core kernel (an e4m3 cache widened to f16
+  // in its shared memory).
+  const bool tc_prefill = ext->max_query_len > 1;
   mark(0);
   if (tc_prefill) {
     // The plan kernel clears the header and the counters and builds the
     // prefill work list.
     if (launch_plan(p) != cudaSuccess) return PATTN_ERR_CUDA;
   } else {
-    // No tensor-core prefill (decode only, or an e4m3 cache): nothing to plan
-    // (the decode and generic kernels validate their own rows); clear the
-    // status word and the partition counters and order the requests longest
-    // first.
+    // Decode only: nothing to plan (the decode kernel validates its own
+    // rows); clear the status word and the partition counters and order the
+    // requests longest first.
     if (launch_decode_prep(p) != cudaSuccess) return PATTN_ERR_CUDA;
   }
   // The decode kernel is a programmatic dependent of the kernel before it,
@@ -560,15 +557,6 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
     return PATTN_ERR_CUDA;
   if (launch_decode(p, dmap) != cudaSuccess) return PATTN_ERR_CUDA;
   mark(5);
-  if (generic_prefill) {
-    // the prefill phase's events move here (their earlier records are
-    // overwritten)
-    mark(2);
-    if (launch_generic(p, head_size, head_size, /*split=*/true, /*skip_decode=*/true) !=
-        cudaSuccess)
-      return PATTN_ERR_CUDA;
-    mark(3);
-  }
   // The partitions are merged inside the decode kernel (its last CTA of each
   // request and KV-head group); the combine phase is empty.
   mark(6);

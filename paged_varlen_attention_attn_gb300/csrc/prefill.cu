@@ -72,15 +72,23 @@ constexpr int PF_VST = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr unsigned FULL = 0xffffffffu;
 
-template <int D>
+// FP8: an e4m3 cache.  Each K or V tile is copied by TMA into a staging
+// buffer as bytes and widened by its producer warp into the ring as f16 (one
+// stage fewer of K makes room for the two staging buffers).
+template <int D, bool FP8 = false>
 struct PrefillCfg {
   static constexpr int DH = D / 64;                 // 128-byte column blocks
   static constexpr int HALF = BLOCK_M * 128;        // bytes of one 128-row column block
   static constexpr int TILE = DH * HALF;            // bytes of a Q, K or V tile
+  static constexpr int KST = FP8 ? 2 : PF_KST;      // K ring stages
+  static constexpr int VST = PF_VST;                // V ring stages
+  static constexpr int TILE_F8 = BLOCK_N * D;       // bytes of an e4m3 K or V tile
   static constexpr int Q_OFF = 0;                   // two Q tiles
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
-  static constexpr int V_OFF = K_OFF + PF_KST * TILE;
-  static constexpr int BAR_OFF = V_OFF + PF_VST * TILE;
+  static constexpr int V_OFF = K_OFF + KST * TILE;
+  static constexpr int KS_OFF = V_OFF + VST * TILE;  // e4m3 staging (FP8 only)
+  static constexpr int VS_OFF = KS_OFF + (FP8 ? TILE_F8 : 0);
+  static constexpr int BAR_OFF = VS_OFF + (FP8 ? TILE_F8 : 0);
   // + barriers + alignment slack; at least 116 KB so one CTA holds an SM (and
   // its 512 TMEM columns) alone
   static constexpr int SMEM_RAW = BAR_OFF + 512 + 1024;
@@ -97,6 +105,9 @@ struct Bars {
   uint64_t k_empty[PF_KST];
   uint64_t v_empty[PF_VST];
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
+  uint64_t kst_full;    // e4m3 K tile landed in staging (FP8)
+  uint64_t vst_full;    // e4m3 V tile landed in staging (FP8)
+  uint64_t q_conv[2];   // Q tile of sub-tile X converted to f16 (FP8)
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
   uint64_t q_empty;     // every S MMA of an item issued and done: Q may be replaced
@@ -127,6 +138,20 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float b, float c) {
       "mov.b64 {%0, %1}, ra;\n\t}"
       : "+f"(a0), "+f"(a1)
       : "f"(b), "f"(c));
+}
+
+// Two e4m3 codes (the low 16 bits of v) -> f16x2, exactly (the hardware pair
+// conversion; every e4m3 value is an f16 value).
+__device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
+  unsigned r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
+  return r;
+}
+
+// bf16x2 -> f16x2 (exact for bf16 values in f16's range; q of an e4m3 call)
+__device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<const unsigned*>(&h);
 }
 
 // (s0, s1) += (a0, a1)
@@ -196,7 +221,10 @@ __device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) 
   return u1 - u0;
 }
 
-// HALF: q, the cache and out are f16 (else bf16).
+// HALF: q, the cache and out are f16 (else bf16).  FP8: an e4m3 cache with
+// bf16 q and out; K and V tiles are widened to f16 in shared memory (exact:
+// every e4m3 value is an f16 value), Q is converted to f16 in place, and the
+// MMAs and P run in f16; the K scale is in sl2 and the V scale is out_scale.
 //
 // Persistent: the grid holds at most one CTA per SM and CTA b takes items
 // b, 2G-1-b, 2G+b, ... of the LPT-ordered list (G = grid size; the order
@@ -208,11 +236,12 @@ __device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) 
 // that follows the item's last S MMA, and the first P V of the next item
 // (which overwrites O) waits on p_full, which the softmax warps arrive on only
 // after their epilogue has read O.
-template <int D, bool HALF>
+template <int D, bool HALF, bool FP8>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ Problem p, const __grid_constant__ CUtensorMap qmap,
-                   const __grid_constant__ CUtensorMap kvmap, float sl2) {
-  using C = PrefillCfg<D>;
+                   const __grid_constant__ CUtensorMap kvmap, float sl2, float out_scale) {
+  using C = PrefillCfg<D, FP8>;
+  constexpr bool MMA_F16 = HALF || FP8;  // operand and P type of the MMAs
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,6 +278,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->v_empty[i], 1);
     }
     mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->kst_full, 1);
+    mbar_init(&bars->vst_full, 1);
+    mbar_init(&bars->q_conv[0], 1);
+    mbar_init(&bars->q_conv[1], 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -281,10 +314,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // so a tile costs one copy instruction, not 2 x pages of them in one
     // thread.
     const int kv = (warp == 10) ? 1 : 0;
-    const int nst = kv ? PF_VST : PF_KST;
+    const int nst = kv ? C::VST : C::KST;
     unsigned char* ring = kv ? sV : sK;
-    // Copy `lane` of a tile: page lane / DH, d half lane % DH.
-    const int my_pg = lane / C::DH, my_dh = lane % C::DH;
+    // Copy `lane` of a tile: page lane / DH, d half lane % DH (an e4m3 page
+    // row is one copy: page lane).
+    const int my_pg = FP8 ? lane : lane / C::DH, my_dh = FP8 ? 0 : lane % C::DH;
+    unsigned char* stage8 = smem + (kv ? C::VS_OFF : C::KS_OFF);
+    uint64_t* stage8_full = kv ? &bars->vst_full : &bars->kst_full;
     if (kv == 0 && lane == 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kvmap);
@@ -342,21 +378,66 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
         const int my_key0 = key_base + my_pg * rows_box;
         const int my_slot = p.bs_shift >= 0 ? (my_key0 & (p.bs - 1)) : (my_key0 % p.bs);
-        const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
         const int st = jg % nst;
         uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
         uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-        if (lane == 0) {
-          if (jg >= nst && !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
-            ok = 0;
-          else
-            mbar_arrive_expect_tx(full, bytes);
+        if constexpr (!FP8) {
+          const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
+          if (lane == 0) {
+            if (jg >= nst && !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
+              ok = 0;
+            else
+              mbar_arrive_expect_tx(full, bytes);
+          }
+          ok = __shfl_sync(FULL, ok, 0);
+          if (!ok) break;
+          if (my_pg < n_load)
+            tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap,
+                        full, my_dh * 64, g, my_slot, kv * p.NB + my_blk);
+        } else {
+          // e4m3: the tile's pages land in the staging buffer (rows of D
+          // bytes, no swizzle); the warp then widens them into the ring stage
+          // in the swizzled f16 layout TMA would have written, and announces
+          // the stage with a plain arrival.  The staging buffer is reused by
+          // the next tile only after this warp has read it (and fenced).
+          if (lane == 0)
+            mbar_arrive_expect_tx(stage8_full, static_cast<unsigned>(n_load * rows_box * D));
+          __syncwarp();
+          if (my_pg < n_load)
+            tma_load_4d(stage8 + my_pg * rows_box * D, &kvmap, stage8_full, 0, g, my_slot,
+                        kv * p.NB + my_blk);
+          int good = mbar_wait(stage8_full, jg & 1, status, abort_flag) ? 1 : 0;
+          if (lane == 0 && good && jg >= nst &&
+              !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
+            good = 0;
+          ok = __all_sync(FULL, good) ? 1 : 0;
+          if (!ok) break;
+          // 16 codes per piece: row r, bytes 16 c .. 16 c + 15 -> f16 d half
+          // (16 c) / 64, 16-byte chunks 2 (c % 4) and + 1 of that row, each at
+          // chunk position (chunk ^ (r % 8)) of the 128-byte swizzle.
+          constexpr int PPR = D / 16;  // pieces per row
+          const int rows = n_load * rows_box;
+          unsigned char* dst0 = ring + st * C::TILE;
+          for (int pc = lane; pc < rows * PPR; pc += 32) {
+            const int r = pc / PPR, c = pc % PPR;
+            const uint4 w = *reinterpret_cast<const uint4*>(stage8 + r * D + c * 16);
+            const unsigned src[4] = {w.x, w.y, w.z, w.w};
+            unsigned h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              h[2 * e] = e4m3x2_to_f16x2(src[e]);
+              h[2 * e + 1] = e4m3x2_to_f16x2(src[e] >> 16);
+            }
+            unsigned char* rowp = dst0 + (c >> 2) * C::HALF + r * 128;
+            const int cc = 2 * (c & 3);
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) =
+                make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full);
         }
-        ok = __shfl_sync(FULL, ok, 0);
-        if (!ok) break;
-        if (my_pg < n_load)
-          tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap, full,
-                      my_dh * 64, g, my_slot, kv * p.NB + my_blk);
       }
       if (!ok) break;
       ++n_worked;
@@ -364,8 +445,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !HALF, false);
-      constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, !HALF, true);
+      constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !MMA_F16, false);
+      constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, !MMA_F16, true);
       // Base descriptors; a byte offset o moves the start address field by
       // o >> 4 (shared addresses stay far below the field's 256 KB range).
       const uint64_t q_d = smem_desc_sw128(smem_u32(sQ), 16, 1024);
@@ -401,13 +482,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             bool& q_ready = X ? q_ready1 : q_ready0;
             // P V for the previous key tile
             if (j >= 1 && u.active(kt - 1)) {
-              const int stp = (jj - 1) % PF_VST;
+              const int stp = (jj - 1) % C::VST;
               if (!mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag)) {
                 ok = false;
                 break;
               }
               if (!v_ready) {
-                if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status, abort_flag)) {
+                if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / C::VST) & 1, status, abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -432,16 +513,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             // scores for this key tile
             if (j < n_union && u.active(kt)) {
-              const int st = jj % PF_KST;
+              const int st = jj % C::KST;
               if (!k_ready) {
-                if (!mbar_wait(&bars->k_full[st], (jj / PF_KST) & 1, status, abort_flag)) {
+                if (!mbar_wait(&bars->k_full[st], (jj / C::KST) & 1, status, abort_flag)) {
                   ok = false;
                   break;
                 }
                 k_ready = true;
               }
               if (!q_ready) {
-                if (!mbar_wait(&bars->q_full[X], q_tot & 1, status, abort_flag)) {
+                // an e4m3 call's Q is usable once warp 11 has converted it
+                if (!mbar_wait(FP8 ? &bars->q_conv[X] : &bars->q_full[X], q_tot & 1, status,
+                               abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -472,6 +555,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       if (issued) {
         tc_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, status, nullptr);
+      }
+    }
+  } else if (FP8 && warp == 11) {
+    // ------------------------------------------------------------ Q converter (e4m3 calls)
+    // Each item's Q tiles (bf16, as TMA loaded them) become f16 in place for
+    // the f16 MMAs: an elementwise change, so the swizzled layout stays.
+    int q_tot0 = 0, q_tot1 = 0;
+    bool ok = true;
+    for (int k = 0; ok && k * GS < n_items; ++k) {
+      const Item it = load_item(p, item_at(k), n_items, NP, KC);
+      const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
+      int u0;
+      if (union_tiles(subA, subB, u0) <= 0) continue;
+#pragma unroll
+      for (int X = 0; X < 2; ++X) {
+        const Sub& u = X ? subB : subA;
+        int& q_tot = X ? q_tot1 : q_tot0;
+        if (!ok || u.x1 <= u.x0) continue;
+        if (!__all_sync(FULL, mbar_wait(&bars->q_full[X], q_tot & 1, status, abort_flag))) {
+          ok = false;
+          continue;
+        }
+        unsigned* qw = reinterpret_cast<unsigned*>(sQ + X * C::TILE);
+        for (int w = lane; w < C::TILE / 4; w += 32) qw[w] = bf16x2_to_f16x2(qw[w]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->q_conv[X]);
+        ++q_tot;
       }
     }
   }
@@ -598,8 +709,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             a3 = fast_exp2(a3);
             fadd2(ps0, ps1, a0, a1);
             fadd2(ps2, ps3, a2, a3);
-            pk[e / 2] = pack2<HALF>(a0, a1);
-            pk[e / 2 + 1] = pack2<HALF>(a2, a3);
+            pk[e / 2] = pack2<MMA_F16>(a0, a1);
+            pk[e / 2 + 1] = pack2<MMA_F16>(a2, a3);
           }
           tc_st16u(s_t + 64 + q / 2, pk);
         }
@@ -647,7 +758,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_fence_after();
         // a final output row includes its head's sink in the normaliser
         const float l_tot = p.o32 ? l_run : l_run + sink_term(p.sinks, u.h, m_run);
-        const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+        const float inv = (l_tot > 0.f) ? out_scale / l_tot : 0.f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           float ov[32];
@@ -697,27 +808,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
 int prefill_rows_per_item(int G) { return (G % 2 == 0) ? BLOCK_M : 2 * BLOCK_M; }
 
-template <int D, bool HALF>
-cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
-                             unsigned grid) {
-  auto k = prefill_kernel<D, HALF>;
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, k);
-  if (e != cudaSuccess) return e;
-  // The register split must fit in what the CTA is launched with.
-  if (static_cast<long long>(attr.numRegs) * PF_THREADS < SPLIT_REGS_TOTAL)
-    return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg<D>::SMEM);
-  if (e != cudaSuccess) return e;
-  // Scores are scaled to log2 units by sl2 = scale * log2(e).  It is kept
-  // strictly positive so a masked score (-inf) always maps to exp2(-inf) = 0;
-  // at scale == 0 the visible scores become ~1e-30 * q.k, whose exp2 is 1.0f
-  // exactly (uniform weights, as the definition gives).
-  const float sl2 = fmaxf(p.scale * LOG2E, 1e-30f);
-  k<<<grid, PF_THREADS, PrefillCfg<D>::SMEM, p.stream>>>(p, q_map, kv_map, sl2);
-  return cudaGetLastError();
-}
-
 // Number of SMs of the current device (cached per device).
 static int prefill_sms() {
   static int counts[64] = {0};
@@ -732,6 +822,30 @@ static int prefill_sms() {
   return counts[dev];
 }
 
+template <int D, bool HALF, bool FP8>
+cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                             unsigned grid) {
+  using C = PrefillCfg<D, FP8>;
+  auto k = prefill_kernel<D, HALF, FP8>;
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, k);
+  if (e != cudaSuccess) return e;
+  // The register split must fit in what the CTA is launched with.
+  if (static_cast<long long>(attr.numRegs) * PF_THREADS < SPLIT_REGS_TOTAL)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  // Scores are scaled to log2 units by sl2 = scale * log2(e) (times the K
+  // scale of an e4m3 cache).  It is kept strictly positive so a masked score
+  // (-inf) always maps to exp2(-inf) = 0; at scale == 0 the visible scores
+  // become ~1e-30 * q.k, whose exp2 is 1.0f exactly (uniform weights, as the
+  // definition gives).  out_scale is the V scale of an e4m3 cache.
+  const float sl2 = fmaxf(p.scale * LOG2E * (FP8 ? p.k_scale : 1.f), 1e-30f);
+  const float out_scale = FP8 ? p.v_scale : 1.f;
+  k<<<grid, PF_THREADS, C::SMEM, p.stream>>>(p, q_map, kv_map, sl2, out_scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map) {
   const int NP = (p.G % 2 == 0) ? p.H / 2 : p.H;
   // Persistent grid: one CTA per SM (the shared memory and the 512 TMEM
@@ -740,10 +854,13 @@ cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUt
   if (items == 0) return cudaSuccess;
   const unsigned g = static_cast<unsigned>(std::min<long long>(items, prefill_sms()));
   if (p.kv_dtype == PATTN_KV_F16)
-    return p.D == 128 ? launch_prefill_t<128, true>(p, q_map, kv_map, g)
-                      : launch_prefill_t<64, true>(p, q_map, kv_map, g);
-  return p.D == 128 ? launch_prefill_t<128, false>(p, q_map, kv_map, g)
-                    : launch_prefill_t<64, false>(p, q_map, kv_map, g);
+    return p.D == 128 ? launch_prefill_t<128, true, false>(p, q_map, kv_map, g)
+                      : launch_prefill_t<64, true, false>(p, q_map, kv_map, g);
+  if (p.kv_dtype == PATTN_KV_FP8_E4M3)
+    return p.D == 128 ? launch_prefill_t<128, false, true>(p, q_map, kv_map, g)
+                      : launch_prefill_t<64, false, true>(p, q_map, kv_map, g);
+  return p.D == 128 ? launch_prefill_t<128, false, false>(p, q_map, kv_map, g)
+                    : launch_prefill_t<64, false, false>(p, q_map, kv_map, g);
 }
 
 }  // namespace pattn
