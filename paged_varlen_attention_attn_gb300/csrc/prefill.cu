@@ -72,23 +72,18 @@ constexpr int PF_VST = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr unsigned FULL = 0xffffffffu;
 
-// FP8: an e4m3 cache.  Each K or V tile is copied by TMA into a staging
-// buffer as bytes and widened by its producer warp into the ring as f16 (one
-// stage fewer of K makes room for the two staging buffers).
-template <int D, bool FP8 = false>
+template <int D>
 struct PrefillCfg {
   static constexpr int DH = D / 64;                 // 128-byte column blocks
   static constexpr int HALF = BLOCK_M * 128;        // bytes of one 128-row column block
   static constexpr int TILE = DH * HALF;            // bytes of a Q, K or V tile
-  static constexpr int KST = FP8 ? 2 : PF_KST;      // K ring stages
-  static constexpr int VST = PF_VST;                // V ring stages
-  static constexpr int TILE_F8 = BLOCK_N * D;       // bytes of an e4m3 K or V tile
+  // An e4m3 K or V tile (rows of D bytes) lands at the top of its ring stage
+  // and is widened there, in place, to the f16 tile.
+  static constexpr int SRC8 = TILE - BLOCK_N * D;
   static constexpr int Q_OFF = 0;                   // two Q tiles
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
-  static constexpr int V_OFF = K_OFF + KST * TILE;
-  static constexpr int KS_OFF = V_OFF + VST * TILE;  // e4m3 staging (FP8 only)
-  static constexpr int VS_OFF = KS_OFF + (FP8 ? TILE_F8 : 0);
-  static constexpr int BAR_OFF = VS_OFF + (FP8 ? TILE_F8 : 0);
+  static constexpr int V_OFF = K_OFF + PF_KST * TILE;
+  static constexpr int BAR_OFF = V_OFF + PF_VST * TILE;
   // + barriers + alignment slack; at least 116 KB so one CTA holds an SM (and
   // its 512 TMEM columns) alone
   static constexpr int SMEM_RAW = BAR_OFF + 512 + 1024;
@@ -105,8 +100,8 @@ struct Bars {
   uint64_t k_empty[PF_KST];
   uint64_t v_empty[PF_VST];
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
-  uint64_t kst_full;    // e4m3 K tile landed in staging (FP8)
-  uint64_t vst_full;    // e4m3 V tile landed in staging (FP8)
+  uint64_t k_land[PF_KST];  // e4m3 K tile landed at the top of its stage (FP8)
+  uint64_t v_land[PF_VST];  // e4m3 V tile landed at the top of its stage (FP8)
   uint64_t q_conv[2];   // Q tile of sub-tile X converted to f16 (FP8)
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
@@ -146,6 +141,63 @@ __device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
   unsigned r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
   return r;
+}
+
+// Widens the first `rows` rows of an e4m3 tile, stored as rows of D bytes
+// in the last BLOCK_N x D bytes of a K or V stage, in place into the stage's
+// f16 tile in the 128-byte-swizzled layout: code c of row r goes to d half
+// c / 64, 16-byte chunk (c % 64) / 8, which sits at chunk position
+// (chunk ^ (r % 8)) of the row.  A lane takes 16 codes (a piece) per pass,
+// and a pass of the warp covers 512 source bytes (512 / D rows); the lane
+// keeps the same row offset r0 and piece c in every pass.  At d 128 the two
+// rows of a quarter-warp take opposite d halves, so its 16-byte loads and
+// stores each land on eight distinct bank groups.  A batch of U passes loads
+// all its pieces before any store: f16 rows overlap only source rows at or
+// below the batch's last row (at d 128 the second d half of row r is
+// exactly source row r; at d 64 f16 row r >= 64 covers source rows 2r - 128
+// and 2r - 127), so every source row is read before it is overwritten.  rows
+// is a multiple of 16, so passes come in whole batches.
+template <int D>
+__device__ __forceinline__ void widen_e4m3_in_place(unsigned char* stage, int rows, int lane) {
+  constexpr int RPP = 512 / D;
+  constexpr int U = (D == 128) ? 4 : 2;
+  constexpr int HALF = BLOCK_M * 128;  // bytes of one d half of a tile
+  constexpr int SRC8 = (D / 64) * HALF - BLOCK_N * D;
+  int r0, c;
+  if constexpr (D == 128) {
+    r0 = ((lane >> 4) << 1) | ((lane >> 2) & 1);
+    c = ((((lane >> 2) ^ (lane >> 3)) & 1) << 2) | (lane & 3);
+  } else {
+    r0 = lane >> 2;
+    c = lane & 3;
+  }
+  const int n_pass = rows / RPP;
+  const unsigned char* src0 = stage + SRC8 + r0 * D + c * 16;
+  unsigned char* dst0 = stage + (c >> 2) * HALF + r0 * 128;
+  const int cc = 2 * (c & 3);
+  for (int ps = 0; ps < n_pass; ps += U) {
+    uint4 w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) w[u] = *reinterpret_cast<const uint4*>(src0 + (ps + u) * RPP * D);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const unsigned v[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+      unsigned h[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[2 * e] = e4m3x2_to_f16x2(v[e]);
+        h[2 * e + 1] = e4m3x2_to_f16x2(v[e] >> 16);
+      }
+      // ps * RPP is a multiple of 8: the row's swizzle phase is that of
+      // r0 + u * RPP
+      const int sw = (r0 + u * RPP) & 7;
+      unsigned char* rowp = dst0 + (ps + u) * RPP * 128;
+      *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+    __syncwarp();
+  }
 }
 
 // bf16x2 -> f16x2 (exact for bf16 values in f16's range; q of an e4m3 call)
@@ -240,7 +292,7 @@ template <int D, bool HALF, bool FP8>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ Problem p, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kvmap, float sl2, float out_scale) {
-  using C = PrefillCfg<D, FP8>;
+  using C = PrefillCfg<D>;
   constexpr bool MMA_F16 = HALF || FP8;  // operand and P type of the MMAs
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -278,8 +330,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->v_empty[i], 1);
     }
     mbar_init(&bars->q_empty, 1);
-    mbar_init(&bars->kst_full, 1);
-    mbar_init(&bars->vst_full, 1);
+    for (int i = 0; i < PF_KST; ++i) mbar_init(&bars->k_land[i], 1);
+    for (int i = 0; i < PF_VST; ++i) mbar_init(&bars->v_land[i], 1);
     mbar_init(&bars->q_conv[0], 1);
     mbar_init(&bars->q_conv[1], 1);
     mbar_init(&bars->drain, 1);
@@ -299,8 +351,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   unsigned char* sQ = smem + C::Q_OFF;
   unsigned char* sK = smem + C::K_OFF;
   unsigned char* sV = smem + C::V_OFF;
-  const int rows_box = p.bs < BLOCK_N ? p.bs : BLOCK_N;
-  const int pages_per_tile = BLOCK_N / rows_box;
+  const int rows_box = p.bs < BLOCK_N ? p.bs : BLOCK_N;  // rows of one cache copy
+  const int pages_per_tile = BLOCK_N / rows_box;         // copies of one key tile
 
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(OTHER_REGS));
@@ -314,13 +366,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // so a tile costs one copy instruction, not 2 x pages of them in one
     // thread.
     const int kv = (warp == 10) ? 1 : 0;
-    const int nst = kv ? C::VST : C::KST;
+    const int nst = kv ? PF_VST : PF_KST;
     unsigned char* ring = kv ? sV : sK;
-    // Copy `lane` of a tile: page lane / DH, d half lane % DH (an e4m3 page
-    // row is one copy: page lane).
-    const int my_pg = FP8 ? lane : lane / C::DH, my_dh = FP8 ? 0 : lane % C::DH;
-    unsigned char* stage8 = smem + (kv ? C::VS_OFF : C::KS_OFF);
-    uint64_t* stage8_full = kv ? &bars->vst_full : &bars->kst_full;
+    // Copy `lane` of a tile: page lane / DH, d half lane % DH.
+    const int my_pg = lane / C::DH, my_dh = lane % C::DH;
     if (kv == 0 && lane == 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kvmap);
@@ -369,19 +418,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         return blk;
       };
-      int blk_next = page_block(u0);
-      for (int j = 0; j < n_union; ++j, ++jg) {
-        const int key_base = (u0 + j) * BLOCK_N;
-        const int my_blk = __shfl_sync(FULL, blk_next, my_pg);
-        if (j + 1 < n_union) blk_next = page_block(u0 + j + 1);
-        // pages of this tile that hold keys below seq_len
-        const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
-        const int my_key0 = key_base + my_pg * rows_box;
-        const int my_slot = p.bs_shift >= 0 ? (my_key0 & (p.bs - 1)) : (my_key0 % p.bs);
-        const int st = jg % nst;
-        uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
-        uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-        if constexpr (!FP8) {
+      if constexpr (!FP8) {
+        int blk_next = page_block(u0);
+        for (int j = 0; j < n_union; ++j, ++jg) {
+          const int key_base = (u0 + j) * BLOCK_N;
+          const int my_blk = __shfl_sync(FULL, blk_next, my_pg);
+          if (j + 1 < n_union) blk_next = page_block(u0 + j + 1);
+          // pages of this tile that hold keys below seq_len
+          const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
+          const int my_key0 = key_base + my_pg * rows_box;
+          const int my_slot = p.bs_shift >= 0 ? (my_key0 & (p.bs - 1)) : (my_key0 % p.bs);
+          const int st = jg % nst;
+          uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+          uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
           const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
           if (lane == 0) {
             if (jg >= nst && !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
@@ -394,50 +443,62 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           if (my_pg < n_load)
             tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap,
                         full, my_dh * 64, g, my_slot, kv * p.NB + my_blk);
-        } else {
-          // e4m3: the tile's pages land in the staging buffer (rows of D
-          // bytes, no swizzle); the warp then widens them into the ring stage
-          // in the swizzled f16 layout TMA would have written, and announces
-          // the stage with a plain arrival.  The staging buffer is reused by
-          // the next tile only after this warp has read it (and fenced).
-          if (lane == 0)
-            mbar_arrive_expect_tx(stage8_full, static_cast<unsigned>(n_load * rows_box * D));
-          __syncwarp();
-          if (my_pg < n_load)
-            tma_load_4d(stage8 + my_pg * rows_box * D, &kvmap, stage8_full, 0, g, my_slot,
-                        kv * p.NB + my_blk);
-          int good = mbar_wait(stage8_full, jg & 1, status, abort_flag) ? 1 : 0;
-          if (lane == 0 && good && jg >= nst &&
-              !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
-            good = 0;
-          ok = __all_sync(FULL, good) ? 1 : 0;
-          if (!ok) break;
-          // 16 codes per piece: row r, bytes 16 c .. 16 c + 15 -> f16 d half
-          // (16 c) / 64, 16-byte chunks 2 (c % 4) and + 1 of that row, each at
-          // chunk position (chunk ^ (r % 8)) of the 128-byte swizzle.
-          constexpr int PPR = D / 16;  // pieces per row
-          const int rows = n_load * rows_box;
-          unsigned char* dst0 = ring + st * C::TILE;
-          for (int pc = lane; pc < rows * PPR; pc += 32) {
-            const int r = pc / PPR, c = pc % PPR;
-            const uint4 w = *reinterpret_cast<const uint4*>(stage8 + r * D + c * 16);
-            const unsigned src[4] = {w.x, w.y, w.z, w.w};
-            unsigned h[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              h[2 * e] = e4m3x2_to_f16x2(src[e]);
-              h[2 * e + 1] = e4m3x2_to_f16x2(src[e] >> 16);
-            }
-            unsigned char* rowp = dst0 + (c >> 2) * C::HALF + r * 128;
-            const int cc = 2 * (c & 3);
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) =
-                make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      } else {
+        // e4m3: a tile's pages land as bytes at the top of its ring stage (the
+        // last BLOCK_N x D bytes, rows of D bytes, no swizzle), where the warp
+        // widens them in place into the swizzled f16 tile TMA would have
+        // written, then announces the stage with a plain arrival.  Copies run
+        // nst - 1 tiles ahead of the widening: after widening tile j the warp
+        // waits for the stage of tile j - 1 and refills it with tile
+        // j + nst - 1.  They stop at the item's last tile.
+        uint64_t* lands = kv ? bars->v_land : bars->k_land;
+        auto issue = [&](int jt, int kt, int blkv) {
+          const int key_base = kt * BLOCK_N;
+          const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
+          const int st = jt % nst;
+          uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+          int good = 1;
+          if (lane == 0) {
+            if (jt >= nst && !mbar_wait(empty, ((jt / nst) - 1) & 1, status, abort_flag))
+              good = 0;
+            else
+              mbar_arrive_expect_tx(&lands[st], static_cast<unsigned>(n_load * rows_box * D));
           }
+          good = __shfl_sync(FULL, good, 0);
+          if (good && lane < n_load) {
+            const int key0 = key_base + lane * rows_box;
+            const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
+            tma_load_4d(ring + st * C::TILE + C::SRC8 + lane * rows_box * D, &kvmap, &lands[st],
+                        0, g, slot, kv * p.NB + blkv);
+          }
+          return good;
+        };
+        int blk_next = page_block(u0);
+        int n_issued = 0;
+        auto issue_next = [&]() {
+          const int blk = blk_next;
+          if (n_issued + 1 < n_union) blk_next = page_block(u0 + n_issued + 1);
+          const int good = issue(jg + n_issued, u0 + n_issued, blk);
+          ++n_issued;
+          return good;
+        };
+        while (ok && n_issued < min(nst - 1, n_union)) ok = issue_next();
+        for (int j = 0; ok && j < n_union; ++j) {
+          const int jt = jg + j, st = jt % nst;
+          if (!__all_sync(FULL, mbar_wait(&lands[st], (jt / nst) & 1, status, abort_flag))) {
+            ok = 0;
+            break;
+          }
+          const int key_base = (u0 + j) * BLOCK_N;
+          const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
+          widen_e4m3_in_place<D>(ring + st * C::TILE, n_load * rows_box, lane);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(full);
+          if (lane == 0) mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
+          if (n_issued < n_union) ok = issue_next();
         }
+        jg += n_union;
       }
       if (!ok) break;
       ++n_worked;
@@ -482,13 +543,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             bool& q_ready = X ? q_ready1 : q_ready0;
             // P V for the previous key tile
             if (j >= 1 && u.active(kt - 1)) {
-              const int stp = (jj - 1) % C::VST;
+              const int stp = (jj - 1) % PF_VST;
               if (!mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag)) {
                 ok = false;
                 break;
               }
               if (!v_ready) {
-                if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / C::VST) & 1, status, abort_flag)) {
+                if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status, abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -513,9 +574,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             // scores for this key tile
             if (j < n_union && u.active(kt)) {
-              const int st = jj % C::KST;
+              const int st = jj % PF_KST;
               if (!k_ready) {
-                if (!mbar_wait(&bars->k_full[st], (jj / C::KST) & 1, status, abort_flag)) {
+                if (!mbar_wait(&bars->k_full[st], (jj / PF_KST) & 1, status, abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -825,7 +886,7 @@ static int prefill_sms() {
 template <int D, bool HALF, bool FP8>
 cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
                              unsigned grid) {
-  using C = PrefillCfg<D, FP8>;
+  using C = PrefillCfg<D>;
   auto k = prefill_kernel<D, HALF, FP8>;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, k);

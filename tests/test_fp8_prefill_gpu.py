@@ -3,7 +3,7 @@ decode kernel and the prefill rows (full and chunked prefills) on the
 tensor-core prefill kernel, which widens the codes to f16 in shared memory
 and applies the per-tensor scales.  Compared with the float64 oracle at the
 e4m3 tolerance: head sizes 64 and 128, even and odd GQA ratios, a sliding
-window, block sizes 64 and 256 (pages larger than a key tile), attention
+window, block sizes 64, 128 and 256 (pages of a key tile or more), attention
 sinks, a batch of chunked prefills beside many decodes, and a prefill
 request whose query is longer than its sequence (reported, rows zero,
 others exact)."""
@@ -62,7 +62,7 @@ def _check(case, out, sinks=None, skip=()):
 
 @pytest.mark.parametrize("H,Hkv,d,bs,window", [(8, 2, 128, 16, 0), (6, 2, 64, 16, 0),
                                                (4, 4, 128, 64, 0), (16, 2, 128, 16, 90),
-                                               (12, 4, 128, 256, 0)])
+                                               (12, 4, 128, 256, 0), (8, 8, 64, 128, 0)])
 def test_mixed_batches(H, Hkv, d, bs, window):
     sp = small_spec(1800 + H + d + bs + window, H=H, Hkv=Hkv, d=d, bs=bs, n_req=6, max_s=600,
                     window=window, kv_dtype=W.KV_FP8_E4M3)
