@@ -15,10 +15,11 @@
 // longest-first list, so one item's loads and first scores overlap the end of
 // the previous one instead of a CTA launch, set-up and drain.  Twelve warps:
 //   warps 0-3  softmax + epilogue of sub-tile A, thread i owns row i (TMEM lane i)
-//   warps 4-7  softmax + epilogue of sub-tile B
+//              (over an e4m3 cache they also convert their Q tile to f16)
+//   warps 4-7  softmax + epilogue of sub-tile B, likewise
 //   warp  8    TMA producer of both Q tiles of each item and the K tiles, page by
 //              page through block_table into a 3-stage ring, one lane per
-//              page copy
+//              page copy (over an e4m3 cache it also widens each K tile)
 //   warp  9    MMA issuer (one thread)
 //   warp 10    TMA producer of the V tiles (2-stage ring), likewise
 //   warp 11    idle (it completes the third warpgroup for setmaxnreg)
@@ -102,7 +103,7 @@ struct Bars {
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
   uint64_t k_land[PF_KST];  // e4m3 K tile landed at the top of its stage (FP8)
   uint64_t v_land[PF_VST];  // e4m3 V tile landed at the top of its stage (FP8)
-  uint64_t q_conv[2];   // Q tile of sub-tile X converted to f16 (FP8)
+  uint64_t q_conv[2];   // Q tile of sub-tile X converted to f16 by its warpgroup (FP8)
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
   uint64_t q_empty;     // every S MMA of an item issued and done: Q may be replaced
@@ -201,6 +202,37 @@ __device__ __forceinline__ void widen_e4m3_in_place(unsigned char* stage, int ro
 }
 
 // bf16x2 -> f16x2 (exact for bf16 values in f16's range; q of an e4m3 call)
+__device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w);
+
+// Converts a Q tile (bf16, as TMA loaded it) to f16 in place for the f16
+// MMAs of an e4m3 call, once its copy has landed (q_full at `parity`): an
+// elementwise change, so the swizzled layout stays.  Thread t of the
+// 128-thread softmax warpgroup converts the 16-byte pieces t + 128 i, eight
+// loads ahead; each warp then arrives on q_conv (four arrivals complete it).
+template <int TILE>
+__device__ __forceinline__ bool convert_q_tile(unsigned char* q, uint64_t* q_full,
+                                               uint64_t* q_conv, unsigned parity, int t,
+                                               unsigned* status, volatile int* abort_flag) {
+  if (!__all_sync(0xffffffffu, mbar_wait(q_full, parity, status, abort_flag))) return false;
+  constexpr int PER = TILE / 16 / 128;
+  static_assert(PER % 8 == 0, "whole batches of eight pieces");
+  uint4* q4 = reinterpret_cast<uint4*>(q) + t;
+  for (int b = 0; b < PER; b += 8) {
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = q4[128 * (b + i)];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      q4[128 * (b + i)] = make_uint4(bf16x2_to_f16x2(w[i].x), bf16x2_to_f16x2(w[i].y),
+                                     bf16x2_to_f16x2(w[i].z), bf16x2_to_f16x2(w[i].w));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if ((t & 31) == 0) mbar_arrive(q_conv);
+  return true;
+}
+
+// bf16x2 -> f16x2 (exact for bf16 values in f16's range; q of an e4m3 call)
 __device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w) {
   const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   return *reinterpret_cast<const unsigned*>(&h);
@@ -275,8 +307,9 @@ __device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) 
 
 // HALF: q, the cache and out are f16 (else bf16).  FP8: an e4m3 cache with
 // bf16 q and out; K and V tiles are widened to f16 in shared memory (exact:
-// every e4m3 value is an f16 value), Q is converted to f16 in place, and the
-// MMAs and P run in f16; the K scale is in sl2 and the V scale is out_scale.
+// every e4m3 value is an f16 value), each softmax warpgroup converts its Q
+// tile to f16 in place, and the MMAs and P run in f16; the K scale is in sl2
+// and the V scale is out_scale.
 //
 // Persistent: the grid holds at most one CTA per SM and CTA b takes items
 // b, 2G-1-b, 2G+b, ... of the LPT-ordered list (G = grid size; the order
@@ -332,8 +365,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < PF_KST; ++i) mbar_init(&bars->k_land[i], 1);
     for (int i = 0; i < PF_VST; ++i) mbar_init(&bars->v_land[i], 1);
-    mbar_init(&bars->q_conv[0], 1);
-    mbar_init(&bars->q_conv[1], 1);
+    mbar_init(&bars->q_conv[0], 4);  // one arrival per warp of the softmax warpgroup
+    mbar_init(&bars->q_conv[1], 4);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -583,7 +616,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 k_ready = true;
               }
               if (!q_ready) {
-                // an e4m3 call's Q is usable once warp 11 has converted it
+                // an e4m3 call's Q is usable once its softmax warpgroup has converted it
                 if (!mbar_wait(FP8 ? &bars->q_conv[X] : &bars->q_full[X], q_tot & 1, status,
                                abort_flag)) {
                   ok = false;
@@ -618,34 +651,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         mbar_wait(&bars->drain, 0, status, nullptr);
       }
     }
-  } else if (FP8 && warp == 11) {
-    // ------------------------------------------------------------ Q converter (e4m3 calls)
-    // Each item's Q tiles (bf16, as TMA loaded them) become f16 in place for
-    // the f16 MMAs: an elementwise change, so the swizzled layout stays.
-    int q_tot0 = 0, q_tot1 = 0;
-    bool ok = true;
-    for (int k = 0; ok && k * GS < n_items; ++k) {
-      const Item it = load_item(p, item_at(k), n_items, NP, KC);
-      const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
-      int u0;
-      if (union_tiles(subA, subB, u0) <= 0) continue;
-#pragma unroll
-      for (int X = 0; X < 2; ++X) {
-        const Sub& u = X ? subB : subA;
-        int& q_tot = X ? q_tot1 : q_tot0;
-        if (!ok || u.x1 <= u.x0) continue;
-        if (!__all_sync(FULL, mbar_wait(&bars->q_full[X], q_tot & 1, status, abort_flag))) {
-          ok = false;
-          continue;
-        }
-        unsigned* qw = reinterpret_cast<unsigned*>(sQ + X * C::TILE);
-        for (int w = lane; w < C::TILE / 4; w += 32) qw[w] = bf16x2_to_f16x2(qw[w]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->q_conv[X]);
-        ++q_tot;
-      }
-    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
@@ -663,6 +668,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     static_assert(PF_VST == 2, "the packed V ring position assumes two stages");
     unsigned ph = 0;
     bool ok = true;
+    int qn = 0;             // Q tiles of this sub-tile converted so far (FP8)
+    bool q_ahead = false;   // this item's Q tile was converted during the previous item
     Item it = load_item(p, item_at(0), n_items, NP, KC);
     for (int k = 0; ok && k * GS < n_items; ++k) {
       const Sub u = make_sub(p, it, head_pairs, X);
@@ -694,6 +701,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const int chunk = it.chunk;
       float m_run = -INFINITY, l_run = 0.f;
       const int nt = u.x1 - u.x0;
+      if constexpr (FP8) {
+        // an e4m3 call's Q tile becomes f16 before its first scores
+        if (nt > 0 && !q_ahead) {
+          if (!convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
+                                       qn & 1, row, status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++qn;
+        }
+        q_ahead = false;
+      }
       for (int c = 0; c < nt; ++c) {
         const int kt = u.x0 + c;
         const int key0 = kt * BLOCK_N;
@@ -803,6 +822,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       // The next item's metadata is fetched here, where the score registers
       // are dead, and lands while the epilogue runs.
       const Item nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
+      if constexpr (FP8) {
+        // The next item's Q tile of this sub-tile is loaded once this item's
+        // last S MMA is done: convert it now, while the last P V runs, so
+        // the next item's first scores need not wait for the epilogue.
+        if (ok && make_sub(p, nxt, head_pairs, X).x1 > make_sub(p, nxt, head_pairs, X).x0) {
+          if (!convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
+                                       qn & 1, row, status, abort_flag)) {
+            ok = false;
+          } else {
+            ++qn;
+            q_ahead = true;
+          }
+        }
+      }
 
       // ---------------------------------------------------------- epilogue
       // The normalised row goes to out, or (partial-result mode) to o32 in
