@@ -22,7 +22,9 @@
 //              page copy (over an e4m3 cache it also widens each K tile)
 //   warp  9    MMA issuer (one thread)
 //   warp 10    TMA producer of the V tiles (2-stage ring), likewise
-//   warp 11    idle (it completes the third warpgroup for setmaxnreg)
+//   warp 11    idle (it completes the third warpgroup for setmaxnreg); over an
+//              e4m3 cache at d 128 it widens the last 48 rows of each K and V
+//              tile
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
 // [384,384+D).  P (bf16, 64 columns) overwrites the upper half of its S
 // buffer and is read back from TMEM as the A operand of P V; the next scores
@@ -144,7 +146,7 @@ __device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
   return r;
 }
 
-// Widens the first `rows` rows of an e4m3 tile, stored as rows of D bytes
+// Widens rows [row0, row1) of an e4m3 tile, stored as rows of D bytes
 // in the last BLOCK_N x D bytes of a K or V stage, in place into the stage's
 // f16 tile in the 128-byte-swizzled layout: code c of row r goes to d half
 // c / 64, 16-byte chunk (c % 64) / 8, which sits at chunk position
@@ -156,10 +158,13 @@ __device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
 // all its pieces before any store: f16 rows overlap only source rows at or
 // below the batch's last row (at d 128 the second d half of row r is
 // exactly source row r; at d 64 f16 row r >= 64 covers source rows 2r - 128
-// and 2r - 127), so every source row is read before it is overwritten.  rows
-// is a multiple of 16, so passes come in whole batches.
+// and 2r - 127), so every source row is read before it is overwritten.  row0
+// and row1 are multiples of 16, so passes come in whole batches.  At d 128,
+// where f16 row r overlaps source row r alone, warps may widen disjoint row
+// ranges of one tile at the same time.
 template <int D>
-__device__ __forceinline__ void widen_e4m3_in_place(unsigned char* stage, int rows, int lane) {
+__device__ __forceinline__ void widen_e4m3_in_place(unsigned char* stage, int row0, int row1,
+                                                    int lane) {
   constexpr int RPP = 512 / D;
   constexpr int U = (D == 128) ? 4 : 2;
   constexpr int HALF = BLOCK_M * 128;  // bytes of one d half of a tile
@@ -172,11 +177,11 @@ __device__ __forceinline__ void widen_e4m3_in_place(unsigned char* stage, int ro
     r0 = lane >> 2;
     c = lane & 3;
   }
-  const int n_pass = rows / RPP;
+  const int ps0 = row0 / RPP, ps1 = row1 / RPP;
   const unsigned char* src0 = stage + SRC8 + r0 * D + c * 16;
   unsigned char* dst0 = stage + (c >> 2) * HALF + r0 * 128;
   const int cc = 2 * (c & 3);
-  for (int ps = 0; ps < n_pass; ps += U) {
+  for (int ps = ps0; ps < ps1; ps += U) {
     uint4 w[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) w[u] = *reinterpret_cast<const uint4*>(src0 + (ps + u) * RPP * D);
@@ -327,6 +332,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                    const __grid_constant__ CUtensorMap kvmap, float sl2, float out_scale) {
   using C = PrefillCfg<D>;
   constexpr bool MMA_F16 = HALF || FP8;  // operand and P type of the MMAs
+  // e4m3 at d 128: warp 11 widens rows [HELP_ROW, BLOCK_N) of every K and V
+  // tile, the producers rows [0, HELP_ROW) (10 KB and 12 KB of f16 a tile
+  // instead of 16 KB for each producer, on three SM sub-partitions)
+  constexpr bool HELP = FP8 && D == 128;
+  constexpr int HELP_ROW = 80;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -354,12 +364,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->p_full[i], BLOCK_M);
       mbar_init(&bars->o_final[i], 1);
     }
+    // an e4m3 d 128 stage is announced by its producer and by warp 11
     for (int i = 0; i < PF_KST; ++i) {
-      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_full[i], HELP ? 2 : 1);
       mbar_init(&bars->k_empty[i], 1);
     }
     for (int i = 0; i < PF_VST; ++i) {
-      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_full[i], HELP ? 2 : 1);
       mbar_init(&bars->v_empty[i], 1);
     }
     mbar_init(&bars->q_empty, 1);
@@ -525,7 +536,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           }
           const int key_base = (u0 + j) * BLOCK_N;
           const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
-          widen_e4m3_in_place<D>(ring + st * C::TILE, n_load * rows_box, lane);
+          widen_e4m3_in_place<D>(ring + st * C::TILE, 0,
+                                 HELP ? min(n_load * rows_box, HELP_ROW) : n_load * rows_box,
+                                 lane);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
@@ -650,6 +663,43 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, status, nullptr);
       }
+    }
+  } else if (HELP && warp == 11) {
+    // ------------------------------------------------------------ e4m3 widening helper
+    // Follows the producers' tile sequence: for each key tile, K then V (the
+    // order the MMAs need them), waits for the tile's bytes, widens rows
+    // [HELP_ROW, rows) in place and adds its arrival to the stage's full
+    // barrier.  A stage is refilled only after the MMAs that read it, which
+    // wait for this arrival, so a land barrier is never two phases ahead.
+    int jg = 0;
+    bool ok = true;
+    for (int k = 0; ok && k * GS < n_items; ++k) {
+      const Item it = load_item(p, item_at(k), n_items, NP, KC);
+      const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
+      int u0;
+      const int n_union = union_tiles(subA, subB, u0);
+      if (n_union <= 0) continue;
+      for (int j = 0; ok && j < n_union; ++j) {
+        const int jt = jg + j;
+        const int key_base = (u0 + j) * BLOCK_N;
+        const int rows = min(pages_per_tile, (it.s - key_base + rows_box - 1) / rows_box) * rows_box;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int nst = kv ? PF_VST : PF_KST;
+          const int st = jt % nst;
+          uint64_t* land = kv ? &bars->v_land[st] : &bars->k_land[st];
+          if (!__all_sync(FULL, mbar_wait(land, (jt / nst) & 1, status, abort_flag))) {
+            ok = false;
+            break;
+          }
+          widen_e4m3_in_place<D>((kv ? sV : sK) + st * C::TILE, HELP_ROW, max(rows, HELP_ROW),
+                                 lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
+        }
+      }
+      jg += n_union;
     }
   }
   } else {
