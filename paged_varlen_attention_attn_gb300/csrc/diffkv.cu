@@ -9,10 +9,12 @@
 // pattn_varlen_fwd's (causal or not, sliding window, GQA, sinks); out is
 // [T][H][dv].
 //
-// The same generic kernel serves the prefill rows of an e4m3 cache in the
-// standard layout ([2][num_blocks][block_size][num_kv_heads][d]: K and V rows
-// are fetched from their two planes into one staged row), widening the codes
-// with the hardware pair conversion and applying the per-tensor scales.
+// The kernel also has an instance for the standard layout
+// ([2][num_blocks][block_size][num_kv_heads][d]: K and V rows fetched from
+// their two planes into one staged row) over an e4m3 cache, which widens the
+// codes with the hardware pair conversion and applies the per-tensor scales.
+// It served the prefill rows of e4m3 calls before the tensor-core prefill
+// kernel widened e4m3 tiles itself; the library no longer calls it.
 //
 // A generic SIMT kernel for any dk, dv that are multiples of 32 up to 256,
 // not a tensor-core one.  One CTA per (query token, KV head): its four warps

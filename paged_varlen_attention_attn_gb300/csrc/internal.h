@@ -83,7 +83,8 @@ WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int sp
 cudaError_t launch_diffkv(const Problem& p, int dk, int dv);
 // The generic (SIMT) kernel on any cache type: split selects the standard
 // layout (K and V planes, dk == dv == p.D); skip_decode leaves the rows of
-// requests with query_len 1 to the decode kernel.
+// requests with query_len 1 to the decode kernel.  Only launch_diffkv calls
+// it (DiffKV layout, no split).
 cudaError_t launch_generic(const Problem& p, int dk, int dv, bool split, bool skip_decode);
 
 // Kernel launchers; each returns the launch's cudaError_t.
