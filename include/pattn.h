@@ -147,8 +147,9 @@ typedef struct {
  *   window          <= 0: no window; > 0: keys with p - k < window are visible
  *   causal          1: k <= p; 0: every key < seq_len (then window must be <= 0)
  *   kv_dtype        a pattn_kv_dtype_t.  With e4m3, decode rows run on the
- *                   bandwidth-bound decode kernel and prefill rows on a
- *                   generic (SIMT, not tensor-core) kernel
+ *                   bandwidth-bound decode kernel and prefill rows on the
+ *                   tensor-core prefill kernel, which widens K and V tiles to
+ *                   f16 (exactly) and rounds q to f16 for its f16 MMAs
  *   kv_scale        host float[2] {k_scale, v_scale}; required for e4m3, ignored
  *                   for bf16 (may be NULL)
  *   ext             host sizes, workspace and stream (see pattn_ext_t)
@@ -251,8 +252,9 @@ pattn_status_t pattn_decode_fwd_static(const void* q, const void* kv_cache,
  * name the same blocks (the pass reads row 0's), and every request's cached
  * context (seq_len - query_len) must cover the prefix; a request whose
  * context does not is reported as bad metadata (its rows are finite but
- * unspecified).  causal must be 1 and window <= 0; e4m3 caches are not
- * supported (PATTN_ERR_UNSUPPORTED).  The workspace comes from
+ * unspecified).  causal must be 1 and window <= 0 (else
+ * PATTN_ERR_UNSUPPORTED); bf16, f16 and e4m3 caches are served as by
+ * pattn_varlen_fwd.  The workspace comes from
  * pattn_cascade_workspace_bytes: besides the two passes' own scratch it holds
  * their fp32 partial results, 2 * num_tokens * num_heads * (head_size + 1)
  * floats.  The status word is read with pattn_read_device_status as usual.

@@ -585,7 +585,6 @@ pattn_status_t pattn_cascade_fwd(const void* q, const void* kv_cache, const int3
   const int P = common_prefix_len;
   if (P <= 0 || P % block_size != 0) return PATTN_ERR_INVALID_ARGUMENT;
   if (causal != 1 || window > 0) return PATTN_ERR_UNSUPPORTED;
-  if (kv_dtype == PATTN_KV_FP8_E4M3) return PATTN_ERR_UNSUPPORTED;  // the prefix pass is a prefill
   // The prefix pass is one request of every query token: its 128-key tiles
   // need the same page rule as any prefill.
   if (!(BLOCK_N % block_size == 0 || block_size % BLOCK_N == 0)) return PATTN_ERR_UNSUPPORTED;

@@ -198,7 +198,7 @@ def _casc(lib, prefix=32, **kw):
     (0, {}, 1),                                    # no prefix
     (32, dict(causal=0), 2),                       # cascade is causal only
     (32, dict(window=64), 2),                      # no window
-    (32, dict(kv_dtype=1, kv_scale=(1.0, 1.0)), 2),  # e4m3 cache
+    (32, dict(kv_dtype=1), 1),                     # e4m3 cache without scales
 ])
 def test_cascade_arguments_are_rejected_on_the_host(lib, prefix, kw, status):
     assert _casc(lib, prefix=prefix, **kw) == status

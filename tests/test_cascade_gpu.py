@@ -2,8 +2,9 @@
 requests share their first common_prefix_len keys (the same blocks in every
 block-table row) must give plain attention -- the float64 oracle's result --
 and pattn_varlen_fwd's result within the tolerance.  Decode-only and mixed
-batches, short and long prefixes, f16, and a request whose cached context
-does not cover the prefix (reported as bad metadata, others exact)."""
+batches, short and long prefixes, f16, e4m3 caches (the prefix pass then runs
+the tensor-core prefill over widened e4m3 tiles), and a request whose cached
+context does not cover the prefix (reported as bad metadata, others exact)."""
 import numpy as np
 import pytest
 import torch
@@ -41,6 +42,7 @@ def run_cascade(case, prefix, num_splits=0):
                        case.query_start_loc, scale=case.scale, num_heads=s.num_heads,
                        num_kv_heads=s.num_kv_heads, head_size=s.head_size,
                        block_size=s.block_size, common_prefix_len=prefix, kv_dtype=s.kv_dtype,
+                       kv_scale=case.kv_scale if s.kv_dtype == W.KV_FP8_E4M3 else None,
                        max_query_len=case.max_query_len, max_seq_len=case.max_seq_len,
                        num_splits=num_splits, out=out)
     st = pa.pattn_read_device_status(pa.forward.last_ext)
@@ -91,6 +93,34 @@ def test_cascade_f16():
     assert st == 0
     a, b = _rows(case)
     assert_close(out[a:b].float().cpu().numpy(), ref[a:b], W.KV_F16)
+
+
+@pytest.mark.parametrize("bs", [16, 128])
+def test_cascade_e4m3_mixed_batch(bs):
+    prefix = 256
+    q_lens = [200, 1, 1, 64, 1, 130]
+    seq_lens = [prefix + 300, prefix + 900, prefix + 5, prefix + 64, prefix + 2000, prefix + 130]
+    case = shared_prefix_case("casc_e4m3", q_lens, seq_lens, 8, 2, 128, bs, prefix, 1990 + bs,
+                              kv_dtype=W.KV_FP8_E4M3)
+    ref, _ = oracle_all(case)
+    out, st = run_cascade(case, prefix)
+    assert st == 0
+    a, b = _rows(case)
+    assert_close(out[a:b].float().cpu().numpy(), ref[a:b], W.KV_FP8_E4M3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_cascade_e4m3_decode_batch(d):
+    rng = np.random.default_rng(d)
+    B, Hkv, G, bs, prefix = 10, 2, 4, 16, 512
+    seq = [prefix + int(x) for x in rng.integers(1, 700, B)]
+    case = shared_prefix_case("casc_e4m3_dec", [1] * B, seq, G * Hkv, Hkv, d, bs, prefix,
+                              1995 + d, kv_dtype=W.KV_FP8_E4M3)
+    ref, _ = oracle_all(case)
+    out, st = run_cascade(case, prefix)
+    assert st == 0
+    a, b = _rows(case)
+    assert_close(out[a:b].float().cpu().numpy(), ref[a:b], W.KV_FP8_E4M3)
 
 
 def test_cascade_context_shorter_than_prefix_is_reported():
