@@ -501,7 +501,8 @@ def run_cascade(args, world, rank, local, prefix):
     """Time pattn_cascade_fwd against pattn_varlen_fwd on a decode batch whose
     requests share a long cached prefix: 64 requests, `prefix` keys shared
     (default 32768: 134 MB of K/V, more than L2), own suffixes U{128..1024},
-    H 32 / Hkv 8, d 128, block 16 (seed 1501).
+    H 32 / Hkv 8, d 128, block 16 (seed 1501); bf16, or f16 / e4m3 with
+    --f16 / --fp8.
     value = the plain call's algorithmic KV bytes / the cascade call's time
     (effective GB/s); the line also gives both times."""
     import torch
@@ -513,8 +514,9 @@ def run_cascade(args, world, rank, local, prefix):
     B = 64
     suffix = W._uniform_ints(128, 1024, B, 1501)
     seq = [prefix + x for x in suffix]
+    kv = W.KV_FP8_E4M3 if args.fp8 else (W.KV_F16 if args.f16 else W.KV_BF16)
     spec = W.CaseSpec("cascade_decode", [1] * B, seq, 32, 8, 128, 16,
-                      pool_blocks=sum((s + 15) // 16 for s in seq) + 8, seed=1501)
+                      pool_blocks=sum((s + 15) // 16 for s in seq) + 8, seed=1501, kv_dtype=kv)
     case = W.make_case(spec, device=dev)
     case.block_table[:, :prefix // 16] = case.block_table[0, :prefix // 16].clone()
     counts = work_counts(spec)
@@ -524,6 +526,7 @@ def run_cascade(args, world, rank, local, prefix):
     out = torch.empty_like(case.q)
     ws = pa.Workspace()
     kw = dict(scale=case.scale, num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+              kv_dtype=kv, kv_scale=case.kv_scale if kv == W.KV_FP8_E4M3 else None,
               max_query_len=1, max_seq_len=max(seq), out=out, workspace=ws, stream=stream)
 
     def plain():
@@ -562,9 +565,11 @@ def run_cascade(args, world, rank, local, prefix):
             "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_casc, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16 (fp32 accumulate)", "data": "synthetic (seeded N(0,1))",
+            "dtype": {0: "bf16 (fp32 accumulate)", 1: "e4m3 KV, bf16 Q/out, fp32 accumulate",
+                      2: "f16 (fp32 accumulate)"}[kv], "data": "synthetic (seeded N(0,1))",
             "config": {"workload": f"{B} decode requests sharing a {prefix}-key prefix, "
-                                   f"suffixes 128..1024, H 32, Hkv 8, d 128, block 16",
+                                   f"suffixes 128..1024, H 32, Hkv 8, d 128, block 16, "
+                                   f"kv {['bf16', 'e4m3', 'f16'][kv]}",
                        "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)"},
             "plain_ms_per_step": round(ms_plain, 5),
             "speedup_over_plain": round(ms_plain / ms_casc, 3),
