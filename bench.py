@@ -5,9 +5,19 @@
 
 One step = one pattn_varlen_fwd call (plan, prefill, decode, combine -- every
 phase the workload needs) over one synthetic batch already resident in HBM.
-The default workload is the decode-only GQA batch (64 requests, query_len 1,
-seq_len ~ U{512..4096}, 32 query / 8 KV heads, head 128, block 16, 20k-block
-pool); --config 1..5 selects the other workloads.  Prints ONE JSON line.
+The default workload is the largest one, the mixed batch that exercises both
+kernels: 4 chunked prefills of 2048 new tokens on 6144 cached ones plus 192
+decodes with seq_len ~ U{1024..32768}, sliding window 4096, 64 query / 8 KV
+heads, head 128, block 16 (13.4 GB cache).  --config 1..5 selects the other
+workloads.  Prints ONE JSON line.
+
+value: the step's fraction of its roofline, in percent: the roofline time
+max(F / P_tensor, B / BW_hbm) of the step's algorithmic work (F: unmasked
+prefill FLOPs, 4 d per visible (row, key, head); B: visible decode K/V bytes,
+the prefill requests' visible K/V bytes, q and out) divided by the measured
+step time.  The line also carries each kernel's own roofline (prefill TFLOP/s
+against the bf16 tensor peak, decode KV GB/s against HBM) from its own
+event-timed duration.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
 library's stream; L2 is flushed before every step, outside the events: a
@@ -83,10 +93,20 @@ def work_counts(spec):
         if ql > 1:
             lo = max(0, s - ql - spec.window + 1) if spec.window > 0 else 0
             bytes_prefill += (s - lo) * 2 * spec.num_kv_heads * spec.head_size * es
+    tokens = int(sum(spec.q_lens))
+    qo_bytes = 2.0 * tokens * spec.num_heads * spec.head_size * 2
     return dict(flops_prefill=flops_prefill, flops_decode=flops_decode,
-                bytes_decode=bytes_decode, bytes_prefill=bytes_prefill,
-                tokens=int(sum(spec.q_lens)),
+                bytes_decode=bytes_decode, bytes_prefill=bytes_prefill, bytes_qo=qo_bytes,
+                tokens=tokens, row_keys=float(spec.num_heads) * float(dec.sum() + pre.sum()),
                 decode_rows=int(len(dec)), prefill_rows=int(len(pre)))
+
+
+def roofline_seconds(counts, pk):
+    """The step's roofline time: max(F / P_tensor, B / BW) over its algorithmic
+    work (prefill FLOPs; every visible K/V byte, q and out)."""
+    f = counts["flops_prefill"] / (pk["bf16_tflops"] * 1e12)
+    b = (counts["bytes_decode"] + counts["bytes_prefill"] + counts["bytes_qo"]) / (pk["hbm_gbs"] * 1e9)
+    return max(f, b)
 
 
 def peaks():
@@ -341,6 +361,7 @@ def run_ours(args, spec, world, rank, local_rank):
         e2e = run_e2e(args, case, spec, counts, dev, stream, ca, ws)
 
     return dict(case=case, counts=counts, ms=ms_max, ms_local=ms, ms_min=min(step_ms),
+                ms_median=statistics.median(step_ms),
                 wall=wall, phase_ms={k: statistics.mean(v) for k, v in phase_ms.items()},
                 clocks=clk, splits=splits, launches=launches_per_step * K, e2e=e2e)
 
@@ -417,70 +438,117 @@ def run_e2e(args, case, spec, counts, dev, stream, ca, ws):
 
 # ---------------------------------------------------------------- oracle (CPU)
 
-def oracle_sample(case, spec, max_rows):
-    """Host arrays and (token, head) rows of a bounded sample of the workload:
-    whole requests, taken in order until max_rows rows."""
+def oracle_sample(case, spec, stride):
+    """Host arrays and (token, head) rows of a bounded, uniform sample of the
+    workload: every stride-th decode request and, of each prefill request,
+    every stride-th query row (all heads of each chosen token).  Only the KV
+    blocks the chosen rows can see are copied to the host (block ids remapped;
+    the oracle reads no other block)."""
     import torch
     qsl = case.query_start_loc.cpu().numpy()
     sl = case.seq_lens.cpu().numpy()
-    H = spec.num_heads
-    rows, reqs = [], []
+    H, bs, W = spec.num_heads, spec.block_size, spec.window
+    toks, need, n_dec = [], {}, 0
     for r in range(len(sl)):
-        t0, t1 = int(qsl[r]), int(qsl[r + 1])
-        if t1 == t0:
+        t0, ql, s = int(qsl[r]), int(qsl[r + 1] - qsl[r]), int(sl[r])
+        if ql <= 0:
             continue
-        if rows and len(rows) + (t1 - t0) * H > max_rows:
-            break
-        reqs.append(r)
-        rows.extend((t, h) for t in range(t0, t1) for h in range(H))
-    bs = spec.block_size
+        if ql == 1:
+            pick = [0] if n_dec % stride == 0 else []
+            n_dec += 1
+        else:
+            pick = list(range(stride // 2 if ql > stride // 2 else 0, ql, stride))
+        if not pick:
+            continue
+        ctx = s - ql
+        lo = min(max(0, ctx + i - W + 1) if W > 0 else 0 for i in pick)
+        hi = max(min(s, ctx + i + 1) if spec.causal else s for i in pick)
+        need[r] = (lo // bs, (hi + bs - 1) // bs)
+        toks.extend(t0 + i for i in pick)
     bt_full = case.block_table.cpu()
-    blocks = sorted({int(b) for r in reqs
-                     for b in bt_full[r, :(int(sl[r]) + bs - 1) // bs]})
+    blocks = sorted({int(b) for r, (a, e) in need.items() for b in bt_full[r, a:e]})
     remap = {b: i for i, b in enumerate(blocks)}
     kv = case.kv_cache.index_select(1, torch.tensor(blocks, device=case.kv_cache.device)).cpu()
     bt = torch.zeros_like(bt_full)
-    for r in reqs:
-        n = (int(sl[r]) + bs - 1) // bs
-        bt[r, :n] = torch.tensor([remap[int(b)] for b in bt_full[r, :n]], dtype=torch.int32)
+    for r, (a, e) in need.items():
+        bt[r, a:e] = torch.tensor([remap[int(b)] for b in bt_full[r, a:e]], dtype=torch.int32)
     q = case.q.cpu().view(torch.int16).numpy().view(np.uint16)
     kvn = kv.view(torch.int16).numpy().view(np.uint16) if spec.kv_dtype != 1 else kv.numpy()
-    sub = type(spec)(**{**spec.__dict__, "q_lens": [spec.q_lens[r] for r in reqs],
-                        "seq_lens": [spec.seq_lens[r] for r in reqs]})
-    return dict(q=q, kv=kvn, bt=bt.numpy(), sl=sl, qsl=qsl, rows=np.array(rows, np.int32),
-                reqs=reqs, sub=sub)
+    rows = np.array([(t, h) for t in toks for h in range(H)], np.int32).reshape(-1, 2)
+    return dict(q=q, kv=kvn, bt=bt.numpy(), sl=sl, qsl=qsl, rows=rows, tokens=len(toks))
 
 
-def time_oracle(case, spec, max_rows, repeats=1):
+def sample_row_keys(spec, qsl, rows):
+    """Visible (row, key) pairs of the sampled rows: the oracle's work."""
+    qsl = np.asarray(qsl)
+    r = np.searchsorted(qsl, rows[:, 0], side="right") - 1
+    s = np.asarray(spec.seq_lens)[r]
+    ql = np.asarray(spec.q_lens)[r]
+    p = (s - ql) + (rows[:, 0] - qsl[r])
+    hi = np.minimum(p + 1, s) if spec.causal else s
+    lo = np.maximum(0, p - spec.window + 1) if spec.window > 0 else 0
+    return float(np.maximum(0, hi - lo).sum())
+
+
+def time_oracle(case, spec, stride, threads=None):
+    """Wall time of the float64 oracle on a uniform 1/stride sample."""
     import oracle
-    smp = oracle_sample(case, spec, max_rows)
+    smp = oracle_sample(case, spec, stride)
     kw = dict(scale=case.scale, num_heads=spec.num_heads, num_kv_heads=spec.num_kv_heads,
               head_size=spec.head_size, block_size=spec.block_size, window=spec.window,
               causal=spec.causal, kv_dtype=spec.kv_dtype, kv_scale=case.kv_scale)
-    cores = os.cpu_count() or 1
-    times = []
-    for _ in range(repeats):
-        t0 = time.perf_counter()
-        oracle.ref_rows(smp["q"], smp["kv"], smp["bt"], smp["sl"], smp["qsl"],
-                        rows=smp["rows"], num_threads=cores, **kw)
-        times.append(time.perf_counter() - t0)
-    c = work_counts(smp["sub"])
-    return dict(seconds=statistics.mean(times), counts=c, cores=cores,
-                sample=f"{len(smp['reqs'])} of {len(spec.q_lens)} requests, "
-                       f"{len(smp['rows'])} (token, head) rows, all their visible keys")
+    cores = threads or os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.ref_rows(smp["q"], smp["kv"], smp["bt"], smp["sl"], smp["qsl"],
+                    rows=smp["rows"], num_threads=cores, **kw)
+    sec = time.perf_counter() - t0
+    rk = sample_row_keys(spec, smp["qsl"], smp["rows"])
+    return dict(seconds=sec, row_keys=rk, cores=cores, tokens=smp["tokens"],
+                sample=f"one in {stride} decode requests and one in {stride} query rows of "
+                       f"each prefill request: {smp['tokens']} of {sum(spec.q_lens)} query "
+                       f"tokens x {spec.num_heads} heads, all their visible keys "
+                       f"({rk:.3g} (row, key) pairs)")
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_stride(case, spec, budget_s, threads=None):
+    """The sample stride whose oracle run takes about budget_s: calibrated on
+    a small sample first."""
+    full = work_counts(spec)["row_keys"]
+    cal_stride = max(1, int(full / 2e6))  # ~2M (row, key) pairs
+    cal = time_oracle(case, spec, cal_stride, threads)
+    rate = cal["row_keys"] / max(cal["seconds"], 1e-6)
+    want = max(1.0, rate * budget_s)
+    return max(1, int(math.ceil(full / want)))
 
 
 # ---------------------------------------------------------------- metric
 
-def metric_value(counts, seconds, cfg):
-    """(value, unit, bound) for the workload."""
-    if cfg in (2, 5):
-        return counts["bytes_decode"] / seconds / 1e9, "GB/s", "hbm"
-    if cfg == 3:
-        return counts["flops_prefill"] / seconds / 1e12, "TFLOP/s", "tensor"
-    if cfg == 4:
-        return counts["tokens"] / seconds, "tokens/s", "mixed"
-    return counts["tokens"] / seconds, "tokens/s", "latency"
+UNIT = "% of roofline"
+
+
+def metric_value(counts, seconds, pk):
+    """The metric: the step's roofline time over its measured time, percent."""
+    return 100.0 * roofline_seconds(counts, pk) / seconds
+
+
+def config_dict(spec, cfg, world):
+    """The `config` of both arms' lines (identical, so the two are comparable)."""
+    return {"workload": workload_desc(spec, cfg), "config_index": cfg,
+            "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def workload_desc(spec, cfg):
@@ -748,12 +816,13 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--oracle-rows", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU baseline: oracle seconds on the host cores (1-thread: a quarter)")
     ap.add_argument("--cascade-prefix", type=int, default=32768,
                     help="--op cascade: shared prefix length in keys (multiple of 16)")
     ap.add_argument("--f16", action="store_true",
@@ -801,63 +870,88 @@ def main():
     if args.op == "diffkv":
         return run_diffkv(args, spec, world, rank, local)
     res = run_ours(args, spec, world, rank, local)
+    line = attention_line(args, spec, world, rank, local, res)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
+def kernel_roofline(kind, counts, ms, pk, pk_src, spec):
+    """One kernel's roofline object from its event-timed duration."""
+    if kind == "prefill":
+        achieved = counts["flops_prefill"] / (ms / 1e3) / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "kernel": "prefill_kernel" + (" (e4m3 tiles widened to f16 in shared memory)"
+                                              if spec.kv_dtype == 1 else ""),
+                "work_per_launch": f"{counts['flops_prefill']:.6g} FLOP (4 d per visible "
+                                   f"(row, key, head))"}
+    else:
+        achieved = counts["bytes_decode"] / (ms / 1e3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "kernel": "decode_split_kernel",
+                "work_per_launch": f"{counts['bytes_decode']:.6g} B (2 d es per visible "
+                                   f"(key, KV head))"}
+    roof["kernel_ms"] = round(ms, 4)
+    roof["peak_source"] = (f"{pk_src} (MEASURED_PEAKS.json)" if pk_src == "measured"
+                           else pk_src)
+    roof["traffic"] = profiled_traffic(kind, spec.name)
+    return roof
+
+
+def attention_line(args, spec, world, rank, local, res):
     pk, pk_src = peaks()
     counts = res["counts"]
     sec = res["ms"] / 1e3
-    value_local, unit, bound = metric_value(counts, sec, args.config)
+    value_local = metric_value(counts, sec, pk)
+    # whole job: every replica processes the same work; value = the fraction
+    # of the aggregate roofline, i.e. total work / slowest replica's time
     value, _ = aggregate(value_local * sec, sec, device=f"cuda:{local}")
-
-    # dominant kernel and its roofline
     ph = res["phase_ms"]
-    if bound == "tensor" or (bound == "mixed" and ph["prefill"] >= ph["decode"]):
-        kind = "prefill"
-        achieved = counts["flops_prefill"] / (ph["prefill"] / 1e3) / 1e12
-        peak = pk["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4)}
-    else:
-        kind = "decode"
-        achieved = counts["bytes_decode"] / (ph["decode"] / 1e3) / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4)}
-    if kind == "decode":
-        roof["kernel"] = "decode_split_kernel"
-    elif spec.kv_dtype == 1:  # f16 MMAs run at the bf16 rate
-        roof["kernel"] = "prefill_kernel (e4m3 tiles widened to f16 in shared memory)"
-    else:
-        roof["kernel"] = "prefill_kernel"
-    roof["kernel_ms"] = round(ph[kind], 4)
-    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)" if pk_src == "measured" else pk_src
-    roof["traffic"] = profiled_traffic(kind, spec.name)
-
+    rooflines = {k: kernel_roofline(k, counts, ph[k], pk, pk_src, spec)
+                 for k in ("prefill", "decode") if ph.get(k, 0.0) > 0}
+    # dominant kernel: the longer of the two
+    dom = max(rooflines, key=lambda k: ph[k])
+    t_roof = roofline_seconds(counts, pk)
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 4),
+        "ms_per_step_median": round(res["ms_median"], 4),
+        "ms_per_step_min": round(res["ms_min"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
         {0: "bf16 (fp32 accumulate)", 1: "e4m3 KV, bf16 Q/out, fp32 accumulate",
          2: "f16 (fp32 accumulate)"}[spec.kv_dtype],
         "data": "synthetic (seeded N(0,1), seeded block permutation)",
-        "config": {"workload": workload_desc(spec, args.config), "config_index": args.config,
-                   "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
-                   "decode_splits": res["splits"],
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roof,
+        "config": config_dict(spec, args.config, world),
+        "value_definition": "100 x roofline time / step time; roofline time = "
+                            "max(prefill FLOPs / bf16 tensor peak, (decode K/V + prefill K/V "
+                            "+ q + out bytes) / HBM peak)",
+        "step": {"roofline_ms": round(t_roof * 1e3, 4),
+                 "prefill_tflop": round(counts["flops_prefill"] / 1e12, 4),
+                 "hbm_gb": round((counts["bytes_decode"] + counts["bytes_prefill"]
+                                  + counts["bytes_qo"]) / 1e9, 4),
+                 "tokens_per_s": round(counts["tokens"] / sec, 1),
+                 "prefill_tflops_over_step": round(counts["flops_prefill"] / sec / 1e12, 2),
+                 "decode_gbs_over_step": round(counts["bytes_decode"] / sec / 1e9, 1)},
+        "roofline": rooflines[dom],
+        "rooflines": rooflines,
         "phase_ms": {k: round(v, 4) for k, v in ph.items()},
+        "decode_splits": res["splits"],
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
-    if args.config == 4:
-        tf = counts["flops_prefill"] / (ph["prefill"] / 1e3) / 1e12 if ph["prefill"] > 0 else 0
-        gb = counts["bytes_decode"] / (ph["decode"] / 1e3) / 1e9 if ph["decode"] > 0 else 0
-        t_roof = max(counts["flops_prefill"] / (pk["bf16_tflops"] * 1e12),
-                     counts["bytes_decode"] / (pk["hbm_gbs"] * 1e9))
-        line["per_phase"] = {"prefill_tflops": round(tf, 2), "decode_gbs": round(gb, 1),
-                             "step_roofline_frac": round(t_roof / sec, 4)}
+    if args.config == 1:
+        line["latency_us"] = {"mean": round(res["ms"] * 1e3, 2),
+                              "median": round(res["ms_median"] * 1e3, 2),
+                              "min": round(res["ms_min"] * 1e3, 2)}
     if res["e2e"] is not None:
         e = res["e2e"]
-        v_e2e, _, _ = metric_value(counts, e["ms"] / 1e3, args.config)
-        line["e2e"] = {"value": round(v_e2e * world, 3), "unit": unit,
+        line["e2e"] = {"value": round(metric_value(counts, e["ms"] / 1e3, pk), 3),
+                       "unit": UNIT,
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "ms_per_step": round(e["ms"], 4),
                        "note": "serving step through the public API: q, the new tokens' K/V "
@@ -866,51 +960,64 @@ def main():
                                "the resident cache "
                                "(pattn_reshape_and_cache); attention; output read back"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        max_rows = args.oracle_rows or {1: 10**9, 2: 2048, 3: 2048, 4: 512, 5: 128}.get(args.config, 256)
-        ob = time_oracle(res["case"], spec, max_rows)
-        v_cpu, unit_cpu, _ = metric_value(ob["counts"], ob["seconds"], args.config)
-        line["cpu_baseline"] = {"value": round(v_cpu, 6), "unit": unit_cpu, "cores": ob["cores"],
-                                "kind": "oracle", "sample": ob["sample"],
-                                "seconds": round(ob["seconds"], 3)}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    import torch.distributed as dist
-    if dist.is_initialized():
-        dist.destroy_process_group()
+        line["cpu_baseline"] = cpu_baseline(res["case"], spec, counts, pk, args)
+    return line
+
+
+def cpu_baseline(case, spec, counts, pk, args):
+    """The float64 oracle as it stands, on the host cores, on a uniform sample
+    of the workload sized to ~15 s, in the metric's unit (the sample's share of
+    the step's roofline time over the oracle's time); plus a 1-thread time on
+    a smaller sample."""
+    stride = oracle_stride(case, spec, args.cpu_seconds)
+    ob = time_oracle(case, spec, stride)
+    frac = ob["row_keys"] / counts["row_keys"]
+    t_roof = roofline_seconds(counts, pk) * frac
+    one_stride = oracle_stride(case, spec, args.cpu_seconds / 4, threads=1)
+    o1 = time_oracle(case, spec, one_stride, threads=1)
+    t1_roof = roofline_seconds(counts, pk) * (o1["row_keys"] / counts["row_keys"])
+    return {"value": round(100.0 * t_roof / ob["seconds"], 9), "unit": UNIT,
+            "cores": ob["cores"], "kind": "oracle", "sample": ob["sample"],
+            "seconds": round(ob["seconds"], 3),
+            "row_keys_per_s": round(ob["row_keys"] / ob["seconds"], 1),
+            "cpu_model": cpu_model(),
+            "one_thread": {"value": round(100.0 * t1_roof / o1["seconds"], 9),
+                           "seconds": round(o1["seconds"], 3), "cores": 1,
+                           "row_keys_per_s": round(o1["row_keys"] / o1["seconds"], 1),
+                           "sample": o1["sample"]}}
 
 
 def run_reference(args, spec, world, rank):
-    """The float64 CPU oracle, timed on the host cores (rank 0 only)."""
+    """The float64 CPU oracle, timed on the host cores (rank 0 only), each step
+    a uniform sample of the workload sized so the whole run takes ~2 minutes;
+    value in the metric's unit (the sample's share of the step's roofline time
+    over the oracle's time)."""
     if world > 1 and rank != 0:
         return 0
-    import torch
     import workloads as W
     case = W.make_case(spec, device="cpu")
-    # Size each step's sample so the whole run stays within ~2 minutes:
-    # calibrate the oracle's time per row on a small sample first.
-    cal = time_oracle(case, spec, 64)
-    per_row = cal["seconds"] / max(1, cal["counts"]["decode_rows"] + cal["counts"]["prefill_rows"])
-    per_row /= max(1, spec.num_heads)
+    counts = work_counts(spec)
+    pk, _ = peaks()
     budget = 120.0 / (args.steps + args.warmup)
-    max_rows = args.oracle_rows or max(1, int(budget / max(per_row, 1e-9)))
+    stride = oracle_stride(case, spec, budget)
     for _ in range(args.warmup):
-        time_oracle(case, spec, max(1, max_rows // 8))
-    times, value_sum = [], 0.0
-    ob = None
+        time_oracle(case, spec, stride)
+    times, ob = [], None
     for _ in range(args.steps):
-        ob = time_oracle(case, spec, max_rows)
+        ob = time_oracle(case, spec, stride)
         times.append(ob["seconds"])
     sec = statistics.mean(times)
-    value, unit, _ = metric_value(ob["counts"], sec, args.config)
-    line = {"metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": unit,
+    t_roof = roofline_seconds(counts, pk) * ob["row_keys"] / counts["row_keys"]
+    value = 100.0 * t_roof / sec
+    line = {"metric": METRIC, "impl": "reference", "value": round(value, 9), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(spec, args.config),
-                       "config_index": args.config},
-            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": ob["cores"],
-                             "kind": "oracle", "sample": ob["sample"]},
-            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
+            "config": config_dict(spec, args.config, world),
+            "cpu_baseline": {"value": round(value, 9), "unit": UNIT, "cores": ob["cores"],
+                             "kind": "oracle", "sample": ob["sample"],
+                             "cpu_model": cpu_model()},
+            "e2e": {"value": round(value, 9), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

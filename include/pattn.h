@@ -215,14 +215,22 @@ pattn_status_t pattn_read_device_status(const pattn_ext_t* ext);
  * inside the library, held by every GPU that loads the library until the
  * process exits.  A batch whose partials need more
  * (num_seqs * num_heads * splits * (head_size + 1) * 4 bytes, roughly) returns
- * PATTN_ERR_WORKSPACE_TOO_SMALL; pass a smaller num_splits or use
- * pattn_varlen_fwd.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the array and it keeps the
- * last call's contents: calls whose work may overlap on the GPU (different
- * streams or host threads) race and must be serialised by the caller.
- * Device-detected metadata errors are clamped as in pattn_varlen_fwd but are
- * not reported (there is no workspace to read a status from).
+ * PATTN_ERR_WORKSPACE_TOO_SMALL before any GPU work; pass a smaller
+ * num_splits or use pattn_varlen_fwd.  Every call looks up the array's device
+ * address in the current context (cudaGetSymbolAddress, which allocates
+ * nothing), so the device that owns `stream` must be current; the first call
+ * in a context may load the library's device code, so make it before any
+ * stream capture.  Any context the runtime API can make current is served
+ * (the primary one, or one a host application created and made current).
+ * All calls share the array and it keeps the last call's contents: the
+ * status word and the partition counters are cleared on `stream` at the start
+ * of each call; calls whose work may overlap on the GPU (different streams or
+ * host threads) race and must be serialised by the caller.  Requests with
+ * query_len != 1 are skipped: their output rows are neither read nor written
+ * and they are not reported.  Device-detected metadata errors of the decode
+ * rows (a block id outside the pool, seq_len beyond the block table) are
+ * clamped as in pattn_varlen_fwd, those rows are zeroed, and nothing is
+ * reported (there is no workspace to read a status from).
  */
 #define PATTN_STATIC_SCRATCH_BYTES (32u << 20)
 pattn_status_t pattn_decode_fwd_static(const void* q, const void* kv_cache,

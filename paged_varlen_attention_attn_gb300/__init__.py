@@ -310,7 +310,7 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
             num_kv_heads, head_size, block_size, window=0, causal=1, kv_dtype=KV_BF16,
             kv_scale=None, max_query_len, max_seq_len, num_splits=0, out=None,
             workspace=None, stream=None, timing_events=None, sinks=None, head_size_v=0,
-            check=True):
+            check=True, lib=None):
     """pattn_varlen_fwd on torch tensors (all on one CUDA device).
 
     max_query_len / max_seq_len are host ints (as in FlashAttentionMetadata):
@@ -319,7 +319,8 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
     fp32 [num_heads] device tensor of attention-sink logits.  ``head_size_v``:
     > 0 selects the DiffKV cache layout [num_blocks, block_size, num_kv_heads,
     head_size + head_size_v] and an output of head size head_size_v (see
-    pattn_ext_t).  Returns ``out``.
+    pattn_ext_t).  ``lib``: a library handle from ``load(path)`` (default: the
+    built libpattn.so).  Returns ``out``.
     """
     import torch
     dev = q.device
@@ -336,7 +337,7 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
                    num_splits=num_splits, stream=stream.cuda_stream,
                    timing_events=timing_events, sinks=_sinks_ptr(sinks, num_heads, dev),
                    head_size_v=head_size_v)
-    need = pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size)
+    need = pattn_workspace_bytes(ext, num_heads, num_kv_heads, head_size, block_size, lib=lib)
     if need == 0:
         raise PattnError(1, "pattn_workspace_bytes")
     ws = (workspace or _default_ws).get(need, dev)
@@ -345,7 +346,7 @@ def forward(q, kv_cache, block_table, seq_lens, query_start_loc, *, scale, num_h
     st = pattn_varlen_fwd(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
                           seq_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(),
                           scale, num_heads, num_kv_heads, head_size, block_size, window,
-                          causal, kv_dtype, kv_scale, ext)
+                          causal, kv_dtype, kv_scale, ext, lib=lib)
     if check and st != 0:
         raise PattnError(st, "pattn_varlen_fwd")
     forward.last_ext = ext

@@ -3,6 +3,11 @@
 Each .cu file is compiled to an object in parallel, then linked into
 ``paged_varlen_attention_attn_gb300/_build/libpattn.so``.  One -gencode only
 (compute_103a -> sm_103a); -lineinfo keeps ncu's source attribution.
+
+``build_wait_test()`` compiles the same sources with PATTN_WAIT_TEST into
+``_build/wait_test/libpattn_wait_test.so``: a library that only the tests
+load, whose bounded waits give up after 10 ms instead of 2 s and which exports
+``pattn_test_set_wait_skip`` so a test can make one wait run out.
 """
 import concurrent.futures as cf
 import glob
@@ -35,18 +40,23 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+WAIT_TEST_DIR = os.path.join(OUT_DIR, "wait_test")
+WAIT_TEST_LIB = os.path.join(WAIT_TEST_DIR, "libpattn_wait_test.so")
+
+
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force=False, verbose=False, extra_flags=()):
+def build(force=False, verbose=False, extra_flags=(), lib=LIB):
     """Compile (if stale) and return the path of libpattn.so."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    if not force and up_to_date(lib):
+        return lib
+    out_dir = os.path.dirname(lib)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                     "-I", INCLUDE, "-I", CSRC] + list(extra_flags)
@@ -54,7 +64,7 @@ def build(force=False, verbose=False, extra_flags=()):
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         r = subprocess.run([nvcc, "-c", src, "-o", obj] + flags,
                            capture_output=True, text=True)
         return src, obj, r
@@ -67,14 +77,19 @@ def build(force=False, verbose=False, extra_flags=()):
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
             objs.append(obj)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"],
                        capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("link of libpattn.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_wait_test(force=False):
+    """The wait-test library (tests only): short wait limit, skip hook."""
+    return build(force=force, extra_flags=("-DPATTN_WAIT_TEST",), lib=WAIT_TEST_LIB)
 
 
 if __name__ == "__main__":

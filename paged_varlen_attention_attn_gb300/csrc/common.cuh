@@ -21,8 +21,14 @@ namespace pattn {
 constexpr unsigned PATTN_DEV_BAD_METADATA = 1u;
 constexpr unsigned PATTN_DEV_TIMEOUT = 2u;
 
-// A wait that has not finished after this long is treated as a hang.
+// A wait that has not finished after this long is treated as a hang.  The
+// wait-test build (PATTN_WAIT_TEST, a separate library that only the tests
+// load) shortens it so that a test can make a wait run out quickly.
+#ifdef PATTN_WAIT_TEST
+constexpr unsigned long long PATTN_WAIT_LIMIT_NS = 10000000ull;  // 10 ms
+#else
 constexpr unsigned long long PATTN_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+#endif
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -89,6 +95,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
       if (abort_flag) *abort_flag = 1;
       return false;
     }
+  }
+}
+
+// After a role gave up on a wait, a producer waits (bounded, whatever the
+// abort flag says) for the copies it armed on the stages of a ring of nst
+// stages, so that no copy is still writing shared memory when the CTA frees
+// its resources and exits.  Ring positions [0, armed_end) were armed in
+// order, position j on barrier bars[j % nst] in phase j / nst; the latest
+// position of each stage is the only phase of that barrier that can still be
+// open, and earlier phases of the same stage completed before it was armed.
+// skip_pos is a position that was not armed (-1: none).
+__device__ __forceinline__ void drain_armed(uint64_t* bars, int nst, int armed_end, int skip_pos,
+                                            unsigned* status) {
+  for (int j = armed_end - nst; j < armed_end; ++j) {
+    if (j < 0 || j == skip_pos) continue;
+    mbar_wait(&bars[j % nst], (j / nst) & 1, status, nullptr);
   }
 }
 

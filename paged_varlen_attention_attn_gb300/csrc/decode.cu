@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   if (q_len != 1) {
     // A call declared decode-only (max_query_len <= 1) runs no other kernel
     // over its requests: a longer one is bad metadata, reported and zeroed
-    // here (once, clamped to the output).
-    if (p.max_q <= 1 && q_len != 0 && grp == 0 && sp == 0) {
+    // here (once, clamped to the output).  A decode-rows-only call leaves
+    // such requests to another call.
+    if (p.max_q <= 1 && !p.decode_rows_only && q_len != 0 && grp == 0 && sp == 0) {
       if (threadIdx.x == 0) flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
       const int64_t a = static_cast<int64_t>(max(0, t0)) * p.H * D;
       const int64_t b = static_cast<int64_t>(min(p.T, t0 + max(q_len, 0))) * p.H * D;
@@ -281,6 +282,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
     if (lane == 0) tma_prefetch_desc(&kvmap);
     const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
     bool ok = true;
+    int armed_end = 0;  // units [0, armed_end) had their bytes posted
+#ifdef PATTN_WAIT_TEST
+    // wait-test build: this unit posts no bytes and issues no copy, so the
+    // consumers' wait for it runs out
+    const int skip_pos = (p.test_skip == 2 && blockIdx.x == 0) ? 0 : -1;
+#else
+    constexpr int skip_pos = -1;
+#endif
     for (int base = 0; ok && base < n_units; base += 32) {
       const int gu = base + lane;
       int blk = 0;
@@ -300,7 +309,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
           const int i = base + l, st = i % NST;
           if (i >= NST && !mbar_wait(&empty[st], ((i / NST) - 1) & 1, status, nullptr)) {
             good = 0;
-          } else {
+          } else if (i != skip_pos) {
+            armed_end = i + 1;
             const int key0 = (u_begin + i) * UNIT;
             const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
             unsigned char* dk = smem + st * C::STAGE;
@@ -320,6 +330,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         }
       }
     }
+    // A wait gave up: no copy armed here may still be writing shared memory
+    // when the CTA exits.  (Otherwise the consumers wait for every copy.)
+    if (!ok && lane == 0) drain_armed(full, NST, armed_end, skip_pos, status);
     return;  // nothing after this needs the producer
   }
 

@@ -38,6 +38,9 @@ struct Problem {
   int long_queries;  // a request may have more queries than keys (the cascade
                      // prefix pass: every token of the batch over the prefix,
                      // not causal); otherwise that is bad metadata
+  int decode_rows_only;  // the decode kernel serves the query_len == 1 rows and
+                         // leaves every other request's rows untouched and
+                         // unreported (they belong to another call)
   // Partial-result mode (cascade passes): when set, rows are written as
   // normalised fp32 o [T][H][D] and lse [T][H] (log2 units) instead of out.
   float* o32;
@@ -67,7 +70,22 @@ struct Problem {
   int pdl_trigger;  // the prefill kernel lets its dependent start once all of
                     // its CTAs are running (decode CTAs then take the SMs that
                     // finished prefill CTAs leave)
+#ifdef PATTN_WAIT_TEST
+  // Wait-test build only: 1 = CTA 0 of the prefill kernel posts no bytes and
+  // issues no copy for the first K tile it streams; 2 = CTA 0 of the decode
+  // kernel does the same for its first unit.  The wait for that tile then runs
+  // out (a barrier phase that nothing completes), which is how the tests reach
+  // the timeout path without faulting or hanging anything.
+  int test_skip;
+#endif
 };
+
+#ifdef PATTN_WAIT_TEST
+// Wait-test build only: sets Problem::test_skip for the calls that follow
+// (0 turns it off).  Exported as pattn_test_set_wait_skip.
+extern "C" void pattn_test_set_wait_skip(int mode);
+int test_wait_skip();
+#endif
 
 // Workspace layout for a problem (offsets in bytes, 256-byte aligned).
 // The header and the counters come first, so one memset of counters_end

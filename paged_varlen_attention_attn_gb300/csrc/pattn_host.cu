@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstddef>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/pattn.h"
@@ -272,6 +273,13 @@ CascadeLayout cascade_layout(const pattn_ext_t* ext, int H, int Hkv, int D, int 
 
 }  // namespace
 
+#ifdef PATTN_WAIT_TEST
+namespace {
+std::atomic<int> g_test_wait_skip{0};
+}
+int test_wait_skip() { return g_test_wait_skip.load(); }
+#endif
+
 bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv, int bs,
                    int NB, int box_rows) {
   EncodeTiledFn enc = encode_fn();
@@ -398,6 +406,10 @@ extern "C" {
 
 int pattn_version(void) { return 10000; }
 
+#ifdef PATTN_WAIT_TEST
+void pattn_test_set_wait_skip(int mode) { g_test_wait_skip.store(mode); }
+#endif
+
 const char* pattn_status_string(int s) {
   switch (s) {
     case PATTN_OK: return "ok";
@@ -506,6 +518,9 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.o_part = reinterpret_cast<float*>(ws + L.o_part_off);
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.stream = static_cast<cudaStream_t>(ext->stream);
+#ifdef PATTN_WAIT_TEST
+  p.test_skip = test_wait_skip();
+#endif
 
   // Optional per-phase events (profiling): [2k] before and [2k+1] after phase k.
   auto mark = [&](int idx) {

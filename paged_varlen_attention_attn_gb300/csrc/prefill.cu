@@ -420,6 +420,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     int jg = 0;        // key tiles streamed so far (ring position)
     int n_worked = 0;  // items with at least one key tile so far
+    // For the drain after a wait gave up: ring positions [0, armed_end) had
+    // their bytes posted; Q tiles of sub-tile X were posted q_arms_X times.
+    int armed_end = 0, q_arms0 = 0, q_arms1 = 0;
+    bool gave_up = false;
+#ifdef PATTN_WAIT_TEST
+    const int skip_pos = (!FP8 && p.test_skip == 1 && kv == 0 && blockIdx.x == 0) ? 0 : -1;
+#else
+    constexpr int skip_pos = -1;
+#endif
     Item nxt = load_item(p, item_at(0), n_items, NP, KC);
     for (int k = 0; k * GS < n_items; ++k) {
       const Item it = nxt;
@@ -440,6 +449,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           const Sub& u = X ? subB : subA;
           if (!ok || u.x1 <= u.x0) continue;
           mbar_arrive_expect_tx(&bars->q_full[X], C::TILE);
+          ++(X ? q_arms1 : q_arms0);
 #pragma unroll
           for (int dh = 0; dh < C::DH; ++dh)
             tma_load_3d(sQ + X * C::TILE + dh * C::HALF, &qmap, &bars->q_full[X], dh * 64, u.h,
@@ -447,7 +457,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
       }
       ok = __shfl_sync(FULL, ok, 0);
-      if (!ok) break;
+      if (!ok) {
+        gave_up = true;
+        break;
+      }
       const int* bt = p.block_table + static_cast<int64_t>(it.r) * p.bt_stride;
       // block id of page `lane` of key tile kt (0 when that page is past seq_len)
       auto page_block = [&](int kt) {
@@ -476,15 +489,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
           uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
           const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
+          // (wait-test build: the skipped position posts no bytes and issues
+          // no copy, so the MMA thread's wait for it runs out)
+          const bool skip = jg == skip_pos;
           if (lane == 0) {
             if (jg >= nst && !mbar_wait(empty, ((jg / nst) - 1) & 1, status, abort_flag))
               ok = 0;
-            else
+            else if (!skip)
               mbar_arrive_expect_tx(full, bytes);
           }
           ok = __shfl_sync(FULL, ok, 0);
           if (!ok) break;
-          if (my_pg < n_load)
+          armed_end = jg + 1;
+          if (my_pg < n_load && !skip)
             tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap,
                         full, my_dh * 64, g, my_slot, kv * p.NB + my_blk);
         }
@@ -510,6 +527,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               mbar_arrive_expect_tx(&lands[st], static_cast<unsigned>(n_load * rows_box * D));
           }
           good = __shfl_sync(FULL, good, 0);
+          if (good) armed_end = jt + 1;
           if (good && lane < n_load) {
             const int key0 = key_base + lane * rows_box;
             const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
@@ -546,8 +564,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         jg += n_union;
       }
-      if (!ok) break;
+      if (!ok) {
+        gave_up = true;
+        break;
+      }
       ++n_worked;
+    }
+    // A role gave up on a wait: no copy this warp armed may still be writing
+    // shared memory when the CTA frees its resources and exits.
+    if (gave_up || *abort_flag) {
+      if (lane == 0) {
+        uint64_t* armed = FP8 ? (kv ? bars->v_land : bars->k_land)
+                              : (kv ? bars->v_full : bars->k_full);
+        drain_armed(armed, nst, armed_end, skip_pos, status);
+        if (kv == 0) {
+          if (q_arms0 > 0) mbar_wait(&bars->q_full[0], (q_arms0 - 1) & 1, status, nullptr);
+          if (q_arms1 > 0) mbar_wait(&bars->q_full[1], (q_arms1 - 1) & 1, status, nullptr);
+        }
+      }
+      __syncwarp();
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer

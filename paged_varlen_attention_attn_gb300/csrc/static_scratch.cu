@@ -17,7 +17,6 @@
 // (other streams, other host threads) race on the array and must be
 // serialised by the caller.
 #include <cmath>
-#include <mutex>
 
 #include "../../include/pattn.h"
 #include "common.cuh"
@@ -29,26 +28,16 @@ namespace {
 constexpr size_t kStaticScratchBytes = static_cast<size_t>(PATTN_STATIC_SCRATCH_BYTES);
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-
-// Device address of g_static_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and cached.
+// Device address of g_static_scratch in the current context.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress (which allocates nothing) on every call, with the
+// caller's device current: a context that was reset or replaced (the module
+// loaded again, possibly at another address) never sees a stale pointer.
 cudaError_t static_scratch_address(void** out) {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -138,6 +127,9 @@ extern "C" pattn_status_t pattn_decode_fwd_static(
   p.lse32 = nullptr;
   p.NB = num_blocks;
   p.max_q = 1;
+  // Rows of requests with query_len != 1 are another call's: the kernel leaves
+  // them as they are.
+  p.decode_rows_only = 1;
   p.max_s = max_seq_len;
   p.splits = splits;
   p.hdr = reinterpret_cast<WsHeader*>(ws);

@@ -96,3 +96,17 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same metric, unit and config as the GPU arm's line for this workload
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["config"] == bench.config_dict(W.config_spec(1), 1, 1)
+
+
+def test_oracle_sample_counts_visible_pairs():
+    # the sampled (row, key) count is what the oracle's loops visit: checked
+    # against a direct count on the mixed workload's lengths
+    spec = W.config_spec(1)
+    case = W.make_case(spec, device="cpu")
+    smp = bench.oracle_sample(case, spec, 1)
+    rk = bench.sample_row_keys(spec, smp["qsl"], smp["rows"])
+    assert rk == bench.work_counts(spec)["row_keys"]
+    assert rk == spec.num_heads * (sum(range(1, 9)) + 40)
