@@ -109,6 +109,10 @@ def roofline_seconds(counts, pk):
     return max(f, b)
 
 
+def has_prefill_rows(spec):
+    return any(q > 1 for q in spec.q_lens)
+
+
 def peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -301,6 +305,9 @@ def run_ours(args, spec, world, rank, local_rank):
         raise RuntimeError("device status after warm-up: " + pa.pattn_status_string(st))
     splits = pa.pattn_decode_splits(pa.forward.last_ext, spec.num_heads, spec.num_kv_heads,
                                     spec.block_size, spec.window)
+    # the prefill grid the plan kernel kept for the co-scheduled step (the
+    # workspace header's third word; 0 = every SM)
+    prefill_ctas = int(ws.buf[8:12].view(torch.int32).item()) if has_prefill_rows(spec) else 0
 
     K = args.steps
     t_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -361,7 +368,7 @@ def run_ours(args, spec, world, rank, local_rank):
         e2e = run_e2e(args, case, spec, counts, dev, stream, ca, ws)
 
     return dict(case=case, counts=counts, ms=ms_max, ms_local=ms, ms_min=min(step_ms),
-                ms_median=statistics.median(step_ms),
+                ms_median=statistics.median(step_ms), prefill_ctas=prefill_ctas,
                 wall=wall, phase_ms={k: statistics.mean(v) for k, v in phase_ms.items()},
                 clocks=clk, splits=splits, launches=launches_per_step * K, e2e=e2e)
 
@@ -941,6 +948,7 @@ def attention_line(args, spec, world, rank, local, res):
         "rooflines": rooflines,
         "phase_ms": {k: round(v, 4) for k, v in ph.items()},
         "decode_splits": res["splits"],
+        "prefill_ctas": res["prefill_ctas"],
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }

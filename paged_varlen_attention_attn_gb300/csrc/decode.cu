@@ -39,6 +39,9 @@ namespace {
 // consumer warps per KV head, which take the partition's 16-key units in turn
 // and merge their partial results at the end, plus one producer warp.
 constexpr int UNIT = 16;  // keys per unit
+constexpr int U = 1;      // units a consumer warp takes per softmax step
+// lazy rescale threshold of the online softmax (log2 units): weights stay below 2^8
+constexpr float RESCALE_LOG2 = 8.0f;
 
 // KV heads per CTA: the largest of 4 / 2 / 1 that divides num_kv_heads and
 // keeps one stage (K + V of 16 keys of the group) within 16 KB, so the ring
@@ -57,23 +60,28 @@ struct DecodeCfg {
   static constexpr int KV_UNIT = HG * RAW_UNIT;     // K (or V) of the whole head group
   static constexpr int STAGE = 2 * KV_UNIT;         // K + V of the head group
   // Ring depth: as many stages as fit in ~96 KB (two CTAs per SM), at most 8,
-  // rounded down to a multiple of WPH.  Unit i goes to warp slot i % WPH and
-  // stage i % NST; with NST a multiple of WPH every use of a stage belongs to
-  // one slot, so a warp waiting on a stage's full barrier has itself consumed
-  // the stage's previous phase and is never two phases ahead of it (where a
-  // parity wait would pass at once).
+  // rounded down to a multiple of SLOTS = U x WPH.  Unit i goes to warp slot
+  // (i / U) % WPH and stage i % NST; with NST a multiple of SLOTS every use of
+  // a stage belongs to one slot, so a warp waiting on a stage's full barrier
+  // has itself consumed the stage's previous phase and is never two phases
+  // ahead of it (where a parity wait would pass at once).
+  static constexpr int SLOTS = U * WPH;
   static constexpr int NST_FIT = (96 * 1024) / STAGE;
   static constexpr int NST_CAP = NST_FIT > 8 ? 8 : NST_FIT;
-  static constexpr int NST = (NST_CAP / WPH) * WPH < 2 * WPH ? 2 * WPH : (NST_CAP / WPH) * WPH;
-  static_assert(NST % WPH == 0, "each stage must belong to one warp slot");
+  static constexpr int NST = (NST_CAP / SLOTS) * SLOTS < 2 * SLOTS ? 2 * SLOTS : (NST_CAP / SLOTS) * SLOTS;
+  static_assert(NST % SLOTS == 0, "each stage must belong to one warp slot");
   static constexpr int NW = HG * WPH;               // consumer warps
   // Partial state one warp hands over for the merge: o, m, l per lane.
   static constexpr int MERGE_FLOATS = (D / 16) * NT * 4 + 4 * NT;
   static constexpr int MERGE_BYTES = (WPH - 1) * HG * MERGE_FLOATS * 32 * 4;
   static constexpr int RING_BYTES = NST * STAGE;
   static constexpr int BAR_OFF = RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES;
-  static constexpr int SMEM = BAR_OFF + 2 * NST * 8 + 1024;
-  static constexpr int THREADS = (NW + 1) * 32;
+  // block ids of the next 32 units, one buffer per producer warp
+  static constexpr int ID_OFF = BAR_OFF + 2 * NST * 8 <= BAR_OFF + 256 ? BAR_OFF + 256 : -1;
+  static_assert(ID_OFF > 0, "barriers fit in 256 bytes");
+  static constexpr int SMEM = ID_OFF + 2 * 32 * 4 + 1024;
+  // consumer warps, then two producer warps (K copies, V copies)
+  static constexpr int THREADS = (NW + 2) * 32;
 };
 
 // e4m3 -> f16 widening with the hardware pair conversion: exact (every e4m3
@@ -267,22 +275,28 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   uint64_t* empty = full + NST;                                       // [NST]
   if (threadIdx.x == 0) {
     for (int b = 0; b < NST; ++b) {
-      mbar_init(&full[b], 1);
+      mbar_init(&full[b], 2);  // the K and the V producer each post their bytes
       mbar_init(&empty[b], HG);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == C::NW) {
-    // ------------------------------------------------------------ producer warp
-    // Block ids are read 32 units at a time (one coalesced load); lane 0
-    // issues one tensor copy for K and one for V per unit (16 keys of all HG
-    // heads) as soon as the consumers release the stage.
+  if (warp >= C::NW) {
+    // ------------------------------------------------------------ producer warps
+    // Warp NW copies the K rows of each unit (16 keys of all HG heads), warp
+    // NW + 1 the V rows, each as one tensor copy per unit, as soon as the
+    // consumers release the stage; each posts its own bytes on the stage's
+    // full barrier.  A warp issues copies one after another (a copy holds
+    // its issuing warp for a while), so two warps double the copy rate.
+    // Block ids are read 32 units at a time (one coalesced load) into a
+    // per-warp buffer; lane 0 then issues those units' copies.
+    const int kv = warp - C::NW;
+    int* ids = reinterpret_cast<int*>(smem + C::ID_OFF) + kv * 32;
     if (lane == 0) tma_prefetch_desc(&kvmap);
     const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
-    bool ok = true;
-    int armed_end = 0;  // units [0, armed_end) had their bytes posted
+    int ok = 1;
+    int armed_end = 0;  // units [0, armed_end) had this warp's bytes posted
 #ifdef PATTN_WAIT_TEST
     // wait-test build: this unit posts no bytes and issues no copy, so the
     // consumers' wait for it runs out
@@ -301,39 +315,37 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
           blk = min(max(blk, 0), p.NB - 1);
         }
       }
-      const int nb = min(32, n_units - base);
-      for (int l = 0; l < nb; ++l) {
-        const int b = __shfl_sync(0xffffffffu, blk, l);
-        int good = 1;
-        if (lane == 0) {
+      ids[lane] = blk;
+      __syncwarp();
+      if (lane == 0) {
+        const int nb = min(32, n_units - base);
+        for (int l = 0; l < nb; ++l) {
           const int i = base + l, st = i % NST;
           if (i >= NST && !mbar_wait(&empty[st], ((i / NST) - 1) & 1, status, nullptr)) {
-            good = 0;
-          } else if (i != skip_pos) {
-            armed_end = i + 1;
-            const int key0 = (u_begin + i) * UNIT;
-            const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
-            unsigned char* dk = smem + st * C::STAGE;
-            mbar_arrive_expect_tx(&full[st], C::STAGE);
-            if constexpr (FP8) {
-              tma_load_4d(dk, &kvmap, &full[st], 0, slot, grp * HG, b);
-              tma_load_4d(dk + C::KV_UNIT, &kvmap, &full[st], 0, slot, grp * HG, p.NB + b);
-            } else {
-              tma_load_5d(dk, &kvmap, &full[st], 0, slot, grp * HG, 0, b);
-              tma_load_5d(dk + C::KV_UNIT, &kvmap, &full[st], 0, slot, grp * HG, 0, p.NB + b);
-            }
+            ok = 0;
+            break;
           }
-        }
-        if (!__shfl_sync(0xffffffffu, good, 0)) {
-          ok = false;
-          break;
+          if (i == skip_pos) continue;
+          armed_end = i + 1;
+          const int key0 = (u_begin + i) * UNIT;
+          const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
+          unsigned char* dst = smem + st * C::STAGE + kv * C::KV_UNIT;
+          mbar_arrive_expect_tx(&full[st], C::KV_UNIT);
+          if constexpr (FP8)
+            tma_load_4d(dst, &kvmap, &full[st], 0, slot, grp * HG, kv * p.NB + ids[l]);
+          else
+            tma_load_5d(dst, &kvmap, &full[st], 0, slot, grp * HG, 0, kv * p.NB + ids[l]);
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
     }
     // A wait gave up: no copy armed here may still be writing shared memory
-    // when the CTA exits.  (Otherwise the consumers wait for every copy.)
+    // when the CTA exits.  (Otherwise the consumers wait for every copy.)  The
+    // stage's phase also needs the other producer's bytes; if that warp gave
+    // up first, this wait runs out (bounded) instead.
     if (!ok && lane == 0) drain_armed(full, NST, armed_end, skip_pos, status);
-    return;  // nothing after this needs the producer
+    return;  // nothing after this needs the producers
   }
 
   // ---------------------------------------------------------------- consumer warps
@@ -375,13 +387,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   for (int m = 0; m < D / 16; ++m)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
-  // running max / sum of heads nt*8 + 2*c4 + e (identical across lanes with
-  // the same c4 once reduced)
-  float m_run[NT][2], l_run[NT][2];
+  // reference max of heads nt*8 + 2*c4 + h2 (identical across the lanes of
+  // a column group), and the row sums of the weights, accumulated by MMAs in
+  // the output fragment layout (every row of o_l holds the sums)
+  float m_run[NT][2], l_run[NT][2], o_l[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
+    o_l[nt][0] = o_l[nt][1] = o_l[nt][2] = o_l[nt][3] = 0.f;
   }
 
   const int kmin = kb, kmax = ke;
@@ -393,15 +406,25 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   const int src0 = 8 * c4 + (quad >> 1), src1 = src0 + 4;
   const unsigned half_sel = (quad & 1) ? 0x7632u : 0x5410u;
 
-  for (int i = wslot; i < n_units; i += WPH) {
-    const int st = i % NST;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (i / NST) & 1, status, nullptr))) break;
-    unsigned char* sk = smem + st * C::STAGE;
-    unsigned char* sv = sk + C::KV_UNIT;
-    const int key0 = (u_begin + i) * UNIT;
+  // Each step takes U consecutive units (U x 16 keys): the scores of all of
+  // them, one online-softmax update over their keys (the max and sum
+  // reductions are shared), then P V for each.  Unit i sits in stage i % NST
+  // and belongs to warp slot (i / U) % WPH.
+  for (int i0 = wslot * U; i0 < n_units; i0 += WPH * U) {
+    const int nu = min(U, n_units - i0);
+    bool landed = true;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (u < nu) landed &= mbar_wait(&full[(i0 + u) % NST], ((i0 + u) / NST) & 1, status, nullptr);
+    if (!__all_sync(0xffffffffu, landed)) break;
+    const int key_base = (u_begin + i0) * UNIT;
     // Rows at or past seq_len may hold anything (NaN included): zero this
-    // head's rows.
-    if (key0 + UNIT > s) {
+    // head's rows (only the partition's last unit can have any).
+    if (key_base + nu * UNIT > s) {
+      const int u = nu - 1;
+      unsigned char* sk = smem + ((i0 + u) % NST) * C::STAGE;
+      unsigned char* sv = sk + C::KV_UNIT;
+      const int key0 = key_base + u * UNIT;
       constexpr int CH_ROW = C::RAW_ROW / 16;
       for (int c = lane; c < UNIT * CH_ROW; c += 32) {
         const int j = c / CH_ROW, cc = c % CH_ROW;
@@ -415,151 +438,194 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
       __syncwarp();
     }
 
-    // S^T = K Q^T for the 16 keys of this unit: M = keys, N = heads, in two
-    // independent accumulation chains (even / odd k-steps).
-    float sc[2][NT][4];
+    // S^T = K Q^T for the 16 keys of each unit: M = keys, N = heads, in two
+    // independent accumulation chains per unit (even / odd k-steps).
+    float sc[U][2][NT][4];
 #pragma unroll
-    for (int ch = 0; ch < 2; ++ch)
+    for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sc[ch][nt][0] = sc[ch][nt][1] = sc[ch][nt][2] = sc[ch][nt][3] = 0.f;
-    if constexpr (FP8) {
-      // K fragments straight from the e4m3 bytes: this lane's D/4 bytes of
-      // key rows quad and quad + 8, widened in registers.
-      constexpr int CPL = D / 64;  // 16-byte chunks per lane per row
-      uint4 kr[2][CPL];
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr)
-#pragma unroll
-        for (int q = 0; q < CPL; ++q)
-          kr[hr][q] = *reinterpret_cast<const uint4*>(sk + raw_off<D, FP8, HG>(hh, quad + 8 * hr, c4 * CPL + q));
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint4& ra = kr[0][kk >> 2];
-        const uint4& rb = kr[1][kk >> 2];
-        const unsigned w0 = (kk & 3) == 0 ? ra.x : (kk & 3) == 1 ? ra.y : (kk & 3) == 2 ? ra.z : ra.w;
-        const unsigned w1 = (kk & 3) == 0 ? rb.x : (kk & 3) == 1 ? rb.y : (kk & 3) == 2 ? rb.z : rb.w;
-        const unsigned a0 = e4m3_b02_to_f16x2(w0);   // key quad,     d base, base + 2
-        const unsigned a2 = e4m3_b13_to_f16x2(w0);   // key quad,     d base + 1, base + 3
-        const unsigned a1 = e4m3_b02_to_f16x2(w1);   // key quad + 8
-        const unsigned a3 = e4m3_b13_to_f16x2(w1);
+      for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          mma_16816<true>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
-      }
-    } else {
-      const unsigned sk_a = smem_u32(sk);
+          sc[u][ch][nt][0] = sc[u][ch][nt][1] = sc[u][ch][nt][2] = sc[u][ch][nt][3] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        unsigned a0, a1, a2, a3;
-        ldsm_x4(sk_a + raw_off<D, FP8, HG>(hh, s_row, 2 * kk + s_csel), a0, a1, a2, a3);
+    for (int u = 0; u < U; ++u) {
+      if (u >= nu) break;
+      const unsigned char* sk = smem + ((i0 + u) % NST) * C::STAGE;
+      if constexpr (FP8) {
+        // K fragments straight from the e4m3 bytes: this lane's D/4 bytes of
+        // key rows quad and quad + 8, widened in registers.
+        constexpr int CPL = D / 64;  // 16-byte chunks per lane per row
+        uint4 kr[2][CPL];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_16816<HALF>(sc[kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+          for (int q = 0; q < CPL; ++q)
+            kr[hr][q] = *reinterpret_cast<const uint4*>(sk + raw_off<D, FP8, HG>(hh, quad + 8 * hr, c4 * CPL + q));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint4& ra = kr[0][kk >> 2];
+          const uint4& rb = kr[1][kk >> 2];
+          const unsigned w0 = (kk & 3) == 0 ? ra.x : (kk & 3) == 1 ? ra.y : (kk & 3) == 2 ? ra.z : ra.w;
+          const unsigned w1 = (kk & 3) == 0 ? rb.x : (kk & 3) == 1 ? rb.y : (kk & 3) == 2 ? rb.z : rb.w;
+          const unsigned a0 = e4m3_b02_to_f16x2(w0);   // key quad,     d base, base + 2
+          const unsigned a2 = e4m3_b13_to_f16x2(w0);   // key quad,     d base + 1, base + 3
+          const unsigned a1 = e4m3_b02_to_f16x2(w1);   // key quad + 8
+          const unsigned a3 = e4m3_b13_to_f16x2(w1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816<true>(sc[u][kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+        }
+      } else {
+        const unsigned sk_a = smem_u32(sk);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          unsigned a0, a1, a2, a3;
+          ldsm_x4(sk_a + raw_off<D, FP8, HG>(hh, s_row, 2 * kk + s_csel), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816<HALF>(sc[u][kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+        }
       }
     }
 
-    // Mask (keys quad and quad + 8 of this unit), scale to log2 units, online
-    // softmax per head (a column of S^T: reduce over the 8 lanes of a column group).
-    const int ka = key0 + quad, kb2 = ka + 8;
-    const bool va = ka >= kmin && ka < kmax, vb = kb2 >= kmin && kb2 < kmax;
-    unsigned pk_lo[NT], pk_hi[NT];
-    float alpha[NT][2];
-    bool moved = false;
+    // Mask (keys quad and quad + 8 of each unit) and scale to log2 units.
+    // Online softmax with a lazy reference max per head: the reference moves
+    // only when a score exceeds it by more than 2^RESCALE_LOG2, so the common
+    // step needs no cross-lane reduction and the weights 2^(x - ref) stay
+    // below 2^RESCALE_LOG2.  O and the row sums (accumulated by the same MMAs)
+    // are relative to the same reference, so the final O / l is exact.
+    float x[U][NT][4];
+    bool grow = false;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float x[4];
+    for (int u = 0; u < U; ++u) {
+      const int ka = key_base + u * UNIT + quad, kb2 = ka + 8;
+      const bool va = ka >= kmin && ka < kmax, vb = kb2 >= kmin && kb2 < kmax;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float v = sc[0][nt][e] + sc[1][nt][e];
-        x[e] = ((e < 2) ? va : vb) ? v * sl2 : -INFINITY;
-      }
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float mx = fmaxf(x[h2], x[2 + h2]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[nt][h2], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        alpha[nt][h2] = fast_exp2(m_run[nt][h2] - m_use);
-        moved |= (alpha[nt][h2] != 1.f);
-        m_run[nt][h2] = m_new;
-        const float pa = fast_exp2(x[h2] - m_use), pb = fast_exp2(x[2 + h2] - m_use);
-        x[h2] = pa;
-        x[2 + h2] = pb;
-        float ps = pa + pb;
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l_run[nt][h2] = l_run[nt][h2] * alpha[nt][h2] + ps;
-      }
-      pk_lo[nt] = pack2<FP8 || HALF>(x[0], x[1]);  // key quad,     heads 2*c4, 2*c4+1
-      pk_hi[nt] = pack2<FP8 || HALF>(x[2], x[3]);  // key quad + 8, heads 2*c4, 2*c4+1
-    }
-    if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-      for (int m = 0; m < D / 16; ++m)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          o[m][nt][0] *= alpha[nt][0];
-          o[m][nt][1] *= alpha[nt][1];
-          o[m][nt][2] *= alpha[nt][0];
-          o[m][nt][3] *= alpha[nt][1];
+        for (int e = 0; e < 4; ++e) {
+          const float v = sc[u][0][nt][e] + sc[u][1][nt][e];
+          x[u][nt][e] = ((e < 2) ? va : vb) ? v * sl2 : -INFINITY;
+          grow |= x[u][nt][e] > m_run[nt][e & 1] + RESCALE_LOG2;
         }
     }
-    // P^T as the B operand (16 keys x 8 heads, "col"): this lane needs head
-    // nt*8 + quad at keys 2*c4, 2*c4+1 (b0) and 2*c4+8, 2*c4+9 (b1); they sit
-    // in lanes src0 (even key) and src1 (odd key), half quad & 1.
-    unsigned pb0[NT], pb1[NT];
+    if (__any_sync(0xffffffffu, grow)) {
+      // A head column's reference moves to its exact running max (the same in
+      // the 8 lanes of the column after the reduction) when that max exceeds
+      // it by more than the threshold; O and the sums are rescaled.
+      float alpha[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float mx = fmaxf(x[0][nt][h2], x[0][nt][2 + h2]);
+#pragma unroll
+          for (int u = 1; u < U; ++u) mx = fmaxf(mx, fmaxf(x[u][nt][h2], x[u][nt][2 + h2]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const bool mv = mx > m_run[nt][h2] + RESCALE_LOG2;
+          alpha[nt][h2] = !mv ? 1.f : (m_run[nt][h2] == -INFINITY) ? 0.f : fast_exp2(m_run[nt][h2] - mx);
+          if (mv) m_run[nt][h2] = mx;
+        }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_l[nt][e] *= alpha[nt][e & 1];
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[m][nt][e] *= alpha[nt][e & 1];
+      }
+    }
+    unsigned pk_lo[U][NT], pk_hi[U][NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const unsigned x0 = __shfl_sync(0xffffffffu, pk_lo[nt], src0);
-      const unsigned x1 = __shfl_sync(0xffffffffu, pk_lo[nt], src1);
-      const unsigned y0 = __shfl_sync(0xffffffffu, pk_hi[nt], src0);
-      const unsigned y1 = __shfl_sync(0xffffffffu, pk_hi[nt], src1);
-      pb0[nt] = __byte_perm(x0, x1, half_sel);
-      pb1[nt] = __byte_perm(y0, y1, half_sel);
+      const float r0 = (m_run[nt][0] == -INFINITY) ? 0.f : m_run[nt][0];
+      const float r1 = (m_run[nt][1] == -INFINITY) ? 0.f : m_run[nt][1];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        // key quad / quad + 8, heads 2*c4, 2*c4+1
+        pk_lo[u][nt] = pack2<FP8 || HALF>(fast_exp2(x[u][nt][0] - r0), fast_exp2(x[u][nt][1] - r1));
+        pk_hi[u][nt] = pack2<FP8 || HALF>(fast_exp2(x[u][nt][2] - r0), fast_exp2(x[u][nt][3] - r1));
+      }
     }
 
-    // O^T += V^T P^T: M = d (16 per tile), N = heads, K = the 16 keys.
-    if constexpr (FP8) {
-      // V^T fragments straight from the e4m3 bytes.  The d axis of V (and so
-      // of O) is permuted: tile m, fragment row quad is d = quad*D/8 + 2m and
-      // row quad + 8 is d = quad*D/8 + 2m + 1, so each lane reads D/8
-      // contiguous bytes of each of its key rows 2*c4, 2*c4+1, 2*c4+8, 2*c4+9.
-      unsigned v0[D / 32], v1[D / 32], v2[D / 32], v3[D / 32];
-      load_v_bytes<D, HG>(sv, hh, 2 * c4, quad, v0);
-      load_v_bytes<D, HG>(sv, hh, 2 * c4 + 1, quad, v1);
-      load_v_bytes<D, HG>(sv, hh, 2 * c4 + 8, quad, v2);
-      load_v_bytes<D, HG>(sv, hh, 2 * c4 + 9, quad, v3);
 #pragma unroll
-      for (int m = 0; m < D / 16; ++m) {
-        // bytes d0 and d0 + 1 of two key rows in one word: [r.d0, r.d0+1,
-        // r'.d0, r'.d0+1]; bytes 0 and 2 are the pair at d0, 1 and 3 at d0 + 1
-        const int wi = m >> 1;
-        const unsigned sel = (m & 1) ? 0x7632u : 0x5410u;
-        const unsigned x01 = __byte_perm(v0[wi], v1[wi], sel);
-        const unsigned x23 = __byte_perm(v2[wi], v3[wi], sel);
-        const unsigned a0 = e4m3_b02_to_f16x2(x01);
-        const unsigned a1 = e4m3_b13_to_f16x2(x01);
-        const unsigned a2 = e4m3_b02_to_f16x2(x23);
-        const unsigned a3 = e4m3_b13_to_f16x2(x23);
+    for (int u = 0; u < U; ++u) {
+      if (u >= nu) break;
+      const unsigned char* sv = smem + ((i0 + u) % NST) * C::STAGE + C::KV_UNIT;
+      // P^T as the B operand (16 keys x 8 heads, "col"): this lane needs head
+      // nt*8 + quad at keys 2*c4, 2*c4+1 (b0) and 2*c4+8, 2*c4+9 (b1); they sit
+      // in lanes src0 (even key) and src1 (odd key), half quad & 1.
+      unsigned pb0[NT], pb1[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816<true>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+      for (int nt = 0; nt < NT; ++nt) {
+        const unsigned x0 = __shfl_sync(0xffffffffu, pk_lo[u][nt], src0);
+        const unsigned x1 = __shfl_sync(0xffffffffu, pk_lo[u][nt], src1);
+        const unsigned y0 = __shfl_sync(0xffffffffu, pk_hi[u][nt], src0);
+        const unsigned y1 = __shfl_sync(0xffffffffu, pk_hi[u][nt], src1);
+        pb0[nt] = __byte_perm(x0, x1, half_sel);
+        pb1[nt] = __byte_perm(y0, y1, half_sel);
       }
-    } else {
-      const unsigned sv_a = smem_u32(sv);
+
+      // O^T += V^T P^T: M = d (16 per tile), N = heads, K = the 16 keys.
+      if constexpr (FP8) {
+        // V^T fragments straight from the e4m3 bytes.  The d axis of V (and so
+        // of O) is permuted: tile m, fragment row quad is d = quad*D/8 + 2m and
+        // row quad + 8 is d = quad*D/8 + 2m + 1, so each lane reads D/8
+        // contiguous bytes of each of its key rows 2*c4, 2*c4+1, 2*c4+8, 2*c4+9.
+        unsigned v0[D / 32], v1[D / 32], v2[D / 32], v3[D / 32];
+        load_v_bytes<D, HG>(sv, hh, 2 * c4, quad, v0);
+        load_v_bytes<D, HG>(sv, hh, 2 * c4 + 1, quad, v1);
+        load_v_bytes<D, HG>(sv, hh, 2 * c4 + 8, quad, v2);
+        load_v_bytes<D, HG>(sv, hh, 2 * c4 + 9, quad, v3);
 #pragma unroll
-      for (int m = 0; m < D / 16; ++m) {
-        unsigned a0, a1, a2, a3;
-        ldsm_x4_t(sv_a + raw_off<D, FP8, HG>(hh, v_row, 2 * m + v_csel), a0, a1, a2, a3);
+        for (int m = 0; m < D / 16; ++m) {
+          // bytes d0 and d0 + 1 of two key rows in one word: [r.d0, r.d0+1,
+          // r'.d0, r'.d0+1]; bytes 0 and 2 are the pair at d0, 1 and 3 at d0 + 1
+          const int wi = m >> 1;
+          const unsigned sel = (m & 1) ? 0x7632u : 0x5410u;
+          const unsigned x01 = __byte_perm(v0[wi], v1[wi], sel);
+          const unsigned x23 = __byte_perm(v2[wi], v3[wi], sel);
+          const unsigned a0 = e4m3_b02_to_f16x2(x01);
+          const unsigned a1 = e4m3_b13_to_f16x2(x01);
+          const unsigned a2 = e4m3_b02_to_f16x2(x23);
+          const unsigned a3 = e4m3_b13_to_f16x2(x23);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816<HALF>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+          for (int nt = 0; nt < NT; ++nt) mma_16816<true>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        }
+      } else {
+        const unsigned sv_a = smem_u32(sv);
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+          unsigned a0, a1, a2, a3;
+          ldsm_x4_t(sv_a + raw_off<D, FP8, HG>(hh, v_row, 2 * m + v_csel), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816<HALF>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        }
       }
+      // Row sums l = 1^T P^T by the tensor core: every row of the all-ones A
+      // tile gives each head's sum of this unit's (rounded) weights.
+      constexpr unsigned ONES = (FP8 || HALF) ? 0x3C003C00u : 0x3F803F80u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_16816<FP8 || HALF>(o_l[nt], ONES, ONES, ONES, ONES, pb0[nt], pb1[nt]);
     }
-    // Release the stage once every lane of every consumer warp has read it.
+    // Release the stages once every lane of every consumer warp has read them.
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if (lane == 0) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (u < nu) mbar_arrive(&empty[(i0 + u) % NST]);
+    }
+  }
+
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    l_run[nt][0] = o_l[nt][0];
+    l_run[nt][1] = o_l[nt][1];
   }
 
   // ---------------------------------------------------------------- merge

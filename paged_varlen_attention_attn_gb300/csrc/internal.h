@@ -16,7 +16,10 @@ constexpr int BLOCK_N = 128;
 struct WsHeader {
   unsigned status;        // PATTN_DEV_* bits
   int num_prefill_tiles;  // written by the plan kernel
-  int pad[62];
+  int prefill_ctas;       // written by the plan kernel: CTAs of the prefill grid
+                          // that run (0: all); the decode grid takes the SMs of
+                          // the others while prefill runs
+  int pad[61];
 };
 
 struct Problem {
@@ -70,6 +73,15 @@ struct Problem {
   int pdl_trigger;  // the prefill kernel lets its dependent start once all of
                     // its CTAs are running (decode CTAs then take the SMs that
                     // finished prefill CTAs leave)
+  // Co-scheduling of a mixed batch (host-side choice and cost model): the
+  // plan kernel leaves the prefill kernel only as many CTAs (one per SM) as
+  // balance the two kernels, and the decode kernel, a programmatic dependent,
+  // runs on the other SMs at the same time.
+  int co_schedule;
+  int num_sms;
+  float pf_us_per_tile;    // prefill: us per key tile of one item, per SM
+  float dec_bytes_per_us;  // decode: K/V bytes per us one SM streams (two CTAs)
+  float hbm_bytes_per_us;  // decode: HBM bytes per us available beside prefill
 #ifdef PATTN_WAIT_TEST
   // Wait-test build only: 1 = CTA 0 of the prefill kernel posts no bytes and
   // issues no copy for the first K tile it streams; 2 = CTA 0 of the decode

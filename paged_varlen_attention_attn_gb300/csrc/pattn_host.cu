@@ -155,6 +155,21 @@ pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* bl
   return PATTN_OK;
 }
 
+// Cost model of the co-scheduled mixed batch (measured on GB300): a prefill
+// key tile of one item (two 128-row sub-tiles, 128 keys) takes about
+// 2.1 us per SM at head size 128 (about 1.3 us at 64; e4m3 tiles about 1.3x
+// longer, for the widening); one SM running two decode CTAs streams about
+// 140 GB/s of 16-bit K/V (e4m3 about 100 GB/s, bound by the widening); decode
+// gets about 85 % of HBM beside the prefill.  The estimate only balances the
+// two kernels; the result does not depend on it.
+void set_cost_model(Problem& p) {
+  p.num_sms = sm_count();
+  const bool fp8 = p.kv_dtype == PATTN_KV_FP8_E4M3;
+  p.pf_us_per_tile = (p.D == 128 ? 2.1f : 1.3f) * (fp8 ? 1.3f : 1.f);
+  p.dec_bytes_per_us = fp8 ? 100000.f : 140000.f;
+  p.hbm_bytes_per_us = 0.85f * 6800000.f;
+}
+
 // The fields of a Problem every pass shares.
 void base_problem(Problem& p, const void* q, const void* kv_cache, void* out, float scale,
                   int num_heads, int num_kv_heads, int head_size, int block_size, int kv_dtype,
@@ -531,6 +546,12 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   // Prefill rows run on the tensor-core kernel (an e4m3 cache widened to f16
   // in its shared memory).
   const bool tc_prefill = ext->max_query_len > 1;
+  // A batch with prefill rows co-schedules the two kernels (the plan kernel
+  // sizes the prefill grid from the actual work; with no decode rows it keeps
+  // every SM).  With per-phase events between the kernels they run one after
+  // the other on every SM instead.
+  p.co_schedule = (ext->timing_events == nullptr && tc_prefill) ? 1 : 0;
+  set_cost_model(p);
   mark(0);
   if (tc_prefill) {
     // The plan kernel clears the header and the counters and builds the
@@ -552,6 +573,7 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   p.pdl_launch = timed ? 0 : 1;
   p.pdl_wait = tc_prefill ? 0 : 1;
   p.pdl_trigger = (!timed && tc_prefill) ? 1 : 0;
+
   mark(1);
   mark(2);
 

@@ -9,6 +9,7 @@
 // the status word, so later kernels of the same call report into a clean one,
 // and the decode kernel's partition counters, and orders the decode requests
 // by their visible length, longest first, for the decode grid.
+#include "../../include/pattn.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -95,24 +96,60 @@ __device__ int scan_descending(int* hist, int* warp_sums) {
 // Writes p.decode_order: every request, by decreasing decode cost (a counting
 // sort; the order within one cost is whatever the atomics give).  A thread's
 // first request keeps its cost in a register between the two passes, so the
-// metadata is read once (the decode kernel waits for this).
-__device__ void order_decodes(const Problem& p, int* hist, int* warp_sums) {
+// metadata is read once (the decode kernel waits for this).  Adds the visible
+// KV blocks of every decode row to *blocks.
+__device__ void order_decodes(const Problem& p, int* hist, int* warp_sums,
+                              unsigned long long* blocks) {
   const int tid = threadIdx.x;
   const int cost0 = (tid < p.B) ? decode_cost(p, tid) : 0;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
-  for (int r = tid; r < p.B; r += PLAN_THREADS)
-    atomicAdd(&hist[r == tid ? cost0 : decode_cost(p, r)], 1);
+  for (int r = tid; r < p.B; r += PLAN_THREADS) {
+    const int c = r == tid ? cost0 : decode_cost(p, r);
+    atomicAdd(&hist[c], 1);
+    atomicAdd(blocks, static_cast<unsigned long long>(c));
+  }
   __syncthreads();
   scan_descending(hist, warp_sums);
   for (int r = tid; r < p.B; r += PLAN_THREADS)
     p.decode_order[atomicAdd(&hist[r == tid ? cost0 : decode_cost(p, r)], 1)] = r;
 }
 
+// Estimated time (us) of a mixed batch whose prefill keeps `gs` SMs and
+// whose decode runs on the other `m` = num_sms - gs at the same time, then on
+// every SM once prefill is done.  Prefill: the longest-processing-time list is
+// walked in rounds of gs items, a round lasting about its first (largest)
+// item, and never less than the total work over gs SMs.  Decode: m SMs
+// stream at dec_bytes_per_us each, capped by the HBM bandwidth beside prefill.
+__device__ float co_schedule_estimate(const Problem& p, int gs, int n_items, int np,
+                                      unsigned long long work_items, double dec_bytes) {
+  float rounds = 0.f;
+  for (int x = 0; x < n_items; x += gs) {
+    const int2 tl = p.tiles[x / np];
+    const int t0 = p.qsl[tl.x];
+    rounds += static_cast<float>(tile_cost(p, p.qsl[tl.x + 1] - t0, p.seq_lens[tl.x], tl.y));
+  }
+  const float t_pre = p.pf_us_per_tile * fmaxf(rounds, static_cast<float>(work_items) / gs);
+  const int m = p.num_sms - gs;
+  const float full_rate = fminf(p.num_sms * p.dec_bytes_per_us, p.hbm_bytes_per_us);
+  if (m <= 0) return t_pre + static_cast<float>(dec_bytes / full_rate);
+  const float rate = fminf(m * p.dec_bytes_per_us, p.hbm_bytes_per_us);
+  const float t_dec = static_cast<float>(dec_bytes / rate);
+  if (t_dec <= t_pre) return t_pre;
+  return t_pre + static_cast<float>((dec_bytes - static_cast<double>(rate) * t_pre) / full_rate);
+}
+
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __shared__ int hist[NBUCKET];
   __shared__ int warp_sums[PLAN_THREADS / 32 + 1];
+  __shared__ unsigned long long s_tile_work, s_dec_blocks;
+  __shared__ float s_best[PLAN_THREADS / 32];
+  __shared__ int s_best_gs[PLAN_THREADS / 32];
   const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_tile_work = 0ull;
+    s_dec_blocks = 0ull;
+  }
   if (tid == 0 && p.clear_status) p.hdr->status = 0u;
   for (int i = tid; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
@@ -141,7 +178,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
     }
     if (q_len <= 1) continue;
     const int nt = (q_len + p.rows_per_item - 1) / p.rows_per_item;
-    for (int qt = 0; qt < nt; ++qt) atomicAdd(&hist[tile_cost(p, q_len, s, qt)], 1);
+    unsigned long long work = 0ull;
+    for (int qt = 0; qt < nt; ++qt) {
+      const int c = tile_cost(p, q_len, s, qt);
+      atomicAdd(&hist[c], 1);
+      work += static_cast<unsigned long long>(c);
+    }
+    atomicAdd(&s_tile_work, work);
   }
   __syncthreads();
 
@@ -165,7 +208,55 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __syncthreads();
 
   // Pass 3: the decode grid's request order.
-  if (p.decode_order) order_decodes(p, hist, warp_sums);
+  if (p.decode_order) order_decodes(p, hist, warp_sums, &s_dec_blocks);
+  __syncthreads();
+
+  // Pass 4 (mixed batches): how many SMs the prefill kernel keeps.  Each
+  // thread estimates a few prefill grid sizes; the fastest estimate wins (the
+  // largest grid on ties).
+  if (!p.co_schedule) {
+    if (tid == 0) p.hdr->prefill_ctas = 0;
+    return;
+  }
+  const int np = ((p.G % 2) == 0 ? p.H / 2 : p.H) * p.kv_chunks;
+  const int n_items = min(p.hdr->num_prefill_tiles, p.max_tiles) * np;
+  const double dec_bytes = static_cast<double>(s_dec_blocks) * p.bs * p.Hkv * 2.0 * p.D *
+                           (p.kv_dtype == PATTN_KV_FP8_E4M3 ? 1.0 : 2.0);
+  const unsigned long long work_items = s_tile_work * static_cast<unsigned long long>(np);
+  float best = INFINITY;
+  int best_gs = p.num_sms;
+  if (n_items > 0 && dec_bytes > 0.0) {
+    for (int gs = p.num_sms - tid; gs >= max(1, p.num_sms / 2); gs -= PLAN_THREADS) {
+      const float e = co_schedule_estimate(p, gs, n_items, np, work_items, dec_bytes);
+      if (e < best || (e == best && gs > best_gs)) {
+        best = e;
+        best_gs = gs;
+      }
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int og = __shfl_xor_sync(0xffffffffu, best_gs, o);
+    if (ob < best || (ob == best && og > best_gs)) {
+      best = ob;
+      best_gs = og;
+    }
+  }
+  if ((tid & 31) == 0) {
+    s_best[tid >> 5] = best;
+    s_best_gs[tid >> 5] = best_gs;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float b = s_best[0];
+    int g = s_best_gs[0];
+    for (int w = 1; w < PLAN_THREADS / 32; ++w)
+      if (s_best[w] < b || (s_best[w] == b && s_best_gs[w] > g)) {
+        b = s_best[w];
+        g = s_best_gs[w];
+      }
+    p.hdr->prefill_ctas = (b == INFINITY) ? 0 : g;
+  }
 }
 
 // Decode-only calls: clear the status word and the partition counters and
@@ -175,13 +266,16 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
 __global__ void __launch_bounds__(PLAN_THREADS) decode_prep_kernel(const Problem p) {
   __shared__ int hist[NBUCKET];
   __shared__ int warp_sums[PLAN_THREADS / 32 + 1];
+  __shared__ unsigned long long s_dec_blocks;
   grid_dep_trigger();
   if (threadIdx.x == 0) {
     p.hdr->status = 0u;
     p.hdr->num_prefill_tiles = 0;
+    p.hdr->prefill_ctas = 0;
+    s_dec_blocks = 0ull;
   }
   for (int i = threadIdx.x; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
-  order_decodes(p, hist, warp_sums);
+  order_decodes(p, hist, warp_sums, &s_dec_blocks);
 }
 
 }  // namespace

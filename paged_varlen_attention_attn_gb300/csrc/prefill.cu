@@ -347,10 +347,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int NP = head_pairs ? p.H / 2 : p.H;
   const int KC = p.kv_chunks;
   const int n_items = p.hdr->num_prefill_tiles * NP * KC;
-  const int GS = gridDim.x;
+  // In a co-scheduled mixed batch the plan kernel keeps only prefill_ctas of
+  // the grid's CTAs (one per SM); the others leave at once, and the decode
+  // kernel runs on their SMs.
+  const int keep = p.hdr->prefill_ctas;
+  const int GS = (keep > 0 && keep < static_cast<int>(gridDim.x)) ? keep : static_cast<int>(gridDim.x);
   // The decode kernel of the same call reads nothing this kernel writes.
   if (p.pdl_trigger && threadIdx.x == 0) grid_dep_trigger();
-  if (static_cast<int>(blockIdx.x) >= n_items) return;
+  if (static_cast<int>(blockIdx.x) >= n_items || static_cast<int>(blockIdx.x) >= GS) return;
   auto item_at = [&](int k) {
     return k * GS + ((k & 1) ? GS - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
   };
