@@ -73,6 +73,11 @@ constexpr int SPLIT_REGS_TOTAL = 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS;
 constexpr int PF_KST = 3;
 constexpr int PF_VST = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+// 2^RESCALE_THRESHOLD: if any of a row's weights against an unmoved
+// reference exceeds it, so does their sum; a sum above this sends the tile
+// down the path that takes the row max (a larger sum with every weight in
+// range only costs that path).
+constexpr float FAST_SUM_LIMIT = 256.0f;
 constexpr unsigned FULL = 0xffffffffu;
 
 template <int D>
@@ -825,65 +830,86 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           for (int q = 0; q < BLOCK_N; ++q)
             sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
         }
-        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+        // The weights 2^(x - ref) of the row against reference ref, packed
+        // and stored to TMEM as P (the upper half of this sub-tile's S
+        // columns); returns their sum.
+        auto exp_store = [&](float ref) -> float {
+          const float neg_m = -ref;
+          float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
-        for (int q = 4; q < BLOCK_N - 4; q += 8) {
-          m4[0] = max3(m4[0], sv[q + 0], sv[q + 1]);
-          m4[1] = max3(m4[1], sv[q + 2], sv[q + 3]);
-          m4[2] = max3(m4[2], sv[q + 4], sv[q + 5]);
-          m4[3] = max3(m4[3], sv[q + 6], sv[q + 7]);
-        }
-        m4[0] = max3(m4[0], sv[BLOCK_N - 4], sv[BLOCK_N - 3]);
-        m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
-        const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
-        const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-
-        // Lazy rescale: move the reference max only when it grows by > 2^8.
-        const bool grow = mx_s > m_run + RESCALE_THRESHOLD;
-        const bool need_o = grow && (m_run != -INFINITY) && (c > 0);
-        float alpha = 1.f;
-        if (grow) {
-          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mx_s);
-          l_run *= alpha;
-          m_run = mx_s;
-        }
-        if (__any_sync(FULL, need_o)) {
-          // P V of the previous tile is complete: the commit that announced
-          // these scores was issued after it.
-          const float a = need_o ? alpha : 1.f;
+          for (int q = 0; q < BLOCK_N; q += 32) {
+            unsigned pk[16];
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            float ov[32];
-            tc_ld32(o_t + q * 32, ov);
-            tc_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] *= a;
-            tc_st32(o_t + q * 32, ov);
+            for (int e = 0; e < 32; e += 4) {
+              float a0 = sv[q + e], a1 = sv[q + e + 1], a2 = sv[q + e + 2], a3 = sv[q + e + 3];
+              ffma2(a0, a1, sl2, neg_m);
+              ffma2(a2, a3, sl2, neg_m);
+              a0 = fast_exp2(a0);
+              a1 = fast_exp2(a1);
+              a2 = fast_exp2(a2);
+              a3 = fast_exp2(a3);
+              fadd2(ps0, ps1, a0, a1);
+              fadd2(ps2, ps3, a2, a3);
+              pk[e / 2] = pack2<MMA_F16>(a0, a1);
+              pk[e / 2 + 1] = pack2<MMA_F16>(a2, a3);
+            }
+            tc_st16u(s_t + 64 + q / 2, pk);
           }
+          return (ps0 + ps1) + (ps2 + ps3);
+        };
+        // Common case: the reference stays.  The weights against it are
+        // computed and stored; if any exceeded 2^RESCALE_THRESHOLD, their sum
+        // did too, and the tile is redone below against a moved reference.
+        // So the row max is taken only for a row's first tile and for the
+        // rare tile whose scores outgrow the reference.
+        bool slow = (m_run == -INFINITY);
+        float ps = 0.f;
+        if (!__any_sync(FULL, slow)) {
+          ps = exp_store(m_run);
+          slow = !(ps <= FAST_SUM_LIMIT);
         }
-
-        const float neg_m = -((m_run == -INFINITY) ? 0.f : m_run);
-        float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+        if (__any_sync(FULL, slow)) {
+          float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int q = 0; q < BLOCK_N; q += 32) {
-          unsigned pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float a0 = sv[q + e], a1 = sv[q + e + 1], a2 = sv[q + e + 2], a3 = sv[q + e + 3];
-            ffma2(a0, a1, sl2, neg_m);
-            ffma2(a2, a3, sl2, neg_m);
-            a0 = fast_exp2(a0);
-            a1 = fast_exp2(a1);
-            a2 = fast_exp2(a2);
-            a3 = fast_exp2(a3);
-            fadd2(ps0, ps1, a0, a1);
-            fadd2(ps2, ps3, a2, a3);
-            pk[e / 2] = pack2<MMA_F16>(a0, a1);
-            pk[e / 2 + 1] = pack2<MMA_F16>(a2, a3);
+          for (int q = 4; q < BLOCK_N - 4; q += 8) {
+            m4[0] = max3(m4[0], sv[q + 0], sv[q + 1]);
+            m4[1] = max3(m4[1], sv[q + 2], sv[q + 3]);
+            m4[2] = max3(m4[2], sv[q + 4], sv[q + 5]);
+            m4[3] = max3(m4[3], sv[q + 6], sv[q + 7]);
           }
-          tc_st16u(s_t + 64 + q / 2, pk);
+          m4[0] = max3(m4[0], sv[BLOCK_N - 4], sv[BLOCK_N - 3]);
+          m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
+          const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+
+          // Lazy rescale: move the reference max only when it grows by > 2^8,
+          // or, for a row whose own weights summed above the limit, whenever
+          // it grows (else that row would take this path on every tile).
+          const bool grow = mx_s > m_run + (slow ? 0.f : RESCALE_THRESHOLD);
+          const bool need_o = grow && (m_run != -INFINITY) && (c > 0);
+          float alpha = 1.f;
+          if (grow) {
+            alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mx_s);
+            l_run *= alpha;
+            m_run = mx_s;
+          }
+          if (__any_sync(FULL, need_o)) {
+            // P V of the previous tile is complete: the commit that announced
+            // these scores was issued after it.
+            const float a = need_o ? alpha : 1.f;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+              float ov[32];
+              tc_ld32(o_t + q * 32, ov);
+              tc_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] *= a;
+              tc_st32(o_t + q * 32, ov);
+            }
+          }
+          ps = exp_store((m_run == -INFINITY) ? 0.f : m_run);
         }
-        l_run += (ps0 + ps1) + (ps2 + ps3);
+        l_run += ps;
         tc_wait_st();
 
         // Zero V rows at or past seq_len before P V reads them (done by the
