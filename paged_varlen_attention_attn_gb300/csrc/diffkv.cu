@@ -9,15 +9,10 @@
 // pattn_varlen_fwd's (causal or not, sliding window, GQA, sinks); out is
 // [T][H][dv].
 //
-// The kernel also has an instance for the standard layout
-// ([2][num_blocks][block_size][num_kv_heads][d]: K and V rows fetched from
-// their two planes into one staged row) over an e4m3 cache, which widens the
-// codes with the hardware pair conversion and applies the per-tensor scales.
-// It served the prefill rows of e4m3 calls before the tensor-core prefill
-// kernel widened e4m3 tiles itself; the library no longer calls it.
-//
-// A generic SIMT kernel for any dk, dv that are multiples of 32 up to 256,
-// not a tensor-core one.  One CTA per (query token, KV head): its four warps
+// This generic SIMT kernel serves the rows with query_len > 1 (the decode
+// rows run on the tensor-core kernel of diffkv_decode.cu when dk and dv are
+// multiples of 64; otherwise this kernel serves them too), for any dk, dv that
+// are multiples of 32 up to 256.  One CTA per (query token, KV head): its four warps
 // share the KV head's G query heads (warp w takes heads w, w + 4, ...).  Key
 // tiles of 32 rows (K and V together) are copied into shared memory with
 // 16-byte cp.async (rows past the visible range zero-filled), double
@@ -95,17 +90,6 @@ __device__ __forceinline__ float half_bits_to_float(unsigned short b) {
     return __bfloat162float(__ushort_as_bfloat16(b));
 }
 
-// Two e4m3 codes (the low 16 bits of v) as floats, exactly (the pair
-// conversion widens to f16; every e4m3 value is an f16 value).
-__device__ __forceinline__ float2 e4m3x2_to_float2(unsigned v) {
-  unsigned r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
-  return __half22float2(*reinterpret_cast<const __half2*>(&r));
-}
-
-// Cache element types of the generic kernel.
-constexpr int GK_BF16 = 0, GK_E4M3 = 1, GK_F16 = 2;
-
 // (d0, d1) += (a0, a1) * (b0, b1) on the paired fp32 pipe
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
@@ -132,26 +116,15 @@ __device__ __forceinline__ void dot8(const float4 qa, const float4 qb, const uin
   fma2(d0, d1, qb.z, qb.w, f.x, f.y);
 }
 
-// dot(q[0..3], 4 e4m3 codes in w) into (d0, d1)
-__device__ __forceinline__ void dot4_e4m3(const float4 q, unsigned w, float& d0, float& d1) {
-  float2 f = e4m3x2_to_float2(w);
-  fma2(d0, d1, q.x, q.y, f.x, f.y);
-  f = e4m3x2_to_float2(w >> 16);
-  fma2(d0, d1, q.z, q.w, f.x, f.y);
-}
-
-// KV: GK_BF16, GK_E4M3 (with bf16 q and out) or GK_F16 (f16 q and out).
+// HALF: q, the cache and out are f16 (else bf16).
 // NC: dv / 32, the output columns per lane.  With NC even a lane owns pairs of
-// adjacent columns (2 lane + 64 c, + 1), read as one 32-bit (16-bit for e4m3)
-// word per key and stored together; with NC odd, columns lane + 32 c.
-// split: the standard layout (K and V planes); else the DiffKV layout.
+// adjacent columns (2 lane + 64 c, + 1), read as one 32-bit word per key and
+// stored together; with NC odd, columns lane + 32 c.
 // skip_decode: rows of requests with query_len 1 are left to the decode kernel.
-template <int KV, int NC>
+template <bool HALF, int NC>
 __global__ void __launch_bounds__(DKV_THREADS)
-    diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2, float out_scale,
-                  int split, int skip_decode) {
-  constexpr bool HALF = KV == GK_F16;       // q, out (and a 16-bit cache) are f16
-  constexpr int ES = (KV == GK_E4M3) ? 1 : 2;
+    diffkv_kernel(const __grid_constant__ Problem p, int dk, int dv, float sl2, int skip_decode) {
+  constexpr int ES = 2;
   extern __shared__ __align__(16) unsigned char smem[];
   const int kbytes = dk * ES;
   const int rbytes = (dk + dv) * ES;  // a staged row: K then V
@@ -187,12 +160,8 @@ __global__ void __launch_bounds__(DKV_THREADS)
   const int lo = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
   const int* bt = p.block_table + static_cast<int64_t>(r) * p.bt_stride;
   const unsigned char* cache = static_cast<const unsigned char*>(p.kv);
-  // Source bytes of a row (the DiffKV row, or the K row of the standard
-  // layout) and the extra offset of the V pieces (the V plane lies
-  // NB * bs * Hkv rows after the K plane; a DiffKV row continues in place).
-  const int64_t src_row = split ? kbytes : rbytes;
-  const int64_t v_extra =
-      split ? static_cast<int64_t>(p.NB) * p.bs * p.Hkv * kbytes - kbytes : 0;
+  // bytes of a cache row (K then V)
+  const int64_t src_row = rbytes;
 
   // Copy keys k0 .. k0 + 31 into buffer b: warp w copies rows w, w + 4, ...
   // The 32 keys' row offsets come from one coalesced block-table load (lane
@@ -215,7 +184,7 @@ __global__ void __launch_bounds__(DKV_THREADS)
       const bool ok = off >= 0;
       const unsigned char* src = cache + (ok ? off : 0);
       for (int c = lane; c < cpr; c += 32)
-        cp_async16(dst + kk * rs + c * 16, src + (ok ? c * 16 + (c >= ck ? v_extra : 0) : 0), ok);
+        cp_async16(dst + kk * rs + c * 16, src + (ok ? c * 16 : 0), ok);
     }
     cp_async_commit();
   };
@@ -258,15 +227,7 @@ __global__ void __launch_bounds__(DKV_THREADS)
       float dot0 = 0.f, dot1 = 0.f;
 #pragma unroll 4
       for (int c = 0; c < ck; ++c) {
-        const uint4 w = krow[c];
-        if constexpr (KV == GK_E4M3) {  // 16 codes
-          dot4_e4m3(q4[4 * c], w.x, dot0, dot1);
-          dot4_e4m3(q4[4 * c + 1], w.y, dot0, dot1);
-          dot4_e4m3(q4[4 * c + 2], w.z, dot0, dot1);
-          dot4_e4m3(q4[4 * c + 3], w.w, dot0, dot1);
-        } else {                         // 8 16-bit values
-          dot8<HALF>(q4[2 * c], q4[2 * c + 1], w, dot0, dot1);
-        }
+        dot8<HALF>(q4[2 * c], q4[2 * c + 1], krow[c], dot0, dot1);  // 8 16-bit values
       }
       const float s2 = key_ok ? (dot0 + dot1) * sl2 : -INFINITY;
       const float m_new = fmaxf(m_run[jh], warp_max(s2));
@@ -285,21 +246,14 @@ __global__ void __launch_bounds__(DKV_THREADS)
         if constexpr (PAIRS) {
 #pragma unroll
           for (int c2 = 0; c2 < NC / 2; ++c2) {
-            float2 v;
-            if constexpr (KV == GK_E4M3)
-              v = e4m3x2_to_float2(reinterpret_cast<const unsigned short*>(vbase)[lane + 32 * c2]);
-            else
-              v = unpack2<HALF>(reinterpret_cast<const unsigned*>(vbase)[lane + 32 * c2]);
+            const float2 v = unpack2<HALF>(reinterpret_cast<const unsigned*>(vbase)[lane + 32 * c2]);
             fma2(o[jh][2 * c2], o[jh][2 * c2 + 1], pb, pb, v.x, v.y);
           }
         } else {
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
-            float v;
-            if constexpr (KV == GK_E4M3)
-              v = e4m3x2_to_float2(vbase[lane + 32 * c]).x;
-            else
-              v = half_bits_to_float<HALF>(reinterpret_cast<const unsigned short*>(vbase)[lane + 32 * c]);
+            const float v =
+                half_bits_to_float<HALF>(reinterpret_cast<const unsigned short*>(vbase)[lane + 32 * c]);
             o[jh][c] = fmaf(pb, v, o[jh][c]);
           }
         }
@@ -314,7 +268,7 @@ __global__ void __launch_bounds__(DKV_THREADS)
     const int hh = warp + 4 * jh;
     if (hh >= G) continue;
     const float l_tot = l_run[jh] + sink_term(p.sinks, g * G + hh, m_run[jh]);
-    const float inv = (l_tot > 0.f) ? out_scale / l_tot : 0.f;
+    const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
     const int64_t ob = orow + static_cast<int64_t>(hh) * dv;
     if constexpr (PAIRS) {
 #pragma unroll
@@ -330,51 +284,55 @@ __global__ void __launch_bounds__(DKV_THREADS)
 
 }  // namespace
 
-size_t generic_smem_bytes(int G, int dk, int dv, int es) {
-  return 2 * static_cast<size_t>(DKV_KEYS) * ((dk + dv) * es + 16) +
+size_t generic_smem_bytes(int G, int dk, int dv) {
+  return 2 * static_cast<size_t>(DKV_KEYS) * ((dk + dv) * 2 + 16) +
          static_cast<size_t>(G) * dk * sizeof(float);
 }
 
-template <int KV, int NC>
-cudaError_t launch_generic_t(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
-  const size_t smem = generic_smem_bytes(p.G, dk, dv, KV == GK_E4M3 ? 1 : 2);
-  const float sl2 = fmaxf(p.scale * LOG2E * (KV == GK_E4M3 ? p.k_scale : 1.f), 1e-30f);
-  const float out_scale = (KV == GK_E4M3) ? p.v_scale : 1.f;
+template <bool HALF, int NC>
+cudaError_t launch_generic_t(const Problem& p, int dk, int dv, bool skip_decode) {
+  const size_t smem = generic_smem_bytes(p.G, dk, dv);
+  const float sl2 = fmaxf(p.scale * LOG2E, 1e-30f);
   const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>(p.Hkv));
-  auto kern = diffkv_kernel<KV, NC>;
+  auto kern = diffkv_kernel<HALF, NC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2, out_scale, split ? 1 : 0,
-                                              skip_decode ? 1 : 0);
+  kern<<<grid, DKV_THREADS, smem, p.stream>>>(p, dk, dv, sl2, skip_decode ? 1 : 0);
   return cudaGetLastError();
 }
 
-template <int KV>
-cudaError_t launch_generic_kv(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
+template <bool HALF>
+cudaError_t launch_generic_h(const Problem& p, int dk, int dv, bool skip_decode) {
   switch (dv / 32) {
-    case 1: return launch_generic_t<KV, 1>(p, dk, dv, split, skip_decode);
-    case 2: return launch_generic_t<KV, 2>(p, dk, dv, split, skip_decode);
-    case 3: return launch_generic_t<KV, 3>(p, dk, dv, split, skip_decode);
-    case 4: return launch_generic_t<KV, 4>(p, dk, dv, split, skip_decode);
-    case 5: return launch_generic_t<KV, 5>(p, dk, dv, split, skip_decode);
-    case 6: return launch_generic_t<KV, 6>(p, dk, dv, split, skip_decode);
-    case 7: return launch_generic_t<KV, 7>(p, dk, dv, split, skip_decode);
-    case 8: return launch_generic_t<KV, 8>(p, dk, dv, split, skip_decode);
+    case 1: return launch_generic_t<HALF, 1>(p, dk, dv, skip_decode);
+    case 2: return launch_generic_t<HALF, 2>(p, dk, dv, skip_decode);
+    case 3: return launch_generic_t<HALF, 3>(p, dk, dv, skip_decode);
+    case 4: return launch_generic_t<HALF, 4>(p, dk, dv, skip_decode);
+    case 5: return launch_generic_t<HALF, 5>(p, dk, dv, skip_decode);
+    case 6: return launch_generic_t<HALF, 6>(p, dk, dv, skip_decode);
+    case 7: return launch_generic_t<HALF, 7>(p, dk, dv, skip_decode);
+    case 8: return launch_generic_t<HALF, 8>(p, dk, dv, skip_decode);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_generic(const Problem& p, int dk, int dv, bool split, bool skip_decode) {
+cudaError_t launch_generic(const Problem& p, int dk, int dv, bool skip_decode) {
   if (p.T == 0 || p.B == 0) return cudaSuccess;
-  if (p.kv_dtype == PATTN_KV_F16) return launch_generic_kv<GK_F16>(p, dk, dv, split, skip_decode);
-  if (p.kv_dtype == PATTN_KV_FP8_E4M3)
-    return launch_generic_kv<GK_E4M3>(p, dk, dv, split, skip_decode);
-  return launch_generic_kv<GK_BF16>(p, dk, dv, split, skip_decode);
+  return p.kv_dtype == PATTN_KV_F16 ? launch_generic_h<true>(p, dk, dv, skip_decode)
+                                    : launch_generic_h<false>(p, dk, dv, skip_decode);
 }
 
+// Rows with query_len > 1 on the generic kernel (when the batch may have
+// them), then the decode rows on the tensor-core kernel; head sizes that are
+// not multiples of 64 run every row on the generic kernel.
 cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {
-  return launch_generic(p, dk, dv, false, false);
+  if (!diffkv_decode_supported(dk, dv)) return launch_generic(p, dk, dv, false);
+  if (p.max_q > 1) {
+    const cudaError_t e = launch_generic(p, dk, dv, true);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_diffkv_decode(p, dk, dv);
 }
 
 }  // namespace pattn

@@ -111,11 +111,18 @@ WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int sp
 // Attention over a DiffKV cache ([NB][bs][Hkv][dk + dv], K then V per row):
 // p.D is dk; out is [T][H][dv].
 cudaError_t launch_diffkv(const Problem& p, int dk, int dv);
-// The generic (SIMT) kernel on any cache type: split selects the standard
-// layout (K and V planes, dk == dv == p.D); skip_decode leaves the rows of
-// requests with query_len 1 to the decode kernel.  Only launch_diffkv calls
-// it (DiffKV layout, no split).
-cudaError_t launch_generic(const Problem& p, int dk, int dv, bool split, bool skip_decode);
+// The generic (SIMT) kernel over a DiffKV cache; skip_decode leaves the rows
+// of requests with query_len 1 to the tensor-core decode kernel.
+cudaError_t launch_generic(const Problem& p, int dk, int dv, bool skip_decode);
+// The decode rows of a DiffKV batch on the tensor cores (mma.sync), for head
+// sizes that diffkv_decode_supported accepts (multiples of 64).
+bool diffkv_decode_supported(int dk, int dv);
+cudaError_t launch_diffkv_decode(const Problem& p, int dk, int dv);
+// TMA tensor map over a DiffKV cache [NB][bs][Hkv][dk + dv] (16-bit) viewed as
+// [NB * bs rows][(dk + dv) / 64 chunks of 64 elements][Hkv]; a box is 16 rows
+// x `chunks` chunks of one head, landing chunk-major with the 128-byte swizzle.
+bool encode_diffkv_map(CUtensorMap* map, const void* cache, int kv_dtype, int dk, int dv, int Hkv,
+                       int bs, int NB, int chunks);
 
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const Problem& p);

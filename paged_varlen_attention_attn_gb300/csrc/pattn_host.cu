@@ -349,6 +349,24 @@ bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_diffkv_map(CUtensorMap* map, const void* cache, int kv_dtype, int dk, int dv, int Hkv,
+                       int bs, int NB, int chunks) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t row = 2ull * static_cast<cuuint64_t>(dk + dv);  // bytes of a K + V row
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(NB) * static_cast<cuuint64_t>(bs),
+                        static_cast<cuuint64_t>((dk + dv) / 64), static_cast<cuuint64_t>(Hkv)};
+  cuuint64_t strides[3] = {row * Hkv, 128, row};
+  cuuint32_t box[4] = {64, 16, static_cast<cuuint32_t>(chunks), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map,
+             kv_dtype == PATTN_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             4, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int splits) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
@@ -372,14 +390,26 @@ WsLayout workspace_layout(int B, int T, int H, int Hkv, int D, int max_q, int sp
   return L;
 }
 
-// pattn_varlen_fwd on a DiffKV cache: the status word is cleared, then one
-// generic kernel serves every row.
+// pattn_varlen_fwd on a DiffKV cache: the status word is cleared and the
+// requests are ordered longest decode first, then the generic kernel serves
+// the rows with query_len > 1 and the tensor-core DiffKV decode kernel the
+// decode rows (head sizes that are multiples of 64; the generic kernel serves
+// every row otherwise).
 pattn_status_t diffkv_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
                           const int32_t* seq_lens, const int32_t* query_start_loc, void* out,
                           float scale, int num_heads, int num_kv_heads, int head_size,
                           int block_size, int window, int causal, int kv_dtype,
                           const pattn_ext_t* ext) {
-  if (ext->workspace_bytes < sizeof(WsHeader)) return PATTN_ERR_WORKSPACE_TOO_SMALL;
+  // the standard layout with rows of the larger head size (pattn_workspace_bytes
+  // sizes it the same way, for no window): header, partition counters, decode
+  // order and the partitions' partial results of the tensor-core decode kernel
+  const int hv = ext_head_size_v(ext);
+  const int splits = diffkv_decode_supported(head_size, hv)
+                         ? choose_splits(ext, num_kv_heads, block_size, window)
+                         : 1;
+  const WsLayout L = workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads,
+                                      std::max(head_size, hv), ext->max_query_len, splits);
+  if (ext->workspace_bytes < L.total) return PATTN_ERR_WORKSPACE_TOO_SMALL;
   if (ext->num_seqs == 0 || ext->num_tokens == 0) return PATTN_OK;
   if (ext->num_blocks == 0 || ext->max_blocks_per_seq == 0) return PATTN_ERR_INVALID_ARGUMENT;
   Problem p;
@@ -404,11 +434,20 @@ pattn_status_t diffkv_fwd(const void* q, const void* kv_cache, const int32_t* bl
   p.mbps = ext->max_blocks_per_seq;
   p.bt_stride = p.mbps;
   p.NB = ext->num_blocks;
+  p.max_q = ext->max_query_len;
+  p.max_s = ext->max_seq_len;
   p.sinks = ext_sinks(ext);
-  p.hdr = static_cast<WsHeader*>(ext->workspace);
+  unsigned char* ws = static_cast<unsigned char*>(ext->workspace);
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.counters = reinterpret_cast<unsigned*>(ws + L.counters_off);
+  p.decode_order = reinterpret_cast<int*>(ws + L.order_off);
+  p.o_part = reinterpret_cast<float*>(ws + L.o_part_off);
+  p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
+  p.splits = splits;
   p.stream = static_cast<cudaStream_t>(ext->stream);
-  if (cudaMemsetAsync(&p.hdr->status, 0, sizeof(unsigned), p.stream) != cudaSuccess)
-    return PATTN_ERR_CUDA;
+  // clears the status word and orders the requests longest decode first (the
+  // decode grid's order), then the kernels run
+  if (launch_decode_prep(p) != cudaSuccess) return PATTN_ERR_CUDA;
   if (launch_diffkv(p, head_size, ext_head_size_v(ext)) != cudaSuccess) return PATTN_ERR_CUDA;
   return PATTN_OK;
 }
@@ -448,9 +487,10 @@ size_t pattn_workspace_bytes(const pattn_ext_t* ext, int num_heads, int num_kv_h
                              int head_size, int block_size) {
   if (validate(ext, num_heads, num_kv_heads, head_size, block_size) != PATTN_OK) return 0;
   // The window only lowers the automatic split count; size for no window.
+  // The DiffKV layout's partial rows have the larger of the two head sizes.
   const int splits = choose_splits(ext, num_kv_heads, block_size, 0);
-  return workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads, head_size,
-                          ext->max_query_len, splits)
+  return workspace_layout(ext->num_seqs, ext->num_tokens, num_heads, num_kv_heads,
+                          std::max(head_size, ext_head_size_v(ext)), ext->max_query_len, splits)
       .total;
 }
 

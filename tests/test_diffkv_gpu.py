@@ -70,6 +70,18 @@ def test_matches_the_oracle(dk, dv, H, Hkv):
     assert_close(_gpu(dc)[a:b].float().cpu().numpy(), ref[a:b], W.KV_BF16)
 
 
+@pytest.mark.parametrize("window,kv_dtype", [(0, W.KV_BF16), (700, W.KV_BF16), (0, W.KV_F16)])
+def test_long_decode_rows_on_the_tensor_core_kernel(window, kv_dtype):
+    # decode rows long enough to wrap the decode kernel's stage ring many
+    # times, at the K 192 / V 128 shape, with and without a window
+    dc = diffkv_case(1680 + window + kv_dtype, H=32, Hkv=8, dk=192, dv=128, n_req=12,
+                     max_s=3000, window=window, kv_dtype=kv_dtype, kinds=("decode",),
+                     device=DEV)
+    ref, _ = _oracle(dc)
+    a, b = _rows(dc)
+    assert_close(_gpu(dc)[a:b].float().cpu().numpy(), ref[a:b], W.KV_BF16)
+
+
 def test_window_sinks_and_f16():
     dc = diffkv_case(1650, H=8, Hkv=2, dk=128, dv=64, n_req=5, max_s=500, window=77,
                      kv_dtype=W.KV_F16, device=DEV)
