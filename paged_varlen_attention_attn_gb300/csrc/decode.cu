@@ -85,20 +85,16 @@ struct DecodeCfg {
 };
 
 // e4m3 -> f16 widening with the hardware pair conversion: exact (every e4m3
-// value, subnormals included, is an f16 value) and NaN codes stay NaN.  The
-// two codes of the low 16 bits of v become the (lo, hi) halves of the result.
-__device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
-  unsigned r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
-  return r;
-}
-// Codes in bytes 0 and 2 of x (bytes 1 and 3 ignored) -> f16x2 (lo, hi).
-__device__ __forceinline__ unsigned e4m3_b02_to_f16x2(unsigned x) {
-  return e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0020u));
-}
-// Codes in bytes 1 and 3 of x (bytes 0 and 2 ignored) -> f16x2 (lo, hi).
-__device__ __forceinline__ unsigned e4m3_b13_to_f16x2(unsigned x) {
-  return e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0031u));
+// value, subnormals included, is an f16 value) and NaN codes stay NaN.
+// The four codes of x as two f16x2: (bytes 0, 1) -> lo, (bytes 2, 3) -> hi.
+// The 16-bit halves feed the pair conversions directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(unsigned x, unsigned& lo, unsigned& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
 
 // Byte offset of 16-byte chunk c of row j of head hh in a K (or V) unit as
@@ -355,8 +351,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   // (the same permutation on Q and K leaves every dot product unchanged) so
   // each lane reads its K bytes contiguously and widens whole words: k-step
   // kk, fragment columns 2*c4, 2*c4+1, 2*c4+8, 2*c4+9 map to d = base,
-  // base + 2, base + 1, base + 3 with base = c4*D/4 + 4kk (bytes 0, 2 and 1, 3
-  // of the word holding d = base..base+3).
+  // base + 1, base + 2, base + 3 with base = c4*D/4 + 4kk (the two 16-bit
+  // halves of the word holding d = base..base+3).
   unsigned qb[D / 16][NT][2];
   {
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
@@ -371,9 +367,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
           unsigned v = 0;
           if (head < G) {
             if constexpr (FP8) {
-              // d = base + e and base + 2 + e, base = c4*D/4 + 4kk
-              const __nv_bfloat16* qd = qrow + head * D + c4 * (D / 4) + 4 * kk + e;
-              v = pack2<true>(__bfloat162float(qd[0]), __bfloat162float(qd[2]));
+              // d = base + 2e and base + 2e + 1, base = c4*D/4 + 4kk
+              const __nv_bfloat16* qd = qrow + head * D + c4 * (D / 4) + 4 * kk + 2 * e;
+              v = pack2<true>(__bfloat162float(qd[0]), __bfloat162float(qd[1]));
             } else {
               const int d = kk * 16 + 2 * c4 + e * 8;
               v = *reinterpret_cast<const unsigned*>(qrow + head * D + d);
@@ -468,10 +464,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
           const uint4& rb = kr[1][kk >> 2];
           const unsigned w0 = (kk & 3) == 0 ? ra.x : (kk & 3) == 1 ? ra.y : (kk & 3) == 2 ? ra.z : ra.w;
           const unsigned w1 = (kk & 3) == 0 ? rb.x : (kk & 3) == 1 ? rb.y : (kk & 3) == 2 ? rb.z : rb.w;
-          const unsigned a0 = e4m3_b02_to_f16x2(w0);   // key quad,     d base, base + 2
-          const unsigned a2 = e4m3_b13_to_f16x2(w0);   // key quad,     d base + 1, base + 3
-          const unsigned a1 = e4m3_b02_to_f16x2(w1);   // key quad + 8
-          const unsigned a3 = e4m3_b13_to_f16x2(w1);
+          unsigned a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(w0, a0, a2);  // key quad:     d base, base + 1 | base + 2, base + 3
+          e4m3x4_to_f16x2x2(w1, a1, a3);  // key quad + 8
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma_16816<true>(sc[u][kk & 1][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
@@ -583,16 +578,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
         load_v_bytes<D, HG>(sv, hh, 2 * c4 + 9, quad, v3);
 #pragma unroll
         for (int m = 0; m < D / 16; ++m) {
-          // bytes d0 and d0 + 1 of two key rows in one word: [r.d0, r.d0+1,
-          // r'.d0, r'.d0+1]; bytes 0 and 2 are the pair at d0, 1 and 3 at d0 + 1
+          // bytes d0 and d0 + 1 of two key rows r, r' interleaved in one
+          // word, [r.d0, r'.d0, r.d0+1, r'.d0+1]: its low half is the pair at
+          // d0 (fragment row quad), its high half the pair at d0 + 1 (row
+          // quad + 8)
           const int wi = m >> 1;
-          const unsigned sel = (m & 1) ? 0x7632u : 0x5410u;
+          const unsigned sel = (m & 1) ? 0x7362u : 0x5140u;
           const unsigned x01 = __byte_perm(v0[wi], v1[wi], sel);
           const unsigned x23 = __byte_perm(v2[wi], v3[wi], sel);
-          const unsigned a0 = e4m3_b02_to_f16x2(x01);
-          const unsigned a1 = e4m3_b13_to_f16x2(x01);
-          const unsigned a2 = e4m3_b02_to_f16x2(x23);
-          const unsigned a3 = e4m3_b13_to_f16x2(x23);
+          unsigned a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(x01, a0, a1);
+          e4m3x4_to_f16x2x2(x23, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_16816<true>(o[m][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
         }

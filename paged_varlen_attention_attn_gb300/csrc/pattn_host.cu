@@ -73,10 +73,10 @@ int ext_head_size_v(const pattn_ext_t* ext) {
 }
 
 // Decode partition count.  A forced count is used as given; otherwise enough
-// partitions that there are about 8 (request, KV head, partition) items per
-// SM (2 to 4 decode CTAs, depending on how many KV heads one CTA serves), and
-// that no partition is longer than ~8192 keys, bounded by the block count a
-// row can see and by PATTN_MAX_SPLITS.  The decode grid runs the requests
+// partitions that there are about 7 (request, KV head, partition) items per
+// SM, rounded down (about two decode CTAs per SM, depending on how many KV
+// heads one CTA serves), and that no partition is longer than ~8192 keys,
+// bounded by the block count a row can see and by PATTN_MAX_SPLITS.  The decode grid runs the requests
 // longest first, so its ragged end is short partitions and few, long
 // partitions beat many short ones (each CTA has a fixed set-up and merge
 // cost); the length bound only keeps one very long request from becoming the
@@ -89,7 +89,7 @@ int choose_splits(const pattn_ext_t* ext, int num_kv_heads, int block_size, int 
   const int max_blocks = std::max(1, (visible + block_size - 1) / block_size);
   const long long items = static_cast<long long>(std::max(1, ext->num_seqs)) * num_kv_heads;
   const int sms = sm_count();
-  int by_grid = static_cast<int>((8LL * sms + items - 1) / items);
+  int by_grid = static_cast<int>(7LL * sms / items);
   int by_len = (visible + 8191) / 8192;
   int s = std::max(1, std::max(by_grid, by_len));
   s = std::min(s, max_blocks);
