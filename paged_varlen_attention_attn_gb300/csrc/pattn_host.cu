@@ -158,15 +158,17 @@ pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* bl
 // Cost model of the co-scheduled mixed batch (measured on GB300): a prefill
 // key tile of one item (two 128-row sub-tiles, 128 keys) takes about
 // 2.1 us per SM at head size 128 (about 1.3 us at 64; e4m3 tiles about 1.3x
-// longer, for the widening); one SM running two decode CTAs streams about
-// 140 GB/s of 16-bit K/V (e4m3 about 100 GB/s, bound by the widening); decode
-// gets about 85 % of HBM beside the prefill.  The estimate only balances the
-// two kernels; the result does not depend on it.
+// longer, for the widening); beside the prefill, one SM running two decode
+// CTAs streams about 120 GB/s of 16-bit K/V (e4m3 about 100 GB/s); decode
+// gets about 85 % of HBM beside the prefill.  (A sweep of the prefill grid
+// on the mixed workload put the best at 128 of 152 SMs, which these figures
+// reproduce.)  The estimate only balances the two kernels; the result does
+// not depend on it.
 void set_cost_model(Problem& p) {
   p.num_sms = sm_count();
   const bool fp8 = p.kv_dtype == PATTN_KV_FP8_E4M3;
   p.pf_us_per_tile = (p.D == 128 ? 2.1f : 1.3f) * (fp8 ? 1.3f : 1.f);
-  p.dec_bytes_per_us = fp8 ? 100000.f : 140000.f;
+  p.dec_bytes_per_us = fp8 ? 100000.f : 120000.f;
   p.hbm_bytes_per_us = 0.85f * 6800000.f;
 }
 
