@@ -59,6 +59,8 @@ KERNEL_SOURCES = {
                "paged_varlen_attention_attn_gb300/csrc/common.cuh"],
     "prefill": ["paged_varlen_attention_attn_gb300/csrc/prefill.cu",
                 "paged_varlen_attention_attn_gb300/csrc/common.cuh"],
+    "diffkv": ["paged_varlen_attention_attn_gb300/csrc/diffkv_decode.cu",
+               "paged_varlen_attention_attn_gb300/csrc/common.cuh"],
 }
 
 
@@ -774,7 +776,8 @@ def run_diffkv(args, spec, world, rank, local):
                        "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)"},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                         "kernel": "diffkv_kernel", "peak_source": pk_src, "traffic": None},
+                         "kernel": "diffkv_decode_kernel", "peak_source": pk_src,
+                         "traffic": profiled_traffic("diffkv", spec.name)},
             "gpu_launches": K, "clocks": clk}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -121,14 +121,12 @@ __device__ void order_decodes(const Problem& p, int* hist, int* warp_sums,
 // walked in rounds of gs items, a round lasting about its first (largest)
 // item, and never less than the total work over gs SMs.  Decode: m SMs
 // stream at dec_bytes_per_us each, capped by the HBM bandwidth beside prefill.
-__device__ float co_schedule_estimate(const Problem& p, int gs, int n_items, int np,
-                                      unsigned long long work_items, double dec_bytes) {
+// cost[t]: the key tiles of sorted tile t (kept in shared memory by pass 2).
+__device__ float co_schedule_estimate(const Problem& p, const unsigned short* cost, int gs,
+                                      int n_items, int np, unsigned long long work_items,
+                                      double dec_bytes) {
   float rounds = 0.f;
-  for (int x = 0; x < n_items; x += gs) {
-    const int2 tl = p.tiles[x / np];
-    const int t0 = p.qsl[tl.x];
-    rounds += static_cast<float>(tile_cost(p, p.qsl[tl.x + 1] - t0, p.seq_lens[tl.x], tl.y));
-  }
+  for (int x = 0; x < n_items; x += gs) rounds += static_cast<float>(cost[x / np]);
   const float t_pre = p.pf_us_per_tile * fmaxf(rounds, static_cast<float>(work_items) / gs);
   const int m = p.num_sms - gs;
   const float full_rate = fminf(p.num_sms * p.dec_bytes_per_us, p.hbm_bytes_per_us);
@@ -145,6 +143,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __shared__ unsigned long long s_tile_work, s_dec_blocks;
   __shared__ float s_best[PLAN_THREADS / 32];
   __shared__ int s_best_gs[PLAN_THREADS / 32];
+  __shared__ unsigned short s_cost[NBUCKET];  // cost of sorted tile t < NBUCKET
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_tile_work = 0ull;
@@ -201,8 +200,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
     if (!request_ok(p, r, q_len, s, t0) || q_len <= 1) continue;
     const int nt = (q_len + p.rows_per_item - 1) / p.rows_per_item;
     for (int qt = 0; qt < nt; ++qt) {
-      const int slot = atomicAdd(&hist[tile_cost(p, q_len, s, qt)], 1);
+      const int c = tile_cost(p, q_len, s, qt);
+      const int slot = atomicAdd(&hist[c], 1);
       if (slot < p.max_tiles) p.tiles[slot] = make_int2(r, qt);
+      if (slot < NBUCKET) s_cost[slot] = static_cast<unsigned short>(c);
     }
   }
   __syncthreads();
@@ -225,9 +226,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   const unsigned long long work_items = s_tile_work * static_cast<unsigned long long>(np);
   float best = INFINITY;
   int best_gs = p.num_sms;
-  if (n_items > 0 && dec_bytes > 0.0) {
+  // (the tile costs are kept for the first NBUCKET sorted tiles; a batch with
+  // more keeps every SM for its prefill)
+  if (n_items > 0 && dec_bytes > 0.0 && n_items / np <= NBUCKET) {
     for (int gs = p.num_sms - tid; gs >= max(1, p.num_sms / 2); gs -= PLAN_THREADS) {
-      const float e = co_schedule_estimate(p, gs, n_items, np, work_items, dec_bytes);
+      const float e = co_schedule_estimate(p, s_cost, gs, n_items, np, work_items, dec_bytes);
       if (e < best || (e == best && gs > best_gs)) {
         best = e;
         best_gs = gs;
