@@ -26,7 +26,7 @@
 //              e4m3 cache at d 128 it widens the last 48 rows of each K and V
 //              tile
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
-// [384,384+D).  P (bf16, 64 columns) overwrites the upper half of its S
+// [384,384+D).  P (bf16, 64 columns) overwrites the lower half of its S
 // buffer and is read back from TMEM as the A operand of P V; the next scores
 // of that sub-tile are issued right after P V and overwrite it.  The tensor
 // core executes one thread's MMAs in issue order, so P V has read its operand
@@ -61,13 +61,17 @@ namespace pattn {
 namespace {
 
 constexpr int PF_THREADS = 384;
-// Register split (setmaxnreg): the two softmax warpgroups take SOFTMAX_REGS
-// per thread, the producer / MMA warpgroup gives its share back.  The sum must
-// stay within the launch allocation (PF_THREADS x the kernel's register count,
-// checked on the host before every launch) or setmaxnreg.inc would wait forever.
-constexpr int SOFTMAX_REGS = 216;
-constexpr int OTHER_REGS = 72;
-constexpr int SPLIT_REGS_TOTAL = 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS;
+// Register split (setmaxnreg): the two softmax warpgroups take
+// softmax_regs(FP8) per thread, the producer / MMA warpgroup gives its share
+// back (other_regs).  An e4m3 call's producer widens tiles and needs more.
+// The sum must stay within the launch allocation (PF_THREADS x the kernel's
+// register count, checked on the host before every launch) or
+// setmaxnreg.inc would wait forever; both splits total SPLIT_REGS_TOTAL.
+__host__ __device__ constexpr int softmax_regs(bool fp8) { return fp8 ? 200 : 216; }
+__host__ __device__ constexpr int other_regs(bool fp8) { return fp8 ? 104 : 72; }
+constexpr int SPLIT_REGS_TOTAL = 2 * 128 * softmax_regs(false) + 128 * other_regs(false);
+static_assert(2 * 128 * softmax_regs(true) + 128 * other_regs(true) == SPLIT_REGS_TOTAL,
+              "both register splits fit the same launch allocation");
 // K and V rings: K gets the extra stage because the next scores need it
 // before the next P V needs V.  224 KB of shared memory at head size 128.
 constexpr int PF_KST = 3;
@@ -259,6 +263,30 @@ __device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) 
       : "f"(a0), "f"(a1));
 }
 
+// The weights 2^(x sl2 - ref) of 32 scores, packed in pairs (bf16, or f16
+// when F16) as P; returns their sum.
+template <bool F16>
+__device__ __forceinline__ float exp_piece(const float (&x)[32], float sl2, float ref,
+                                           unsigned (&pk)[16]) {
+  const float neg_m = -ref;
+  float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    float a0 = x[e], a1 = x[e + 1], a2 = x[e + 2], a3 = x[e + 3];
+    ffma2(a0, a1, sl2, neg_m);
+    ffma2(a2, a3, sl2, neg_m);
+    a0 = fast_exp2(a0);
+    a1 = fast_exp2(a1);
+    a2 = fast_exp2(a2);
+    a3 = fast_exp2(a3);
+    fadd2(ps0, ps1, a0, a1);
+    fadd2(ps2, ps3, a2, a3);
+    pk[e / 2] = pack2<F16>(a0, a1);
+    pk[e / 2 + 1] = pack2<F16>(a2, a3);
+  }
+  return (ps0 + ps1) + (ps2 + ps3);
+}
+
 // One work item: a 128-row query tile (two sub-tiles) of one request, one head
 // pair (or head) and one key chunk, read from the LPT-ordered tile list.
 struct Item {
@@ -408,7 +436,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int pages_per_tile = BLOCK_N / rows_box;         // copies of one key tile
 
   if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(OTHER_REGS));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(other_regs(FP8)));
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ TMA producers
     // Warp 8 streams the Q tiles and the K tiles, warp 10 the V tiles, each
@@ -649,7 +677,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               // The base addresses are made opaque here so that their per-MMA
               // offsets are added at each use instead of being hoisted out of
               // the loops as 16 live registers.
-              unsigned p_t = tmem + C::s_col(X) + 64;
+              unsigned p_t = tmem + C::s_col(X);
               unsigned o_t = tmem + C::o_col(X);
               asm volatile("" : "+r"(p_t), "+r"(o_t));
               const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
@@ -747,7 +775,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(softmax_regs(FP8)));
     // ------------------------------------------------------------ softmax warpgroups
     const int X = warp >> 2;            // 0: A (warps 0-3), 1: B (warps 4-7)
     const int row = threadIdx.x & 127;  // TMEM lane
@@ -815,60 +843,56 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           break;
         }
         tc_fence_after();
-        float sv[BLOCK_N];
-#pragma unroll
-        for (int q = 0; q < BLOCK_N / 32; ++q)
-          tc_ld32(s_t + q * 32, *reinterpret_cast<float(*)[32]>(&sv[q * 32]));
-        tc_wait_ld();
-
-        // Does any row of this sub-tile see a masked key in this tile?
-        if (key0 > edge_hi || key0 <= edge_lo) {
-          // column limits of this row in the tile: visible iff lim_lo <= q < lim_hi
-          const int lim_hi = kmax_row - key0;
-          const int lim_lo = kmin_row - key0;
-#pragma unroll
-          for (int q = 0; q < BLOCK_N; ++q)
-            sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
-        }
-        // The weights 2^(x - ref) of the row against reference ref, packed
-        // and stored to TMEM as P (the upper half of this sub-tile's S
-        // columns); returns their sum.
-        auto exp_store = [&](float ref) -> float {
-          const float neg_m = -ref;
-          float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
-#pragma unroll
-          for (int q = 0; q < BLOCK_N; q += 32) {
-            unsigned pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              float a0 = sv[q + e], a1 = sv[q + e + 1], a2 = sv[q + e + 2], a3 = sv[q + e + 3];
-              ffma2(a0, a1, sl2, neg_m);
-              ffma2(a2, a3, sl2, neg_m);
-              a0 = fast_exp2(a0);
-              a1 = fast_exp2(a1);
-              a2 = fast_exp2(a2);
-              a3 = fast_exp2(a3);
-              fadd2(ps0, ps1, a0, a1);
-              fadd2(ps2, ps3, a2, a3);
-              pk[e / 2] = pack2<MMA_F16>(a0, a1);
-              pk[e / 2 + 1] = pack2<MMA_F16>(a2, a3);
-            }
-            tc_st16u(s_t + 64 + q / 2, pk);
-          }
-          return (ps0 + ps1) + (ps2 + ps3);
-        };
+        const bool edge = key0 > edge_hi || key0 <= edge_lo;
+        // column limits of this row in the tile: visible iff lim_lo <= col < lim_hi
+        const int lim_hi = kmax_row - key0;
+        const int lim_lo = kmin_row - key0;
         // Common case: the reference stays.  The weights against it are
-        // computed and stored; if any exceeded 2^RESCALE_THRESHOLD, their sum
-        // did too, and the tile is redone below against a moved reference.
-        // So the row max is taken only for a row's first tile and for the
-        // rare tile whose scores outgrow the reference.
+        // computed in registers; if any exceeded 2^RESCALE_THRESHOLD, their
+        // sum did too, and the tile goes down the path below, which takes the
+        // row max.  So the max is taken only for a row's first tile and for
+        // the rare tile whose scores outgrow the reference.  P (16 packed
+        // columns per 32 scores) is stored at columns [0, 64) only once the
+        // tile is known to stay on this path, so the scores are still in TMEM
+        // for the other one.
         bool slow = (m_run == -INFINITY);
         float ps = 0.f;
         if (!__any_sync(FULL, slow)) {
-          ps = exp_store(m_run);
+          float sv[BLOCK_N];
+#pragma unroll
+          for (int g = 0; g < BLOCK_N / 32; ++g)
+            tc_ld32(s_t + g * 32, *reinterpret_cast<float(*)[32]>(&sv[g * 32]));
+          tc_wait_ld();
+          if (edge) {
+#pragma unroll
+            for (int q = 0; q < BLOCK_N; ++q)
+              sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
+          }
+          unsigned pk[BLOCK_N / 2];
+#pragma unroll
+          for (int g = 0; g < BLOCK_N / 32; ++g)
+            ps += exp_piece<MMA_F16>(*reinterpret_cast<const float(*)[32]>(&sv[g * 32]), sl2,
+                                     m_run, *reinterpret_cast<unsigned(*)[16]>(&pk[g * 16]));
           slow = !(ps <= FAST_SUM_LIMIT);
+          if (!__any_sync(FULL, slow)) {
+#pragma unroll
+            for (int g = 0; g < BLOCK_N / 32; ++g)
+              tc_st16u(s_t + g * 16, *reinterpret_cast<const unsigned(*)[16]>(&pk[g * 16]));
+          }
         }
         if (__any_sync(FULL, slow)) {
+          // The scores again (still in TMEM: nothing was stored over them),
+          // all 128 columns in one round trip.
+          float sv[BLOCK_N];
+#pragma unroll
+          for (int g = 0; g < BLOCK_N / 32; ++g)
+            tc_ld32(s_t + g * 32, *reinterpret_cast<float(*)[32]>(&sv[g * 32]));
+          tc_wait_ld();
+          if (edge) {
+#pragma unroll
+            for (int q = 0; q < BLOCK_N; ++q)
+              sv[q] = (q < lim_hi && q >= lim_lo) ? sv[q] : -INFINITY;
+          }
           float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
           for (int q = 4; q < BLOCK_N - 4; q += 8) {
@@ -881,7 +905,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
           const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
           const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-
           // Lazy rescale: move the reference max only when it grows by > 2^8,
           // or, for a row whose own weights summed above the limit, whenever
           // it grows (else that row would take this path on every tile).
@@ -893,9 +916,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             l_run *= alpha;
             m_run = mx_s;
           }
+          // The weights, each 32 columns' P stored as soon as it is packed
+          // (to columns [16g, 16g + 16), whose scores are in registers).
+          const float ref = (m_run == -INFINITY) ? 0.f : m_run;
+          ps = 0.f;
+#pragma unroll
+          for (int g = 0; g < BLOCK_N / 32; ++g) {
+            unsigned pk[16];
+            ps += exp_piece<MMA_F16>(*reinterpret_cast<const float(*)[32]>(&sv[g * 32]), sl2,
+                                     ref, pk);
+            tc_st16u(s_t + g * 16, pk);
+          }
+          // O is rescaled last, once the score registers are free.  P V of
+          // the previous tile is complete: the commit that announced these
+          // scores was issued after it.
           if (__any_sync(FULL, need_o)) {
-            // P V of the previous tile is complete: the commit that announced
-            // these scores was issued after it.
             const float a = need_o ? alpha : 1.f;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
@@ -907,7 +942,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               tc_st32(o_t + q * 32, ov);
             }
           }
-          ps = exp_store((m_run == -INFINITY) ? 0.f : m_run);
         }
         l_run += ps;
         tc_wait_st();
