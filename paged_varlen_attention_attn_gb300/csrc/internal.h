@@ -131,13 +131,24 @@ cudaError_t launch_plan(const Problem& p);
 // programmatic dependent.
 cudaError_t launch_decode_prep(const Problem& p);
 cudaError_t launch_decode(const Problem& p, const CUtensorMap& kv_map);
-cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map);
-// TMA tensor map over the KV cache [2 * NB][bs][Hkv][D] with boxes of
-// box_rows rows of one head: 64 16-bit elements (128-byte swizzle) per box, or
-// a whole e4m3 row (128-byte swizzle at D = 128, none at D = 64).  Returns
-// false if the driver entry point is missing or rejects the map.
+cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                           const CUtensorMap& v_map);
+// The prefill kernel's TMA tensor maps over the KV cache [2 * NB][bs][Hkv][D].
+// A 16-bit cache (128-byte swizzle): for the K copies, 4-D {D, KV head, slot,
+// block} with a box of box_rows slots of one head and one 64-element d half;
+// for the V copies (v_groups), 5-D {64, row of a 16-slot group, d half, KV
+// head, group} over the cache's groups (block * bs / 16 + slot / 16), with a
+// box of box_rows / 16 groups of one head, both d halves, which lands as
+// [group][d half][16 rows][128 bytes].  An e4m3 cache: 4-D {D bytes, KV head,
+// slot, block}, one box = box_rows whole rows of one head, unswizzled
+// (v_groups unused).  Returns false if the driver entry point is missing or
+// rejects the map.
 bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv, int bs,
-                   int NB, int box_rows);
+                   int NB, int box_rows, bool v_groups);
+// q's map (encode_q_map) and the K and V maps of a prefill launch.
+bool encode_prefill_maps(CUtensorMap* qmap, CUtensorMap* kmap, CUtensorMap* vmap, const void* q,
+                         const void* kv_cache, int kv_dtype, int H, int D, int T, int Hkv, int bs,
+                         int NB);
 
 // TMA tensor map for the decode kernel: one box is 16 rows of a group of
 // `heads` KV heads (both d halves for 16-bit data), laid out in shared memory

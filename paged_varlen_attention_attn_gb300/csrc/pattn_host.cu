@@ -218,11 +218,11 @@ bool encode_q_map(CUtensorMap* map, const void* q, int kv_dtype, int H, int D, i
 // decode kernel, for one pass.
 pattn_status_t launch_pass(const Problem& p) {
   if (p.max_q > 1) {
-    CUtensorMap qmap, kvmap;
-    if (!encode_q_map(&qmap, p.q, p.kv_dtype, p.H, p.D, p.T)) return PATTN_ERR_CUDA;
-    if (!encode_kv_map(&kvmap, p.kv, p.kv_dtype, p.D, p.Hkv, p.bs, p.NB, std::min(p.bs, BLOCK_N)))
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_prefill_maps(&qmap, &kmap, &vmap, p.q, p.kv, p.kv_dtype, p.H, p.D, p.T, p.Hkv,
+                             p.bs, p.NB))
       return PATTN_ERR_CUDA;
-    if (launch_prefill(p, qmap, kvmap) != cudaSuccess) return PATTN_ERR_CUDA;
+    if (launch_prefill(p, qmap, kmap, vmap) != cudaSuccess) return PATTN_ERR_CUDA;
   }
   CUtensorMap dmap;
   if (!encode_decode_map(&dmap, p.kv, p.kv_dtype, p.D, p.Hkv, p.bs, p.NB,
@@ -298,29 +298,59 @@ int test_wait_skip() { return g_test_wait_skip.load(); }
 #endif
 
 bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv, int bs,
-                   int NB, int box_rows) {
+                   int NB, int box_rows, bool v_groups) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const bool fp8 = kv_dtype == PATTN_KV_FP8_E4M3;
-  const cuuint64_t es = fp8 ? 1 : 2;
-  const cuuint64_t row = static_cast<cuuint64_t>(D) * es;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (kv_dtype == PATTN_KV_FP8_E4M3) {
+    // e4m3 rows land unswizzled in the prefill kernel's staging buffer (its
+    // producers widen them into the swizzled f16 layout).
+    const cuuint64_t row = static_cast<cuuint64_t>(D);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                          static_cast<cuuint64_t>(bs), 2ull * static_cast<cuuint64_t>(NB)};
+    cuuint64_t strides[3] = {row, row * Hkv, row * Hkv * bs};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows), 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv_cache), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+  const CUtensorMapDataType dt = kv_dtype == PATTN_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (v_groups) {
+    // {64, row of a 16-slot group, d half, head, group}: a block's slots are
+    // bs / 16 consecutive groups
+    cuuint64_t dims[5] = {64, 16, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(Hkv),
+                          2ull * static_cast<cuuint64_t>(NB) * static_cast<cuuint64_t>(bs / 16)};
+    cuuint64_t strides[4] = {row * Hkv, 128, row, 16 * row * Hkv};
+    cuuint32_t box[5] = {64, 16, static_cast<cuuint32_t>(D / 64), 1,
+                         static_cast<cuuint32_t>(box_rows / 16)};
+    return enc(map, dt, 5, const_cast<void*>(kv_cache), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(bs), 2ull * static_cast<cuuint64_t>(NB)};
   cuuint64_t strides[3] = {row, row * Hkv, row * Hkv * bs};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(fp8 ? D : 64), 1,
-                       static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  // e4m3 rows land unswizzled in the prefill kernel's staging buffer (its
-  // producers widen them into the swizzled f16 layout).
-  const CUtensorMapSwizzle sw = fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  return enc(map,
-             fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                 : (kv_dtype == PATTN_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
-             4,
-             const_cast<void*>(kv_cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  return enc(map, dt, 4, const_cast<void*>(kv_cache), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The three maps of a prefill launch: q, the K copies and the V copies (the
+// same map for an e4m3 cache).
+bool encode_prefill_maps(CUtensorMap* qmap, CUtensorMap* kmap, CUtensorMap* vmap, const void* q,
+                         const void* kv_cache, int kv_dtype, int H, int D, int T, int Hkv, int bs,
+                         int NB) {
+  const int rows = std::min(bs, BLOCK_N);
+  if (!encode_q_map(qmap, q, kv_dtype, H, D, T)) return false;
+  if (!encode_kv_map(kmap, kv_cache, kv_dtype, D, Hkv, bs, NB, rows, false)) return false;
+  if (kv_dtype == PATTN_KV_FP8_E4M3) {
+    *vmap = *kmap;
+    return true;
+  }
+  return encode_kv_map(vmap, kv_cache, kv_dtype, D, Hkv, bs, NB, rows, true);
 }
 
 bool encode_decode_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, int Hkv,
@@ -620,13 +650,11 @@ pattn_status_t pattn_varlen_fwd(const void* q, const void* kv_cache, const int32
   mark(2);
 
   if (tc_prefill) {
-    CUtensorMap qmap, kvmap;
-    if (!encode_q_map(&qmap, q, kv_dtype, num_heads, head_size, ext->num_tokens))
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_prefill_maps(&qmap, &kmap, &vmap, q, kv_cache, kv_dtype, num_heads, head_size,
+                             ext->num_tokens, num_kv_heads, block_size, ext->num_blocks))
       return PATTN_ERR_CUDA;
-    if (!encode_kv_map(&kvmap, kv_cache, kv_dtype, head_size, num_kv_heads, block_size,
-                       ext->num_blocks, std::min(block_size, BLOCK_N)))
-      return PATTN_ERR_CUDA;
-    if (launch_prefill(p, qmap, kvmap) != cudaSuccess) return PATTN_ERR_CUDA;
+    if (launch_prefill(p, qmap, kmap, vmap) != cudaSuccess) return PATTN_ERR_CUDA;
   }
   mark(3);
   mark(4);

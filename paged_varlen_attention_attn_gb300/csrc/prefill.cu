@@ -20,11 +20,12 @@
 //   warp  8    TMA producer of both Q tiles of each item and the K tiles, page by
 //              page through block_table into a 3-stage ring, one lane per
 //              page copy (over an e4m3 cache it also widens each K tile)
-//   warp  9    MMA issuer (one thread)
-//   warp 10    TMA producer of the V tiles (2-stage ring), likewise
-//   warp 11    idle (it completes the third warpgroup for setmaxnreg); over an
-//              e4m3 cache at d 128 it widens the last 48 rows of each K and V
-//              tile
+//   warp  9    MMA issuer (one thread): sub-tile A's MMAs over a 16-bit
+//              cache, both sub-tiles' over an e4m3 cache
+//   warp 10    TMA producer of the V tiles (2-stage ring), one page per copy
+//   warp 11    MMA issuer of sub-tile B over a 16-bit cache (the two issuers
+//              take turns); over an e4m3 cache at d 128 it widens the last 48
+//              rows of each K and V tile, at d 64 it is idle
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
 // [384,384+D).  P (bf16, 64 columns) overwrites the lower half of its S
 // buffer and is read back from TMEM as the A operand of P V; the next scores
@@ -84,6 +85,13 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr float FAST_SUM_LIMIT = 256.0f;
 constexpr unsigned FULL = 0xffffffffu;
 
+// A 16-bit V tile sits in shared memory as groups of 16 keys, each group's d
+// halves one after the other ([key / 16][d half][key % 16][128 bytes]), so
+// that one copy moves a whole page; an e4m3 V tile is widened into the K tile
+// layout ([d half][key][128 bytes]), the same with groups of V_ROWS = BLOCK_N.
+template <bool FP8>
+__host__ __device__ constexpr int v_rows() { return FP8 ? BLOCK_N : 16; }
+
 template <int D>
 struct PrefillCfg {
   static constexpr int DH = D / 64;                 // 128-byte column blocks
@@ -119,6 +127,7 @@ struct Bars {
   uint64_t o_final[2];  // the last P V of sub-tile X
   uint64_t q_empty;     // every S MMA of an item issued and done: Q may be replaced
   uint64_t drain;       // every MMA issued, before TMEM is released
+  uint64_t tok[2];      // issuer X may take its turn (two MMA issuers)
   unsigned tmem_base;
   int abort_flag;
 };
@@ -359,16 +368,18 @@ __device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) 
 // that follows the item's last S MMA, and the first P V of the next item
 // (which overwrites O) waits on p_full, which the softmax warps arrive on only
 // after their epilogue has read O.
-template <int D, bool HALF, bool FP8>
+template <int D, bool HALF, bool FP8, bool TWO>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ Problem p, const __grid_constant__ CUtensorMap qmap,
-                   const __grid_constant__ CUtensorMap kvmap, float sl2, float out_scale) {
+                   const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, float sl2, float out_scale) {
   using C = PrefillCfg<D>;
   constexpr bool MMA_F16 = HALF || FP8;  // operand and P type of the MMAs
   // e4m3 at d 128: warp 11 widens rows [HELP_ROW, BLOCK_N) of every K and V
   // tile, the producers rows [0, HELP_ROW) (10 KB and 12 KB of f16 a tile
   // instead of 16 KB for each producer, on three SM sub-partitions)
   constexpr bool HELP = FP8 && D == 128;
+  static_assert(!(TWO && FP8), "an e4m3 call has one MMA issuer (warp 11 widens tiles)");
   constexpr int HELP_ROW = 80;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -404,18 +415,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // an e4m3 d 128 stage is announced by its producer and by warp 11
     for (int i = 0; i < PF_KST; ++i) {
       mbar_init(&bars->k_full[i], HELP ? 2 : 1);
-      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->k_empty[i], TWO ? 2 : 1);
     }
     for (int i = 0; i < PF_VST; ++i) {
       mbar_init(&bars->v_full[i], HELP ? 2 : 1);
-      mbar_init(&bars->v_empty[i], 1);
+      mbar_init(&bars->v_empty[i], TWO ? 2 : 1);
     }
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_empty, TWO ? 2 : 1);
+    mbar_init(&bars->tok[0], 1);
+    mbar_init(&bars->tok[1], 1);
     for (int i = 0; i < PF_KST; ++i) mbar_init(&bars->k_land[i], 1);
     for (int i = 0; i < PF_VST; ++i) mbar_init(&bars->v_land[i], 1);
     mbar_init(&bars->q_conv[0], 4);  // one arrival per warp of the softmax warpgroup
     mbar_init(&bars->q_conv[1], 4);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, TWO ? 2 : 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -449,11 +462,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int kv = (warp == 10) ? 1 : 0;
     const int nst = kv ? PF_VST : PF_KST;
     unsigned char* ring = kv ? sV : sK;
-    // Copy `lane` of a tile: page lane / DH, d half lane % DH.
-    const int my_pg = lane / C::DH, my_dh = lane % C::DH;
+    // Copy `lane` of a tile: a K copy is page lane / DH, d half lane % DH; a
+    // 16-bit V copy is the whole of page lane (its rows_box / 16 groups).
+    const bool v16 = kv && !FP8;
+    const int my_pg = v16 ? lane : lane / C::DH, my_dh = v16 ? 0 : lane % C::DH;
     if (kv == 0 && lane == 0) {
       tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kvmap);
+      tma_prefetch_desc(&kmap);
+      if (!FP8) tma_prefetch_desc(&vmap);
     }
     int jg = 0;        // key tiles streamed so far (ring position)
     int n_worked = 0;  // items with at least one key tile so far
@@ -538,9 +554,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           ok = __shfl_sync(FULL, ok, 0);
           if (!ok) break;
           armed_end = jg + 1;
-          if (my_pg < n_load && !skip)
-            tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kvmap,
-                        full, my_dh * 64, g, my_slot, kv * p.NB + my_blk);
+          if (my_pg < n_load && !skip) {
+            if (v16)
+              tma_load_5d(ring + st * C::TILE + my_pg * (C::DH * rows_box * 128), &vmap, full, 0,
+                          0, 0, g, (p.NB + my_blk) * (p.bs >> 4) + (my_slot >> 4));
+            else
+              tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kmap,
+                          full, my_dh * 64, g, my_slot, my_blk);
+          }
         }
       } else {
         // e4m3: a tile's pages land as bytes at the top of its ring stage (the
@@ -568,7 +589,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           if (good && lane < n_load) {
             const int key0 = key_base + lane * rows_box;
             const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
-            tma_load_4d(ring + st * C::TILE + C::SRC8 + lane * rows_box * D, &kvmap, &lands[st],
+            tma_load_4d(ring + st * C::TILE + C::SRC8 + lane * rows_box * D, &kmap, &lands[st],
                         0, g, slot, kv * p.NB + blkv);
           }
           return good;
@@ -621,8 +642,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
       __syncwarp();
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || (TWO && warp == 11)) {
+    // ------------------------------------------------------------ MMA issuers
+    // A tcgen05.mma occupies its issuing thread for about as long as the
+    // tensor core takes to run it, so everything else that thread does (barrier
+    // waits, commits, bookkeeping) leaves the tensor core idle.  With TWO
+    // (a 16-bit cache) two threads issue: warp 9 sub-tile
+    // A's MMAs, warp 11 sub-tile B's.  They take turns, A then B for each key
+    // tile, handing a token over through tok[] (A's turn t waits for B's turn
+    // t - 1, B's turn t for A's turn t), and each waits for its operands and
+    // commits while the other one issues.  Each commits its own release of
+    // every K and V stage and of the Q tiles (those barriers then count one
+    // arrival per issuer).  Otherwise warp 9 issues both sub-tiles' MMAs in
+    // the same order (over an e4m3 cache warp 11 widens tiles).
     if (lane == 0) {
       constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !MMA_F16, false);
       constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, !MMA_F16, true);
@@ -630,87 +662,81 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       // o >> 4 (shared addresses stay far below the field's 256 KB range).
       const uint64_t q_d = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_d = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t v_d = smem_desc_sw128(smem_u32(sV), C::HALF, 1024);
-      int jg = 0;                  // key tiles consumed so far (ring position)
-      int pv_tot0 = 0, pv_tot1 = 0;  // P V of sub-tile X so far (p_full phase)
-      int q_tot0 = 0, q_tot1 = 0;    // Q tiles of sub-tile X so far (q_full phase)
-      bool issued = false, ok = true;
-      // The next item's metadata is read when the item starts: the issuer
-      // then waits for that item's Q tiles anyway.
-      for (int k = 0; ok && k * GS < n_items; ++k) {
-        const Item it = load_item(p, item_at(k), n_items, NP, KC);
-        const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
-        int u0;
-        const int n_union = union_tiles(subA, subB, u0);
-        if (n_union <= 0) continue;
-        issued = true;
-        int n_pv0 = 0, n_pv1 = 0;
-        bool q_ready0 = false, q_ready1 = false;
-        for (int j = 0; ok && j <= n_union; ++j) {
-          const int kt = u0 + j;
-          const int jj = jg + j;
-          bool k_ready = false, v_ready = false;
-          // Unrolled: every per-sub-tile value stays in a register (a runtime
-          // choice between two locals would put them in local memory).
-#pragma unroll
-          for (int X = 0; X < 2; ++X) {
-            const Sub& u = X ? subB : subA;
-            int& n_pv = X ? n_pv1 : n_pv0;
-            int& pv_tot = X ? pv_tot1 : pv_tot0;
-            int& q_tot = X ? q_tot1 : q_tot0;
-            bool& q_ready = X ? q_ready1 : q_ready0;
-            // P V for the previous key tile
-            if (j >= 1 && u.active(kt - 1)) {
-              const int stp = (jj - 1) % PF_VST;
-              if (!mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag)) {
+      // V: the d halves of a group of V_ROWS keys are V_ROWS x 128 bytes apart
+      constexpr int V_ROWS = v_rows<FP8>();
+      const uint64_t v_d = smem_desc_sw128(smem_u32(sV), V_ROWS * 128, 1024);
+      if constexpr (TWO) {
+        // This thread issues sub-tile X's MMAs.
+        const int X = (warp == 11) ? 1 : 0;
+        int jg = 0;         // key tiles consumed so far (ring position)
+        int pv_tot = 0;     // P V of sub-tile X so far (p_full phase)
+        int q_tot = 0;      // Q tiles of sub-tile X so far (q_full phase)
+        unsigned turn = 0;  // turns taken so far
+        bool ok = true;
+        for (int k = 0; ok && k * GS < n_items; ++k) {
+          const Item it = load_item(p, item_at(k), n_items, NP, KC);
+          const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
+          int u0;
+          const int n_union = union_tiles(subA, subB, u0);
+          if (n_union <= 0) continue;
+          const Sub u = X ? subB : subA;
+          int n_pv = 0;
+          bool q_ready = false;
+          for (int j = 0; ok && j <= n_union; ++j, ++turn) {
+            const int kt = u0 + j;
+            const int jj = jg + j;
+            const bool do_pv = j >= 1 && u.active(kt - 1);  // P V for the previous key tile
+            const bool do_s = j < n_union && u.active(kt);  // scores for this key tile
+            const int stp = (jj - 1) % PF_VST;
+            const int st = jj % PF_KST;
+            // The operands, all before the turn: P and V of the previous
+            // tile, K of this tile and Q.
+            if (do_pv && !(mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag) &&
+                           mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status,
+                                     abort_flag))) {
+              ok = false;
+              break;
+            }
+            if (do_s) {
+              if (!mbar_wait(&bars->k_full[st], (jj / PF_KST) & 1, status, abort_flag)) {
                 ok = false;
                 break;
               }
-              if (!v_ready) {
-                if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                v_ready = true;
-              }
-              tc_fence_after();
-              // The base addresses are made opaque here so that their per-MMA
-              // offsets are added at each use instead of being hoisted out of
-              // the loops as 16 live registers.
-              unsigned p_t = tmem + C::s_col(X);
-              unsigned o_t = tmem + C::o_col(X);
-              asm volatile("" : "+r"(p_t), "+r"(o_t));
-              const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-                tc_mma_ts(o_t, p_t + kk * 8, vb + ((kk * 16 * 128) >> 4), idesc_pv,
-                          (n_pv > 0 || kk > 0) ? 1u : 0u);
-              ++n_pv;
-              ++pv_tot;
-              if (kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
-              if (X == 1 || !subB.active(kt - 1)) tc_commit(&bars->v_empty[stp]);
-            }
-            // scores for this key tile
-            if (j < n_union && u.active(kt)) {
-              const int st = jj % PF_KST;
-              if (!k_ready) {
-                if (!mbar_wait(&bars->k_full[st], (jj / PF_KST) & 1, status, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                k_ready = true;
-              }
               if (!q_ready) {
-                // an e4m3 call's Q is usable once its softmax warpgroup has converted it
-                if (!mbar_wait(FP8 ? &bars->q_conv[X] : &bars->q_full[X], q_tot & 1, status,
-                               abort_flag)) {
+                if (!mbar_wait(&bars->q_full[X], q_tot & 1, status, abort_flag)) {
                   ok = false;
                   break;
                 }
                 q_ready = true;
                 ++q_tot;
               }
-              tc_fence_after();
+            }
+            // The turn: A's turn t follows B's turn t - 1, B's turn t follows
+            // A's turn t.
+            if ((X == 1 || turn > 0) &&
+                !mbar_wait(&bars->tok[X], (X ? turn : turn - 1) & 1, status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (do_pv) {
+              // The base addresses are made opaque here so that their per-MMA
+              // offsets are added at each use instead of being hoisted out of
+              // the loops as live registers.
+              unsigned p_t = tmem + C::s_col(X);
+              unsigned o_t = tmem + C::o_col(X);
+              asm volatile("" : "+r"(p_t), "+r"(o_t));
+              const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+                tc_mma_ts(o_t, p_t + kk * 8,
+                          vb + ((((kk * 16) / V_ROWS * C::DH * V_ROWS) + (kk * 16) % V_ROWS) *
+                                    128 >> 4),
+                          idesc_pv, (n_pv > 0 || kk > 0) ? 1u : 0u);
+              ++n_pv;
+              ++pv_tot;
+            }
+            if (do_s) {
               uint64_t qb = q_d + ((X * C::TILE) >> 4);
               unsigned s_t = tmem + C::s_col(X);
               asm volatile("" : "+l"(qb), "+r"(s_t));
@@ -720,20 +746,129 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
                 tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
               }
-              tc_commit(&bars->s_full[X]);
-              if (X == 1 || !subB.active(kt)) tc_commit(&bars->k_empty[st]);
             }
+            mbar_arrive(&bars->tok[1 - X]);  // the other issuer's turn
+            // Commits, while the other issuer's MMAs run.  Every stage of the
+            // item's key tiles is released by both issuers.
+            if (do_s) tc_commit(&bars->s_full[X]);
+            if (do_pv && kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
+            if (j >= 1) tc_commit(&bars->v_empty[stp]);
+            if (j < n_union) tc_commit(&bars->k_empty[st]);
+            // every S of this item is issued: its Q tiles may be replaced
+            if (j == n_union - 1) tc_commit(&bars->q_empty);
           }
-          // every S of this item is issued: its Q tiles may be replaced
-          if (ok && j == n_union - 1) tc_commit(&bars->q_empty);
+          jg += n_union;
         }
-        jg += n_union;
-      }
-      // No MMA may still be running when TMEM is released (matters only when
-      // a role gave up on a wait).
-      if (issued) {
+        // No MMA may still be running when TMEM is released (matters only when
+        // a role gave up on a wait); both issuers arrive on drain.
         tc_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, status, nullptr);
+      } else {
+        int jg = 0;                  // key tiles consumed so far (ring position)
+        int pv_tot0 = 0, pv_tot1 = 0;  // P V of sub-tile X so far (p_full phase)
+        int q_tot0 = 0, q_tot1 = 0;    // Q tiles of sub-tile X so far (q_full phase)
+        bool issued = false, ok = true;
+        for (int k = 0; ok && k * GS < n_items; ++k) {
+          const Item it = load_item(p, item_at(k), n_items, NP, KC);
+          const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
+          int u0;
+          const int n_union = union_tiles(subA, subB, u0);
+          if (n_union <= 0) continue;
+          issued = true;
+          int n_pv0 = 0, n_pv1 = 0;
+          bool q_ready0 = false, q_ready1 = false;
+          for (int j = 0; ok && j <= n_union; ++j) {
+            const int kt = u0 + j;
+            const int jj = jg + j;
+            bool k_ready = false, v_ready = false;
+            // Unrolled: every per-sub-tile value stays in a register (a runtime
+            // choice between two locals would put them in local memory).
+  #pragma unroll
+            for (int X = 0; X < 2; ++X) {
+              const Sub& u = X ? subB : subA;
+              int& n_pv = X ? n_pv1 : n_pv0;
+              int& pv_tot = X ? pv_tot1 : pv_tot0;
+              int& q_tot = X ? q_tot1 : q_tot0;
+              bool& q_ready = X ? q_ready1 : q_ready0;
+              // P V for the previous key tile
+              if (j >= 1 && u.active(kt - 1)) {
+                const int stp = (jj - 1) % PF_VST;
+                if (!mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                if (!v_ready) {
+                  if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  v_ready = true;
+                }
+                tc_fence_after();
+                // The base addresses are made opaque here so that their per-MMA
+                // offsets are added at each use instead of being hoisted out of
+                // the loops as 16 live registers.
+                unsigned p_t = tmem + C::s_col(X);
+                unsigned o_t = tmem + C::o_col(X);
+                asm volatile("" : "+r"(p_t), "+r"(o_t));
+                const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
+  #pragma unroll
+                for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+                  tc_mma_ts(o_t, p_t + kk * 8,
+                            vb + ((((kk * 16) / V_ROWS * C::DH * V_ROWS) + (kk * 16) % V_ROWS) *
+                                      128 >> 4),
+                            idesc_pv,
+                            (n_pv > 0 || kk > 0) ? 1u : 0u);
+                ++n_pv;
+                ++pv_tot;
+                if (kt - 1 == u.x1 - 1) tc_commit(&bars->o_final[X]);
+                if (X == 1 || !subB.active(kt - 1)) tc_commit(&bars->v_empty[stp]);
+              }
+              // scores for this key tile
+              if (j < n_union && u.active(kt)) {
+                const int st = jj % PF_KST;
+                if (!k_ready) {
+                  if (!mbar_wait(&bars->k_full[st], (jj / PF_KST) & 1, status, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  k_ready = true;
+                }
+                if (!q_ready) {
+                  // an e4m3 call's Q is usable once its softmax warpgroup has converted it
+                  if (!mbar_wait(FP8 ? &bars->q_conv[X] : &bars->q_full[X], q_tot & 1, status,
+                                 abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  q_ready = true;
+                  ++q_tot;
+                }
+                tc_fence_after();
+                uint64_t qb = q_d + ((X * C::TILE) >> 4);
+                unsigned s_t = tmem + C::s_col(X);
+                asm volatile("" : "+l"(qb), "+r"(s_t));
+                const uint64_t kb = k_d + ((st * C::TILE) >> 4);
+  #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
+                  tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&bars->s_full[X]);
+                if (X == 1 || !subB.active(kt)) tc_commit(&bars->k_empty[st]);
+              }
+            }
+            // every S of this item is issued: its Q tiles may be replaced
+            if (ok && j == n_union - 1) tc_commit(&bars->q_empty);
+          }
+          jg += n_union;
+        }
+        // No MMA may still be running when TMEM is released (matters only when
+        // a role gave up on a wait).
+        if (issued) {
+          tc_commit(&bars->drain);
+          mbar_wait(&bars->drain, 0, status, nullptr);
+        }
       }
     }
   } else if (HELP && warp == 11) {
@@ -955,12 +1090,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             break;
           }
           if (row >= vz_row) {
-            unsigned char* vrow = sV + st * C::TILE + row * 128;
+            // key `row` of the tile: group row / V_ROWS, row row % V_ROWS of
+            // each of its d halves
+            constexpr int V_ROWS = v_rows<FP8>();
+            unsigned char* vrow = sV + st * C::TILE + (row / V_ROWS) * (C::DH * V_ROWS * 128) +
+                                  (row % V_ROWS) * 128;
 #pragma unroll
             for (int dh = 0; dh < C::DH; ++dh)
 #pragma unroll
               for (int b = 0; b < 128; b += 16)
-                *reinterpret_cast<uint4*>(vrow + dh * C::HALF + b) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(vrow + dh * V_ROWS * 128 + b) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
@@ -1065,11 +1204,12 @@ static int prefill_sms() {
   return counts[dev];
 }
 
-template <int D, bool HALF, bool FP8>
-cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+template <int D, bool HALF, bool FP8, bool TWO>
+cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                             const CUtensorMap& v_map,
                              unsigned grid) {
   using C = PrefillCfg<D>;
-  auto k = prefill_kernel<D, HALF, FP8>;
+  auto k = prefill_kernel<D, HALF, FP8, TWO>;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, k);
   if (e != cudaSuccess) return e;
@@ -1085,25 +1225,28 @@ cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const C
   // definition gives).  out_scale is the V scale of an e4m3 cache.
   const float sl2 = fmaxf(p.scale * LOG2E * (FP8 ? p.k_scale : 1.f), 1e-30f);
   const float out_scale = FP8 ? p.v_scale : 1.f;
-  k<<<grid, PF_THREADS, C::SMEM, p.stream>>>(p, q_map, kv_map, sl2, out_scale);
+  k<<<grid, PF_THREADS, C::SMEM, p.stream>>>(p, q_map, k_map, v_map, sl2, out_scale);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& kv_map) {
+cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                           const CUtensorMap& v_map) {
   const int NP = (p.G % 2 == 0) ? p.H / 2 : p.H;
   // Persistent grid: one CTA per SM (the shared memory and the 512 TMEM
   // columns of one CTA fill an SM), capped by the host-side bound on items.
   const long long items = static_cast<long long>(p.max_tiles) * NP * p.kv_chunks;
   if (items == 0) return cudaSuccess;
   const unsigned g = static_cast<unsigned>(std::min<long long>(items, prefill_sms()));
+  // A 16-bit cache takes two MMA issuers (measured against one: varlen prefill
+  // 1.279 -> 1.199 ms, the mixed chunked-prefill step 1.149 -> 1.108 ms).
   if (p.kv_dtype == PATTN_KV_F16)
-    return p.D == 128 ? launch_prefill_t<128, true, false>(p, q_map, kv_map, g)
-                      : launch_prefill_t<64, true, false>(p, q_map, kv_map, g);
+    return p.D == 128 ? launch_prefill_t<128, true, false, true>(p, q_map, k_map, v_map, g)
+                      : launch_prefill_t<64, true, false, true>(p, q_map, k_map, v_map, g);
   if (p.kv_dtype == PATTN_KV_FP8_E4M3)
-    return p.D == 128 ? launch_prefill_t<128, false, true>(p, q_map, kv_map, g)
-                      : launch_prefill_t<64, false, true>(p, q_map, kv_map, g);
-  return p.D == 128 ? launch_prefill_t<128, false, false>(p, q_map, kv_map, g)
-                    : launch_prefill_t<64, false, false>(p, q_map, kv_map, g);
+    return p.D == 128 ? launch_prefill_t<128, false, true, false>(p, q_map, k_map, v_map, g)
+                      : launch_prefill_t<64, false, true, false>(p, q_map, k_map, v_map, g);
+  return p.D == 128 ? launch_prefill_t<128, false, false, true>(p, q_map, k_map, v_map, g)
+                    : launch_prefill_t<64, false, false, true>(p, q_map, k_map, v_map, g);
 }
 
 }  // namespace pattn
