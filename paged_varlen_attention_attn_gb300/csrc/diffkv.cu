@@ -326,11 +326,16 @@ cudaError_t launch_generic(const Problem& p, int dk, int dv, bool skip_decode) {
 // Rows with query_len > 1 on the generic kernel (when the batch may have
 // them), then the decode rows on the tensor-core kernel; head sizes that are
 // not multiples of 64 run every row on the generic kernel.
+// The decode kernel is the clearing kernel's programmatic dependent only when
+// it follows that kernel directly (p.pdl_launch / pdl_wait from the caller).
 cudaError_t launch_diffkv(const Problem& p, int dk, int dv) {
   if (!diffkv_decode_supported(dk, dv)) return launch_generic(p, dk, dv, false);
   if (p.max_q > 1) {
     const cudaError_t e = launch_generic(p, dk, dv, true);
     if (e != cudaSuccess) return e;
+    Problem after = p;
+    after.pdl_launch = after.pdl_wait = 0;
+    return launch_diffkv_decode(after, dk, dv);
   }
   return launch_diffkv_decode(p, dk, dv);
 }

@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(DKD_THREADS, 2)
   // wrote), so the grid's ragged end holds the short ones.
   const int P = p.splits;
   const int rank = static_cast<int>(blockIdx.y) / P, sp = static_cast<int>(blockIdx.y) % P;
+  // In a decode-only call the clearing kernel before this one may still be
+  // running (this kernel is its programmatic dependent): wait for it before
+  // the decode order, the status word and the counters it writes.
+  if (p.pdl_wait) grid_dep_wait();
   const int r = p.decode_order ? p.decode_order[rank] : rank;
   const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -473,9 +477,23 @@ cudaError_t launch_t(const Problem& p, const CUtensorMap& kmap, const CUtensorMa
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const float sl2 = fmaxf(p.scale * LOG2E, 1e-30f);
-  k<<<dim3(static_cast<unsigned>(p.Hkv),
-           static_cast<unsigned>(p.B) * static_cast<unsigned>(p.splits)),
-      DKD_THREADS, smem, p.stream>>>(p, kmap, vmap, dk, sl2);
+  const dim3 grid(static_cast<unsigned>(p.Hkv),
+                  static_cast<unsigned>(p.B) * static_cast<unsigned>(p.splits));
+  if (p.pdl_launch) {
+    // programmatic dependent of the previous kernel in the stream
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(DKD_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = p.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p, kmap, vmap, dk, sl2);
+  }
+  k<<<grid, DKD_THREADS, smem, p.stream>>>(p, kmap, vmap, dk, sl2);
   return cudaGetLastError();
 }
 

@@ -477,6 +477,9 @@ pattn_status_t diffkv_fwd(const void* q, const void* kv_cache, const int32_t* bl
   p.lse_part = reinterpret_cast<float*>(ws + L.lse_off);
   p.splits = splits;
   p.stream = static_cast<cudaStream_t>(ext->stream);
+  // the decode kernel follows the clearing kernel as its programmatic
+  // dependent (unless the caller records events between the kernels)
+  p.pdl_launch = p.pdl_wait = (ext->timing_events == nullptr) ? 1 : 0;
   // clears the status word and orders the requests longest decode first (the
   // decode grid's order), then the kernels run
   if (launch_decode_prep(p) != cudaSuccess) return PATTN_ERR_CUDA;
