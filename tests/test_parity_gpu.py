@@ -103,6 +103,20 @@ def test_prefill_noncausal():
     check_case(make(spec))
 
 
+@pytest.mark.parametrize("H,Hkv,D,window", [(3, 1, 128, 0), (6, 2, 64, 0), (3, 3, 128, 200),
+                                             (5, 1, 128, 96), (1, 1, 64, 0)])
+def test_prefill_odd_group_row_tile_pairs(H, Hkv, D, window):
+    # An odd GQA ratio makes a work item two consecutive 128-row tiles of one
+    # head, whose key ranges differ (the second tile's causal range reaches one
+    # tile further, and under a window the first one's starts earlier): one
+    # sub-tile has no MMAs for some key tiles of the item, and the two MMA
+    # issuers still take turns over every tile.  Rows span several tile pairs
+    # with ragged tails, and single-tile items leave the second sub-tile empty.
+    spec = small_spec(1000 + 37 * H + 11 * Hkv + D + window, H=H, Hkv=Hkv, d=D, bs=16,
+                      n_req=4, max_s=700, window=window, kinds=("prefill", "chunk", "decode"))
+    check_case(make(spec))
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_mixed_batches(seed):
     spec = small_spec(900 + seed, H=8, Hkv=2, d=128, bs=16, n_req=7, max_s=520,
