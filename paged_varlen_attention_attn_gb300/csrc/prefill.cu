@@ -719,28 +719,26 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               break;
             }
             tc_fence_after();
+            // Both blocks' base addresses are ready before the first MMA, so
+            // nothing but MMAs runs between them; they are made opaque so that
+            // their per-MMA offsets are added at each use instead of being
+            // hoisted out of the loops as live registers.
+            uint64_t qb = q_d + ((X * C::TILE) >> 4);
+            unsigned s_t = tmem + C::s_col(X);
+            const uint64_t kb = k_d + ((st * C::TILE) >> 4);
+            unsigned p_t = tmem + C::s_col(X);
+            unsigned o_t = tmem + C::o_col(X);
+            const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
+            asm volatile("" : "+l"(qb), "+r"(s_t), "+r"(p_t), "+r"(o_t));
             if (do_pv) {
-              // The base addresses are made opaque here so that their per-MMA
-              // offsets are added at each use instead of being hoisted out of
-              // the loops as live registers.
-              unsigned p_t = tmem + C::s_col(X);
-              unsigned o_t = tmem + C::o_col(X);
-              asm volatile("" : "+r"(p_t), "+r"(o_t));
-              const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
 #pragma unroll
               for (int kk = 0; kk < BLOCK_N / 16; ++kk)
                 tc_mma_ts(o_t, p_t + kk * 8,
                           vb + ((((kk * 16) / V_ROWS * C::DH * V_ROWS) + (kk * 16) % V_ROWS) *
                                     128 >> 4),
                           idesc_pv, (n_pv > 0 || kk > 0) ? 1u : 0u);
-              ++n_pv;
-              ++pv_tot;
             }
             if (do_s) {
-              uint64_t qb = q_d + ((X * C::TILE) >> 4);
-              unsigned s_t = tmem + C::s_col(X);
-              asm volatile("" : "+l"(qb), "+r"(s_t));
-              const uint64_t kb = k_d + ((st * C::TILE) >> 4);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
@@ -748,6 +746,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               }
             }
             mbar_arrive(&bars->tok[1 - X]);  // the other issuer's turn
+            if (do_pv) {
+              ++n_pv;
+              ++pv_tot;
+            }
             // Commits, while the other issuer's MMAs run.  Every stage of the
             // item's key tiles is released by both issuers.
             if (do_s) tc_commit(&bars->s_full[X]);
