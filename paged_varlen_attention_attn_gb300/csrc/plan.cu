@@ -37,14 +37,15 @@ __device__ __forceinline__ int tile_cost(const Problem& p, int q_len, int s, int
   return min(max(c, 0), NBUCKET - 1);
 }
 
-// Visible KV blocks of request r's decode row (its partitions' total work), or
+// Visible KV blocks of a request's decode row (its partitions' total work), or
 // 0 for a request that is not a valid decode (it does no decode work).
-__device__ __forceinline__ int decode_cost(const Problem& p, int r) {
-  const int q_len = p.qsl[r + 1] - p.qsl[r];
-  const int s = p.seq_lens[r];
+__device__ __forceinline__ int decode_cost_of(const Problem& p, int q_len, int s) {
   if (q_len != 1 || s < 1 || s > p.mbps * p.bs) return 0;
   const int k_lo = (p.window > 0) ? max(0, s - p.window) : 0;
   return min((s + p.bs - 1) / p.bs - k_lo / p.bs, NBUCKET - 1);
+}
+__device__ __forceinline__ int decode_cost(const Problem& p, int r) {
+  return decode_cost_of(p, p.qsl[r + 1] - p.qsl[r], p.seq_lens[r]);
 }
 
 // Turns hist[] (counts per cost bucket) into cursors in descending cost
@@ -94,14 +95,13 @@ __device__ int scan_descending(int* hist, int* warp_sums) {
 }
 
 // Writes p.decode_order: every request, by decreasing decode cost (a counting
-// sort; the order within one cost is whatever the atomics give).  A thread's
-// first request keeps its cost in a register between the two passes, so the
-// metadata is read once (the decode kernel waits for this).  Adds the visible
-// KV blocks of every decode row to *blocks.
+// sort; the order within one cost is whatever the atomics give).  cost0 is
+// the decode cost of the thread's first request (request tid), which the
+// caller read; a larger batch reads the rest here.  Adds the visible KV
+// blocks of every decode row to *blocks.
 __device__ void order_decodes(const Problem& p, int* hist, int* warp_sums,
-                              unsigned long long* blocks) {
+                              unsigned long long* blocks, int cost0) {
   const int tid = threadIdx.x;
-  const int cost0 = (tid < p.B) ? decode_cost(p, tid) : 0;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
   for (int r = tid; r < p.B; r += PLAN_THREADS) {
@@ -145,6 +145,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __shared__ int s_best_gs[PLAN_THREADS / 32];
   __shared__ unsigned short s_cost[NBUCKET];  // cost of sorted tile t < NBUCKET
   const int tid = threadIdx.x;
+  // Request tid's metadata is read once, here, and kept in registers for
+  // every pass (a batch of more than PLAN_THREADS requests reads the others
+  // in each pass).
+  int q_len0 = 0, s0 = 0, t00 = 0;
+  const bool ok0 = tid < p.B && request_ok(p, tid, q_len0, s0, t00);
   if (tid == 0) {
     s_tile_work = 0ull;
     s_dec_blocks = 0ull;
@@ -156,8 +161,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
 
   // Pass 1: validate requests, histogram prefill tiles by cost.
   for (int r = tid; r < p.B; r += PLAN_THREADS) {
-    int q_len, s, t0;
-    if (!request_ok(p, r, q_len, s, t0)) {
+    int q_len = q_len0, s = s0, t0 = t00;
+    if (r == tid ? !ok0 : !request_ok(p, r, q_len, s, t0)) {
       flag_status(&p.hdr->status, PATTN_DEV_BAD_METADATA);
       // Rows of a bad prefill request are written as zeros (decode rows are
       // handled by the decode kernel), clamped to the output buffer.
@@ -196,8 +201,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
 
   // Pass 2: scatter (request, q-tile) pairs to their slots.
   for (int r = tid; r < p.B; r += PLAN_THREADS) {
-    int q_len, s, t0;
-    if (!request_ok(p, r, q_len, s, t0) || q_len <= 1) continue;
+    int q_len = q_len0, s = s0, t0 = t00;
+    if ((r == tid ? !ok0 : !request_ok(p, r, q_len, s, t0)) || q_len <= 1) continue;
     const int nt = (q_len + p.rows_per_item - 1) / p.rows_per_item;
     for (int qt = 0; qt < nt; ++qt) {
       const int c = tile_cost(p, q_len, s, qt);
@@ -209,7 +214,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   __syncthreads();
 
   // Pass 3: the decode grid's request order.
-  if (p.decode_order) order_decodes(p, hist, warp_sums, &s_dec_blocks);
+  if (p.decode_order)
+    order_decodes(p, hist, warp_sums, &s_dec_blocks,
+                  tid < p.B ? decode_cost_of(p, q_len0, s0) : 0);
   __syncthreads();
 
   // Pass 4 (mixed batches): how many SMs the prefill kernel keeps.  Each
@@ -278,7 +285,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) decode_prep_kernel(const Problem
     s_dec_blocks = 0ull;
   }
   for (int i = threadIdx.x; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
-  order_decodes(p, hist, warp_sums, &s_dec_blocks);
+  order_decodes(p, hist, warp_sums, &s_dec_blocks,
+                threadIdx.x < p.B ? decode_cost(p, threadIdx.x) : 0);
 }
 
 }  // namespace
