@@ -29,9 +29,9 @@
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
 // [384,384+D).  P (bf16, 64 columns) overwrites the lower half of its S
 // buffer and is read back from TMEM as the A operand of P V; the next scores
-// of that sub-tile are issued right after P V and overwrite it.  The tensor
-// core executes one thread's MMAs in issue order, so P V has read its operand
-// before the next S writes the same columns.
+// of that sub-tile are issued right after P V, by the same thread, and
+// overwrite it.  The tensor core executes one thread's MMAs in issue order,
+// so P V has read its operand before the next S writes the same columns.
 //
 // The issue order S_A(0), S_B(0), then per key tile j: P V_A(j), S_A(j+1),
 // P V_B(j), S_B(j+1) makes the two sub-tiles ping-pong: while one softmax
@@ -40,11 +40,12 @@
 // S_X(j+1) also covers P V_X(j), so a softmax warpgroup may rescale its O in
 // TMEM as soon as it sees its next scores.
 //
-// The cache is addressed by one 4-D TMA tensor map over
-// [2 * num_blocks][block_size][num_kv_heads][head_size]; a 128-key tile is
-// 128 / block_size page loads (one partial-page load when block_size > 128),
-// each landing at its rows' offset of a 128-byte-swizzled tile -- the K-major
-// (for S) and MN-major (for P V) operand layouts the MMA descriptors name.
+// The cache is addressed through TMA tensor maps over
+// [2 * num_blocks][block_size][num_kv_heads][head_size].  A K tile is
+// 128 / block_size page loads per d half (one partial-page load when
+// block_size > 128), each landing at its rows' offset of a 128-byte-swizzled
+// column block (the K-major operand of S); a V tile is one load per page, of
+// both d halves, landing as 16-key groups (the MN-major operand of P V).
 // Pages wholly past seq_len are not loaded; V rows at or past seq_len are
 // zeroed in shared memory before P V so stale or NaN slots cannot leak
 // through 0 * NaN.  Key tiles wholly outside the causal band or the window are
