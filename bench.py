@@ -993,6 +993,13 @@ def attention_line(args, spec, world, rank, local, res):
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
+    if ph.get("prefill", 0.0) > 0 and ph.get("decode", 0.0) > 0:
+        # the two kernels timed apart (each on every SM) against the step,
+        # where they run at the same time on different SMs
+        line["co_schedule"] = {
+            "serial_ms": round(ph["prefill"] + ph["decode"], 4),
+            "step_ms": round(res["ms"], 4),
+            "overlap_ms": round(ph["prefill"] + ph["decode"] - res["ms"], 4)}
     if args.config == 1:
         line["latency_us"] = {"mean": round(res["ms"] * 1e3, 2),
                               "median": round(res["ms_median"] * 1e3, 2),
