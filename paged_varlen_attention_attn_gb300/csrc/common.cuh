@@ -283,6 +283,17 @@ __device__ __forceinline__ void tc_mma_ss(unsigned d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with 8-bit operands (kind::f8f6f4: K = 32 per MMA; both e4m3 with
+// an instruction descriptor whose A and B type fields are 0).
+__device__ __forceinline__ void tc_mma_ss_f8(unsigned d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             unsigned idesc, unsigned accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // One MMA, A from tensor memory, B from a shared memory descriptor.
 __device__ __forceinline__ void tc_mma_ts(unsigned d_tmem, unsigned a_tmem, uint64_t b_desc,
                                           unsigned idesc, unsigned accumulate) {

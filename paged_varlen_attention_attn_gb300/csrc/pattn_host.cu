@@ -157,8 +157,9 @@ pattn_status_t check_call(const void* q, const void* kv_cache, const int32_t* bl
 
 // Cost model of the co-scheduled mixed batch (measured on GB300): a prefill
 // key tile of one item (two 128-row sub-tiles, 128 keys) takes about
-// 2.1 us per SM at head size 128 (about 1.3 us at 64; e4m3 tiles about 1.3x
-// longer, for the widening); beside the prefill, one SM running two decode
+// 2.1 us per SM at head size 128 (about 1.3 us at 64; e4m3 tiles 1.1-1.4x
+// longer, for the widening: 1.3x is taken, and the mixed step's time was the
+// same for 0.95x to 1.3x); beside the prefill, one SM running two decode
 // CTAs streams about 120 GB/s of 16-bit K/V (e4m3 about 100 GB/s); decode
 // gets about 85 % of HBM beside the prefill.  (A sweep of the prefill grid
 // on the mixed workload put the best at 128 of 152 SMs, which these figures
@@ -303,15 +304,19 @@ bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, 
   if (!enc) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   if (kv_dtype == PATTN_KV_FP8_E4M3) {
-    // e4m3 rows land unswizzled in the prefill kernel's staging buffer (its
-    // producers widen them into the swizzled f16 layout).
+    // e4m3 rows: for the prefill kernel's 8-bit score MMAs (d 128, v_groups
+    // false) in the 128-byte-swizzled K-major layout; otherwise unswizzled,
+    // into the ring stage where the producers widen them to the swizzled f16
+    // layout.
+    const bool sw = !v_groups && D == 128;
     const cuuint64_t row = static_cast<cuuint64_t>(D);
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                           static_cast<cuuint64_t>(bs), 2ull * static_cast<cuuint64_t>(NB)};
     cuuint64_t strides[3] = {row, row * Hkv, row * Hkv * bs};
     cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows), 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv_cache), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               sw ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   }
   const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
@@ -338,18 +343,14 @@ bool encode_kv_map(CUtensorMap* map, const void* kv_cache, int kv_dtype, int D, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The three maps of a prefill launch: q, the K copies and the V copies (the
-// same map for an e4m3 cache).
+// The three maps of a prefill launch: q, the K copies and the V copies.  An
+// e4m3 cache's V copies (and its K copies at d 64) take the unswizzled rows.
 bool encode_prefill_maps(CUtensorMap* qmap, CUtensorMap* kmap, CUtensorMap* vmap, const void* q,
                          const void* kv_cache, int kv_dtype, int H, int D, int T, int Hkv, int bs,
                          int NB) {
   const int rows = std::min(bs, BLOCK_N);
   if (!encode_q_map(qmap, q, kv_dtype, H, D, T)) return false;
   if (!encode_kv_map(kmap, kv_cache, kv_dtype, D, Hkv, bs, NB, rows, false)) return false;
-  if (kv_dtype == PATTN_KV_FP8_E4M3) {
-    *vmap = *kmap;
-    return true;
-  }
   return encode_kv_map(vmap, kv_cache, kv_dtype, D, Hkv, bs, NB, rows, true);
 }
 

@@ -15,17 +15,23 @@
 // longest-first list, so one item's loads and first scores overlap the end of
 // the previous one instead of a CTA launch, set-up and drain.  Twelve warps:
 //   warps 0-3  softmax + epilogue of sub-tile A, thread i owns row i (TMEM lane i)
-//              (over an e4m3 cache they also convert their Q tile to f16)
+//              (over an e4m3 cache they also split (d 128) or convert (d 64)
+//              their Q tile, below)
 //   warps 4-7  softmax + epilogue of sub-tile B, likewise
 //   warp  8    TMA producer of both Q tiles of each item and the K tiles, page by
 //              page through block_table into a 3-stage ring, one lane per
-//              page copy (over an e4m3 cache it also widens each K tile)
-//   warp  9    MMA issuer (one thread): sub-tile A's MMAs over a 16-bit
-//              cache, both sub-tiles' over an e4m3 cache
+//              page copy (over an e4m3 cache at d 64 it also widens each K tile)
+//   warp  9    MMA issuer (one thread): sub-tile A's MMAs (both sub-tiles'
+//              over an e4m3 cache at d 64)
 //   warp 10    TMA producer of the V tiles (2-stage ring), one page per copy
-//   warp 11    MMA issuer of sub-tile B over a 16-bit cache (the two issuers
-//              take turns); over an e4m3 cache at d 128 it widens the last 48
-//              rows of each K and V tile, at d 64 it is idle
+//              (over an e4m3 cache it also widens each V tile to f16)
+//   warp 11    MMA issuer of sub-tile B (the two issuers take turns); idle
+//              over an e4m3 cache at d 64
+// Over an e4m3 cache at d 128 the scores are 8-bit MMAs (kind::f8f6f4) on the
+// cache's K codes as TMA lands them: each softmax thread splits its bf16 Q row,
+// scaled by a power of two, into e4m3 hi and lo codes whose sum is the scaled
+// row, and S is hi K^T + lo K^T in fp32 (exact products), scaled back in the
+// softmax.  P V stays an f16 MMA on widened V tiles.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B
 // [384,384+D).  P (bf16, 64 columns) overwrites the lower half of its S
 // buffer and is read back from TMEM as the A operand of P V; the next scores
@@ -76,8 +82,12 @@ static_assert(2 * 128 * softmax_regs(true) + 128 * other_regs(true) == SPLIT_REG
               "both register splits fit the same launch allocation");
 // K and V rings: K gets the extra stage because the next scores need it
 // before the next P V needs V.  224 KB of shared memory at head size 128.
+// Over an e4m3 cache at d 128 a K stage holds the 16 KB of codes only, and
+// the space saved gives V (widened in place, after its copy lands) a third
+// stage, so its copies run two tiles ahead of the widening.
 constexpr int PF_KST = 3;
 constexpr int PF_VST = 2;
+constexpr int PF_VST_MAX = 3;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 // 2^RESCALE_THRESHOLD: if any of a row's weights against an unmoved
 // reference exceeds it, so does their sum; a sum above this sends the tile
@@ -93,18 +103,21 @@ constexpr unsigned FULL = 0xffffffffu;
 template <bool FP8>
 __host__ __device__ constexpr int v_rows() { return FP8 ? BLOCK_N : 16; }
 
-template <int D>
+// NK: e4m3 K codes used as they are (an e4m3 cache at d 128).
+template <int D, bool NK = false>
 struct PrefillCfg {
   static constexpr int DH = D / 64;                 // 128-byte column blocks
   static constexpr int HALF = BLOCK_M * 128;        // bytes of one 128-row column block
   static constexpr int TILE = DH * HALF;            // bytes of a Q, K or V tile
+  static constexpr int KSTAGE = NK ? BLOCK_N * D : TILE;  // bytes of a K ring stage
+  static constexpr int VST = NK ? PF_VST_MAX : PF_VST;    // V ring stages
   // An e4m3 K or V tile (rows of D bytes) lands at the top of its ring stage
   // and is widened there, in place, to the f16 tile.
   static constexpr int SRC8 = TILE - BLOCK_N * D;
   static constexpr int Q_OFF = 0;                   // two Q tiles
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
-  static constexpr int V_OFF = K_OFF + PF_KST * TILE;
-  static constexpr int BAR_OFF = V_OFF + PF_VST * TILE;
+  static constexpr int V_OFF = K_OFF + PF_KST * KSTAGE;
+  static constexpr int BAR_OFF = V_OFF + VST * TILE;
   // + barriers + alignment slack; at least 116 KB so one CTA holds an SM (and
   // its 512 TMEM columns) alone
   static constexpr int SMEM_RAW = BAR_OFF + 512 + 1024;
@@ -117,12 +130,12 @@ struct PrefillCfg {
 struct Bars {
   uint64_t q_full[2];
   uint64_t k_full[PF_KST];
-  uint64_t v_full[PF_VST];
+  uint64_t v_full[PF_VST_MAX];
   uint64_t k_empty[PF_KST];
-  uint64_t v_empty[PF_VST];
+  uint64_t v_empty[PF_VST_MAX];
   uint64_t s_full[2];   // one phase per key tile of sub-tile X
   uint64_t k_land[PF_KST];  // e4m3 K tile landed at the top of its stage (FP8)
-  uint64_t v_land[PF_VST];  // e4m3 V tile landed at the top of its stage (FP8)
+  uint64_t v_land[PF_VST_MAX];  // e4m3 V tile landed at the top of its stage (FP8)
   uint64_t q_conv[2];   // Q tile of sub-tile X converted to f16 by its warpgroup (FP8)
   uint64_t p_full[2];
   uint64_t o_final[2];  // the last P V of sub-tile X
@@ -262,6 +275,88 @@ __device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w) {
   return *reinterpret_cast<const unsigned*>(&h);
 }
 
+// f16x2 -> two e4m3 codes (low half -> low byte), round to nearest, saturating.
+__device__ __forceinline__ unsigned f16x2_to_e4m3x2(unsigned h) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+  return r;
+}
+
+// A bf16 pair (w), times sc = 2^k, as e4m3 hi and lo codes with hi + lo equal
+// to the scaled pair: hi rounds the 8-bit significand to 4 bits, and the
+// remainder (at most 4 significant bits, exact in f16) is lo.  Exact while the
+// scaled value's remainder is no finer than e4m3's smallest step (2^-9).
+__device__ __forceinline__ void split_pair(unsigned w, float sc, unsigned& hi, unsigned& lo) {
+  const __half2 y = __floats2half2_rn(__uint_as_float(w << 16) * sc,
+                                      __uint_as_float(w & 0xffff0000u) * sc);
+  const unsigned yb = *reinterpret_cast<const unsigned*>(&y);
+  hi = f16x2_to_e4m3x2(yb);
+  const unsigned hb = e4m3x2_to_f16x2(hi);
+  const __half2 r = __hsub2(y, *reinterpret_cast<const __half2*>(&hb));
+  lo = f16x2_to_e4m3x2(*reinterpret_cast<const unsigned*>(&r));
+}
+
+// An e4m3 call at d 128 computes the scores with 8-bit MMAs straight from the
+// cache's K codes.  Q (bf16, as TMA loaded it: two 128-byte-swizzled d halves)
+// is split in place, once its copy has landed (q_full at `parity`), into two
+// e4m3 tiles, hi over d half 0's bytes and lo over d half 1's, each 128 rows of
+// 128 codes in the 128-byte-swizzled K-major layout.  Thread t of the softmax
+// warpgroup takes row t (the row whose scores it owns): it reads the whole row
+// before writing it, so no other thread's bytes are touched.  The row is
+// scaled by the power of two sc that puts its largest magnitude in [128, 256)
+// (exact), so q = (hi + lo) / sc wherever a value sits within 2^9 of the row
+// maximum (below that its error is under 2^-16 of the maximum); `inv` returns
+// 1 / sc, by which the row's scores are scaled back.  Each warp then arrives
+// on q_conv.
+__device__ __forceinline__ bool split_q_tile(unsigned char* q, uint64_t* q_full, uint64_t* q_conv,
+                                             unsigned parity, int t, unsigned* status,
+                                             volatile int* abort_flag, float& inv) {
+  if (!__all_sync(0xffffffffu, mbar_wait(q_full, parity, status, abort_flag))) return false;
+  constexpr int HALF = BLOCK_M * 128;
+  unsigned char* row = q + t * 128;
+  const int sw = t & 7;
+  uint4 w[16];  // chunk c of d half h (elements 64h + 8c ... + 7) at w[8h + c]
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = *reinterpret_cast<const uint4*>(row + (i >> 3) * HALF + (((i & 7) ^ sw) << 4));
+  // bf16 magnitudes compare as unsigned integers once the sign bit is cleared
+  unsigned m_lo = 0, m_hi = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const unsigned v[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      m_lo = max(m_lo, v[e] & 0x7fffu);
+      m_hi = max(m_hi, v[e] & 0x7fff0000u);
+    }
+  }
+  const int eb = static_cast<int>(max(m_lo, m_hi >> 16) >> 7);  // exponent field of the max
+  const int k = min(126, max(-126, 134 - eb));  // max * 2^k in [2^7, 2^8)
+  const float sc = __int_as_float((k + 127) << 23);
+  inv = __int_as_float((127 - k) << 23);
+  // code chunk c (elements 16c ... 16c + 15) comes from bf16 chunks 2(c % 4)
+  // and 2(c % 4) + 1 of d half c / 4
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 a = w[8 * (c >> 2) + 2 * (c & 3)], b = w[8 * (c >> 2) + 2 * (c & 3) + 1];
+    const unsigned v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    unsigned hi[8], lo[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) split_pair(v[e], sc, hi[e], lo[e]);
+    const int pos = (c ^ sw) << 4;
+    *reinterpret_cast<uint4*>(row + pos) =
+        make_uint4(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16),
+                   hi[6] | (hi[7] << 16));
+    *reinterpret_cast<uint4*>(row + HALF + pos) =
+        make_uint4(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16), lo[4] | (lo[5] << 16),
+                   lo[6] | (lo[7] << 16));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if ((t & 31) == 0) mbar_arrive(q_conv);
+  return true;
+}
+
 // (s0, s1) += (a0, a1)
 __device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) {
   asm("{\n\t.reg .b64 ra, rb;\n\t"
@@ -374,14 +469,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ Problem p, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, float sl2, float out_scale) {
-  using C = PrefillCfg<D>;
-  constexpr bool MMA_F16 = HALF || FP8;  // operand and P type of the MMAs
-  // e4m3 at d 128: warp 11 widens rows [HELP_ROW, BLOCK_N) of every K and V
-  // tile, the producers rows [0, HELP_ROW) (10 KB and 12 KB of f16 a tile
-  // instead of 16 KB for each producer, on three SM sub-partitions)
-  constexpr bool HELP = FP8 && D == 128;
-  static_assert(!(TWO && FP8), "an e4m3 call has one MMA issuer (warp 11 widens tiles)");
-  constexpr int HELP_ROW = 80;
+  // e4m3 at d 128: the score MMAs read the cache's K codes as they are (8-bit
+  // MMAs against the split Q), so only V tiles are widened
+  constexpr bool NK = FP8 && D == 128;
+  using C = PrefillCfg<D, NK>;
+  constexpr bool MMA_F16 = HALF || FP8;  // operand and P type of the P V MMAs
+  constexpr int VST = C::VST;
+  constexpr int V_SPLIT = 80;  // NK: first V row that warp 8 widens
+  static_assert(!(FP8 && D != 128 && TWO), "an e4m3 call at d 64 has one MMA issuer");
+  static_assert(!NK || TWO, "the 8-bit score MMAs are issued by the two-issuer loop");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -413,20 +509,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(&bars->p_full[i], BLOCK_M);
       mbar_init(&bars->o_final[i], 1);
     }
-    // an e4m3 d 128 stage is announced by its producer and by warp 11
     for (int i = 0; i < PF_KST; ++i) {
-      mbar_init(&bars->k_full[i], HELP ? 2 : 1);
+      mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], TWO ? 2 : 1);
     }
-    for (int i = 0; i < PF_VST; ++i) {
-      mbar_init(&bars->v_full[i], HELP ? 2 : 1);
+    // an e4m3 V tile at d 128 is announced by both producers (each widens
+    // part of it)
+    for (int i = 0; i < VST; ++i) {
+      mbar_init(&bars->v_full[i], NK ? 2 : 1);
       mbar_init(&bars->v_empty[i], TWO ? 2 : 1);
     }
     mbar_init(&bars->q_empty, TWO ? 2 : 1);
     mbar_init(&bars->tok[0], 1);
     mbar_init(&bars->tok[1], 1);
     for (int i = 0; i < PF_KST; ++i) mbar_init(&bars->k_land[i], 1);
-    for (int i = 0; i < PF_VST; ++i) mbar_init(&bars->v_land[i], 1);
+    for (int i = 0; i < VST; ++i) mbar_init(&bars->v_land[i], 1);
     mbar_init(&bars->q_conv[0], 4);  // one arrival per warp of the softmax warpgroup
     mbar_init(&bars->q_conv[1], 4);
     mbar_init(&bars->drain, TWO ? 2 : 1);
@@ -461,16 +558,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // so a tile costs one copy instruction, not 2 x pages of them in one
     // thread.
     const int kv = (warp == 10) ? 1 : 0;
-    const int nst = kv ? PF_VST : PF_KST;
+    const int nst = kv ? VST : PF_KST;
     unsigned char* ring = kv ? sV : sK;
-    // Copy `lane` of a tile: a K copy is page lane / DH, d half lane % DH; a
-    // 16-bit V copy is the whole of page lane (its rows_box / 16 groups).
+    const int stage_bytes = kv ? C::TILE : C::KSTAGE;
+    // Copy `lane` of a tile: a K copy is page lane / DH, d half lane % DH (an
+    // e4m3 K tile at d 128 is one 128-byte column block: DHK = 1); a 16-bit V
+    // copy is the whole of page lane (its rows_box / 16 groups).
+    constexpr int DHK = NK ? 1 : C::DH;
     const bool v16 = kv && !FP8;
-    const int my_pg = v16 ? lane : lane / C::DH, my_dh = v16 ? 0 : lane % C::DH;
+    const int my_pg = v16 ? lane : lane / DHK, my_dh = v16 ? 0 : lane % DHK;
+    // the tiles this warp copies as they are (else as e4m3 rows to be widened)
+    const bool direct = !FP8 || (NK && kv == 0);
     if (kv == 0 && lane == 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
-      if (!FP8) tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&vmap);
     }
     int jg = 0;        // key tiles streamed so far (ring position)
     int n_worked = 0;  // items with at least one key tile so far
@@ -529,7 +631,59 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         return blk;
       };
-      if constexpr (!FP8) {
+      if (NK && kv == 0) {
+        // e4m3 at d 128: the K codes go straight to their stage (one
+        // 128-byte-swizzled column block), PF_KST - 1 tiles ahead, and
+        // between copies this warp widens rows [V_SPLIT, BLOCK_N) of each V
+        // tile (warp 10 rows [0, V_SPLIT)).  The copy of tile j + PF_KST - 1
+        // waits for the scores of tile j - 1, whose MMAs need only V tiles
+        // before j - 1, so the two jobs never wait on each other.
+        int blk_next = page_block(u0);
+        int n_issued = 0;
+        auto issue_k = [&]() {
+          const int kt = u0 + n_issued, jt = jg + n_issued;
+          const int key_base = kt * BLOCK_N;
+          const int my_blk = __shfl_sync(FULL, blk_next, lane);
+          if (n_issued + 1 < n_union) blk_next = page_block(kt + 1);
+          const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
+          const int my_key0 = key_base + lane * rows_box;
+          const int my_slot = p.bs_shift >= 0 ? (my_key0 & (p.bs - 1)) : (my_key0 % p.bs);
+          const int st = jt % PF_KST;
+          int good = 1;
+          if (lane == 0) {
+            if (jt >= PF_KST && !mbar_wait(&bars->k_empty[st], ((jt / PF_KST) - 1) & 1, status,
+                                           abort_flag))
+              good = 0;
+            else
+              mbar_arrive_expect_tx(&bars->k_full[st],
+                                    static_cast<unsigned>(n_load * rows_box * 128));
+          }
+          good = __shfl_sync(FULL, good, 0);
+          if (!good) return 0;
+          armed_end = jt + 1;
+          if (lane < n_load)
+            tma_load_4d(sK + st * C::KSTAGE + lane * rows_box * 128, &kmap, &bars->k_full[st], 0,
+                        g, my_slot, my_blk);
+          ++n_issued;
+          return 1;
+        };
+        while (ok && n_issued < min(PF_KST - 1, n_union)) ok = issue_k();
+        for (int j = 0; ok && j < n_union; ++j) {
+          if (n_issued < n_union && !(ok = issue_k())) break;
+          const int jt = jg + j, st = jt % VST;
+          if (!__all_sync(FULL, mbar_wait(&bars->v_land[st], (jt / VST) & 1, status, abort_flag))) {
+            ok = 0;
+            break;
+          }
+          const int key_base = (u0 + j) * BLOCK_N;
+          const int rows = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box) * rows_box;
+          widen_e4m3_in_place<D>(sV + st * C::TILE, V_SPLIT, max(rows, V_SPLIT), lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->v_full[st]);
+        }
+        jg += n_union;
+      } else if (direct) {
         int blk_next = page_block(u0);
         for (int j = 0; j < n_union; ++j, ++jg) {
           const int key_base = (u0 + j) * BLOCK_N;
@@ -542,7 +696,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           const int st = jg % nst;
           uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
           uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-          const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * C::DH);
+          const unsigned bytes = static_cast<unsigned>(n_load * rows_box * 128 * DHK);
           // (wait-test build: the skipped position posts no bytes and issues
           // no copy, so the MMA thread's wait for it runs out)
           const bool skip = jg == skip_pos;
@@ -557,16 +711,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           armed_end = jg + 1;
           if (my_pg < n_load && !skip) {
             if (v16)
-              tma_load_5d(ring + st * C::TILE + my_pg * (C::DH * rows_box * 128), &vmap, full, 0,
+              tma_load_5d(ring + st * stage_bytes + my_pg * (C::DH * rows_box * 128), &vmap, full, 0,
                           0, 0, g, (p.NB + my_blk) * (p.bs >> 4) + (my_slot >> 4));
             else
-              tma_load_4d(ring + st * C::TILE + my_dh * C::HALF + my_pg * rows_box * 128, &kmap,
+              tma_load_4d(ring + st * stage_bytes + my_dh * C::HALF + my_pg * rows_box * 128, &kmap,
                           full, my_dh * 64, g, my_slot, my_blk);
           }
         }
       } else {
-        // e4m3: a tile's pages land as bytes at the top of its ring stage (the
-        // last BLOCK_N x D bytes, rows of D bytes, no swizzle), where the warp
+        // e4m3 (V tiles, and K tiles at d 64): a tile's pages land as bytes
+        // at the top of its ring stage (the last BLOCK_N x D bytes, rows of D
+        // bytes, no swizzle; the map in vmap), where the warp
         // widens them in place into the swizzled f16 tile TMA would have
         // written, then announces the stage with a plain arrival.  Copies run
         // nst - 1 tiles ahead of the widening: after widening tile j the warp
@@ -590,7 +745,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           if (good && lane < n_load) {
             const int key0 = key_base + lane * rows_box;
             const int slot = p.bs_shift >= 0 ? (key0 & (p.bs - 1)) : (key0 % p.bs);
-            tma_load_4d(ring + st * C::TILE + C::SRC8 + lane * rows_box * D, &kmap, &lands[st],
+            tma_load_4d(ring + st * stage_bytes + C::SRC8 + lane * rows_box * D, &vmap, &lands[st],
                         0, g, slot, kv * p.NB + blkv);
           }
           return good;
@@ -613,9 +768,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           }
           const int key_base = (u0 + j) * BLOCK_N;
           const int n_load = min(pages_per_tile, (s - key_base + rows_box - 1) / rows_box);
-          widen_e4m3_in_place<D>(ring + st * C::TILE, 0,
-                                 HELP ? min(n_load * rows_box, HELP_ROW) : n_load * rows_box,
-                                 lane);
+          widen_e4m3_in_place<D>(ring + st * stage_bytes, 0,
+                                 NK ? min(n_load * rows_box, V_SPLIT) : n_load * rows_box, lane);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
@@ -633,8 +787,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // shared memory when the CTA frees its resources and exits.
     if (gave_up || *abort_flag) {
       if (lane == 0) {
-        uint64_t* armed = FP8 ? (kv ? bars->v_land : bars->k_land)
-                              : (kv ? bars->v_full : bars->k_full);
+        uint64_t* armed = !direct ? (kv ? bars->v_land : bars->k_land)
+                                  : (kv ? bars->v_full : bars->k_full);
         drain_armed(armed, nst, armed_end, skip_pos, status);
         if (kv == 0) {
           if (q_arms0 > 0) mbar_wait(&bars->q_full[0], (q_arms0 - 1) & 1, status, nullptr);
@@ -658,6 +812,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // the same order (over an e4m3 cache warp 11 widens tiles).
     if (lane == 0) {
       constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !MMA_F16, false);
+      // e4m3 x e4m3 (type fields 0), fp32 accumulation, both K-major
+      constexpr unsigned idesc_s8 = make_idesc_f16(BLOCK_M, BLOCK_N, false, false);
       constexpr unsigned idesc_pv = make_idesc_f16(BLOCK_M, D, !MMA_F16, true);
       // Base descriptors; a byte offset o moves the start address field by
       // o >> 4 (shared addresses stay far below the field's 256 KB range).
@@ -688,12 +844,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const int jj = jg + j;
             const bool do_pv = j >= 1 && u.active(kt - 1);  // P V for the previous key tile
             const bool do_s = j < n_union && u.active(kt);  // scores for this key tile
-            const int stp = (jj - 1) % PF_VST;
+            const int stp = (jj - 1) % VST;
             const int st = jj % PF_KST;
             // The operands, all before the turn: P and V of the previous
             // tile, K of this tile and Q.
             if (do_pv && !(mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag) &&
-                           mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status,
+                           mbar_wait(&bars->v_full[stp], ((jj - 1) / VST) & 1, status,
                                      abort_flag))) {
               ok = false;
               break;
@@ -704,7 +860,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 break;
               }
               if (!q_ready) {
-                if (!mbar_wait(&bars->q_full[X], q_tot & 1, status, abort_flag)) {
+                // an e4m3 call's Q is usable once its softmax warpgroup has split it
+                if (!mbar_wait(FP8 ? &bars->q_conv[X] : &bars->q_full[X], q_tot & 1, status,
+                               abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -726,7 +884,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // hoisted out of the loops as live registers.
             uint64_t qb = q_d + ((X * C::TILE) >> 4);
             unsigned s_t = tmem + C::s_col(X);
-            const uint64_t kb = k_d + ((st * C::TILE) >> 4);
+            const uint64_t kb = k_d + ((st * C::KSTAGE) >> 4);
             unsigned p_t = tmem + C::s_col(X);
             unsigned o_t = tmem + C::o_col(X);
             const uint64_t vb = v_d + ((stp * C::TILE) >> 4);
@@ -740,10 +898,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                           idesc_pv, (n_pv > 0 || kk > 0) ? 1u : 0u);
             }
             if (do_s) {
+              if constexpr (NK) {
+                // Q hi (d half 0's bytes) then Q lo (d half 1's), each against
+                // the K codes in four 32-code steps
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
-                tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk)
+                  tc_mma_ss_f8(s_t, qb + (((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4),
+                               kb + (((kk & 3) * 32) >> 4), idesc_s8, kk > 0 ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
+                  tc_mma_ss(s_t, qb + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+                }
               }
             }
             mbar_arrive(&bars->tok[1 - X]);  // the other issuer's turn
@@ -795,13 +962,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               bool& q_ready = X ? q_ready1 : q_ready0;
               // P V for the previous key tile
               if (j >= 1 && u.active(kt - 1)) {
-                const int stp = (jj - 1) % PF_VST;
+                const int stp = (jj - 1) % VST;
                 if (!mbar_wait(&bars->p_full[X], pv_tot & 1, status, abort_flag)) {
                   ok = false;
                   break;
                 }
                 if (!v_ready) {
-                  if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / PF_VST) & 1, status, abort_flag)) {
+                  if (!mbar_wait(&bars->v_full[stp], ((jj - 1) / VST) & 1, status, abort_flag)) {
                     ok = false;
                     break;
                   }
@@ -851,7 +1018,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 uint64_t qb = q_d + ((X * C::TILE) >> 4);
                 unsigned s_t = tmem + C::s_col(X);
                 asm volatile("" : "+l"(qb), "+r"(s_t));
-                const uint64_t kb = k_d + ((st * C::TILE) >> 4);
+                const uint64_t kb = k_d + ((st * C::KSTAGE) >> 4);
   #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                   const unsigned off = ((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4;
@@ -874,43 +1041,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
       }
     }
-  } else if (HELP && warp == 11) {
-    // ------------------------------------------------------------ e4m3 widening helper
-    // Follows the producers' tile sequence: for each key tile, K then V (the
-    // order the MMAs need them), waits for the tile's bytes, widens rows
-    // [HELP_ROW, rows) in place and adds its arrival to the stage's full
-    // barrier.  A stage is refilled only after the MMAs that read it, which
-    // wait for this arrival, so a land barrier is never two phases ahead.
-    int jg = 0;
-    bool ok = true;
-    for (int k = 0; ok && k * GS < n_items; ++k) {
-      const Item it = load_item(p, item_at(k), n_items, NP, KC);
-      const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
-      int u0;
-      const int n_union = union_tiles(subA, subB, u0);
-      if (n_union <= 0) continue;
-      for (int j = 0; ok && j < n_union; ++j) {
-        const int jt = jg + j;
-        const int key_base = (u0 + j) * BLOCK_N;
-        const int rows = min(pages_per_tile, (it.s - key_base + rows_box - 1) / rows_box) * rows_box;
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const int nst = kv ? PF_VST : PF_KST;
-          const int st = jt % nst;
-          uint64_t* land = kv ? &bars->v_land[st] : &bars->k_land[st];
-          if (!__all_sync(FULL, mbar_wait(land, (jt / nst) & 1, status, abort_flag))) {
-            ok = false;
-            break;
-          }
-          widen_e4m3_in_place<D>((kv ? sV : sK) + st * C::TILE, HELP_ROW, max(rows, HELP_ROW),
-                                 lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
-        }
-      }
-      jg += n_union;
-    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(softmax_regs(FP8)));
@@ -923,13 +1053,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int W = p.window;
     // Phases carried across items, packed in one word to spare registers:
     // bit 0 the s_full phase of this sub-tile, bit 1 its o_final phase, bits
-    // 2-3 the V ring position of the key tiles so far modulo 2 x PF_VST (a
+    // 2 and up the V ring position of the key tiles so far modulo 2 x VST (a
     // V slot's stage and parity).
-    static_assert(PF_VST == 2, "the packed V ring position assumes two stages");
+    constexpr unsigned VPOS = 2 * VST;
     unsigned ph = 0;
     bool ok = true;
     int qn = 0;             // Q tiles of this sub-tile converted so far (FP8)
     bool q_ahead = false;   // this item's Q tile was converted during the previous item
+    // Score scale of this row: sl2, over a split Q (NK) times the row's 1 / sc,
+    // kept normal so that a masked score (-inf) still maps to -inf.  Set when
+    // the item's Q tile is split (the previous item no longer needs it then).
+    float sl2r = sl2;
     Item it = load_item(p, item_at(0), n_items, NP, KC);
     for (int k = 0; ok && k * GS < n_items; ++k) {
       const Sub u = make_sub(p, it, head_pairs, X);
@@ -954,7 +1088,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       // zeroed by the first sub-tile whose P V reads it.
       const int tail_kt = (s - 1) / BLOCK_N;
       const int vz_kt = (u.active(tail_kt) && (X == 0 || !subA.active(tail_kt))) ? tail_kt : -1;
-      const unsigned vz_m = ((ph >> 2) + (tail_kt - u0)) & 3;  // its V ring position mod 4
+      // its V ring position modulo 2 x VST (used only when vz_kt >= 0, where
+      // tail_kt >= u0)
+      const unsigned vz_m = ((ph >> 2) + static_cast<unsigned>(tail_kt - u0)) % VPOS;
       const int vz_row = s - tail_kt * BLOCK_N;                  // first row to zero
       // output row of the epilogue
       const int64_t orow_i = static_cast<int64_t>(it.t0 + i) * p.H + u.h;
@@ -962,13 +1098,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;
       const int nt = u.x1 - u.x0;
       if constexpr (FP8) {
-        // an e4m3 call's Q tile becomes f16 before its first scores
+        // an e4m3 call's Q tile is split (d 128) or becomes f16 (d 64) before
+        // its first scores
         if (nt > 0 && !q_ahead) {
-          if (!convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
-                                       qn & 1, row, status, abort_flag)) {
+          float inv = 1.f;
+          if (!(NK ? split_q_tile(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X], qn & 1,
+                                  row, status, abort_flag, inv)
+                   : convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X],
+                                             &bars->q_conv[X], qn & 1, row, status,
+                                             abort_flag))) {
             ok = false;
             break;
           }
+          sl2r = fmaxf(sl2 * inv, 1e-37f);
           ++qn;
         }
         q_ahead = false;
@@ -1009,7 +1151,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           unsigned pk[BLOCK_N / 2];
 #pragma unroll
           for (int g = 0; g < BLOCK_N / 32; ++g)
-            ps += exp_piece<MMA_F16>(*reinterpret_cast<const float(*)[32]>(&sv[g * 32]), sl2,
+            ps += exp_piece<MMA_F16>(*reinterpret_cast<const float(*)[32]>(&sv[g * 32]), sl2r,
                                      m_run, *reinterpret_cast<unsigned(*)[16]>(&pk[g * 16]));
           slow = !(ps <= FAST_SUM_LIMIT);
           if (!__any_sync(FULL, slow)) {
@@ -1042,7 +1184,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           m4[0] = max3(m4[0], sv[BLOCK_N - 4], sv[BLOCK_N - 3]);
           m4[1] = max3(m4[1], sv[BLOCK_N - 2], sv[BLOCK_N - 1]);
           const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
-          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * sl2r;
           // Lazy rescale: move the reference max only when it grows by > 2^8,
           // or, for a row whose own weights summed above the limit, whenever
           // it grows (else that row would take this path on every tile).
@@ -1061,7 +1203,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
           for (int g = 0; g < BLOCK_N / 32; ++g) {
             unsigned pk[16];
-            ps += exp_piece<MMA_F16>(*reinterpret_cast<const float(*)[32]>(&sv[g * 32]), sl2,
+            ps += exp_piece<MMA_F16>(*reinterpret_cast<const float(*)[32]>(&sv[g * 32]), sl2r,
                                      ref, pk);
             tc_st16u(s_t + g * 16, pk);
           }
@@ -1087,8 +1229,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         // Zero V rows at or past seq_len before P V reads them (done by the
         // first sub-tile whose P V reads this tile).
         if (kt == vz_kt) {
-          const int st = vz_m & 1;
-          if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], vz_m >> 1, status, abort_flag))) {
+          const int st = vz_m % VST;
+          if (!__all_sync(FULL, mbar_wait(&bars->v_full[st], vz_m / VST, status, abort_flag))) {
             ok = false;
             break;
           }
@@ -1109,7 +1251,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bars->p_full[X]);
       }
-      ph = ((ph ^ (nt & 1)) & 3) | ((((ph >> 2) + n_union) & 3) << 2);
+      ph = ((ph ^ (nt & 1)) & 3) | ((((ph >> 2) + static_cast<unsigned>(n_union)) % VPOS) << 2);
       // The next item's metadata is fetched here, where the score registers
       // are dead, and lands while the epilogue runs.
       const Item nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
@@ -1118,10 +1260,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         // last S MMA is done: convert it now, while the last P V runs, so
         // the next item's first scores need not wait for the epilogue.
         if (ok && make_sub(p, nxt, head_pairs, X).x1 > make_sub(p, nxt, head_pairs, X).x0) {
-          if (!convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
-                                       qn & 1, row, status, abort_flag)) {
+          float inv = 1.f;
+          if (!(NK ? split_q_tile(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X], qn & 1,
+                                  row, status, abort_flag, inv)
+                   : convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X],
+                                             &bars->q_conv[X], qn & 1, row, status,
+                                             abort_flag))) {
             ok = false;
           } else {
+            sl2r = fmaxf(sl2 * inv, 1e-37f);
             ++qn;
             q_ahead = true;
           }
@@ -1211,7 +1358,7 @@ template <int D, bool HALF, bool FP8, bool TWO>
 cudaError_t launch_prefill_t(const Problem& p, const CUtensorMap& q_map, const CUtensorMap& k_map,
                              const CUtensorMap& v_map,
                              unsigned grid) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, FP8 && D == 128>;
   auto k = prefill_kernel<D, HALF, FP8, TWO>;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, k);
@@ -1245,8 +1392,10 @@ cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUt
   if (p.kv_dtype == PATTN_KV_F16)
     return p.D == 128 ? launch_prefill_t<128, true, false, true>(p, q_map, k_map, v_map, g)
                       : launch_prefill_t<64, true, false, true>(p, q_map, k_map, v_map, g);
+  // An e4m3 cache at d 128 takes two as well (its score MMAs read the K codes
+  // directly, so warp 11 no longer widens); at d 64 one.
   if (p.kv_dtype == PATTN_KV_FP8_E4M3)
-    return p.D == 128 ? launch_prefill_t<128, false, true, false>(p, q_map, k_map, v_map, g)
+    return p.D == 128 ? launch_prefill_t<128, false, true, true>(p, q_map, k_map, v_map, g)
                       : launch_prefill_t<64, false, true, false>(p, q_map, k_map, v_map, g);
   return p.D == 128 ? launch_prefill_t<128, false, false, true>(p, q_map, k_map, v_map, g)
                     : launch_prefill_t<64, false, false, true>(p, q_map, k_map, v_map, g);

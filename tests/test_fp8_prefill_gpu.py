@@ -1,12 +1,13 @@
 """GPU parity of e4m3 caches with prefill rows: the decode rows run on the
 decode kernel and the prefill rows (full and chunked prefills) on the
-tensor-core prefill kernel, which widens the codes to f16 in shared memory
-and applies the per-tensor scales.  Compared with the float64 oracle at the
-e4m3 tolerance: head sizes 64 and 128, even and odd GQA ratios, a sliding
-window, block sizes 64, 128 and 256 (pages of a key tile or more), attention
-sinks, a batch of chunked prefills beside many decodes, and a prefill
-request whose query is longer than its sequence (reported, rows zero,
-others exact)."""
+tensor-core prefill kernel, which at head size 128 takes the K codes into
+8-bit score MMAs against a split Q and widens V to f16 in shared memory (at
+64 it widens both), and applies the per-tensor scales.  Compared with the
+float64 oracle at the e4m3 tolerance: head sizes 64 and 128, even and odd GQA
+ratios, a sliding window, block sizes 64, 128 and 256 (pages of a key tile or
+more), attention sinks, a batch of chunked prefills beside many decodes, a
+prefill request whose query is longer than its sequence (reported, rows zero,
+others exact), and query rows whose magnitudes span 2^-40 to 2^8."""
 import numpy as np
 import pytest
 import torch
@@ -102,3 +103,25 @@ def test_query_longer_than_its_sequence():
         x, y = int(qsl[r]), int(qsl[r + 1])
         if y > x:
             assert_close(out[x:y].float().cpu().numpy(), ref[x:y], W.KV_FP8_E4M3)
+
+
+def test_query_rows_of_very_different_magnitudes():
+    # At head size 128 the scores are 8-bit MMAs on the K codes against a Q
+    # split per row into e4m3 hi + lo codes after a power-of-two scaling; rows
+    # scaled from 2^-40 to 2^8 (and rows with one large entry among small
+    # ones) must still match the definition.  (Larger rows would give scores
+    # whose log2-domain magnitude, above ~2^20, an fp32 softmax cannot resolve
+    # to a unit: a limit of every path, not of the split.)
+    sp = small_spec(1880, H=8, Hkv=2, d=128, bs=16, n_req=4, max_s=400, kinds=("prefill",),
+                    kv_dtype=W.KV_FP8_E4M3)
+    case = W.make_case(sp, device=DEV)
+    T, H, D = case.q.shape
+    g = torch.Generator().manual_seed(1880)
+    e = torch.randint(-40, 9, (T, H, 1), generator=g).float()
+    q = case.q.float() * torch.pow(2.0, e).to(DEV)
+    spike = torch.rand(T, H, generator=g).to(DEV) < 0.25
+    col = torch.randint(0, D, (T, H), generator=g).to(DEV)
+    q[spike] = q[spike] * 1e-4
+    q[spike, col[spike]] = 300.0 * torch.sign(torch.randn(int(spike.sum()), device=DEV))
+    case.q.copy_(q.to(case.q.dtype))
+    _check(case, _gpu(case))
