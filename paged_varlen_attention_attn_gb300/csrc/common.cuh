@@ -216,6 +216,55 @@ __device__ __forceinline__ void ldsm_x4_t(unsigned addr, unsigned& r0, unsigned&
 }
 
 // D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate.
+// D += A B on e4m3 operands: m16n8k32, A 16 x 32 row-major (four registers of
+// four codes), B 32 x 8 column-major (two registers), fp32 accumulation.
+__device__ __forceinline__ void mma_16832_e4m3(float (&d)[4], unsigned a0, unsigned a1,
+                                               unsigned a2, unsigned a3, unsigned b0,
+                                               unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (the low 16 bits of v) -> f16x2, exactly (the hardware pair
+// conversion; every e4m3 value is an f16 value).
+__device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
+  unsigned r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
+  return r;
+}
+
+// f16x2 -> two e4m3 codes (low half -> low byte), round to nearest, saturating.
+__device__ __forceinline__ unsigned f16x2_to_e4m3x2(unsigned h) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+  return r;
+}
+
+// A bf16 pair (w), times sc = 2^k, as e4m3 hi and lo codes with hi + lo equal
+// to the scaled pair: hi rounds the 8-bit significand to 4 bits, and the
+// remainder (at most 4 significant bits, exact in f16) is lo.  Exact while the
+// scaled value's remainder is no finer than e4m3's smallest step (2^-9).
+__device__ __forceinline__ void split_pair(unsigned w, float sc, unsigned& hi, unsigned& lo) {
+  const __half2 y = __floats2half2_rn(__uint_as_float(w << 16) * sc,
+                                      __uint_as_float(w & 0xffff0000u) * sc);
+  const unsigned yb = *reinterpret_cast<const unsigned*>(&y);
+  hi = f16x2_to_e4m3x2(yb);
+  const unsigned hb = e4m3x2_to_f16x2(hi);
+  const __half2 r = __hsub2(y, *reinterpret_cast<const __half2*>(&hb));
+  lo = f16x2_to_e4m3x2(*reinterpret_cast<const unsigned*>(&r));
+}
+
+// The power of two 2^k that puts a bf16 magnitude with exponent field eb in
+// [2^7, 2^8) (k clamped to +-126), and its inverse.
+__device__ __forceinline__ void split_scale(int eb, float& sc, float& inv) {
+  const int k = min(126, max(-126, 134 - eb));
+  sc = __int_as_float((k + 127) << 23);
+  inv = __int_as_float((127 - k) << 23);
+}
+
 template <bool F16>
 __device__ __forceinline__ void mma_16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2,
                                           unsigned a3, unsigned b0, unsigned b1) {

@@ -352,31 +352,71 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
   // each lane reads its K bytes contiguously and widens whole words: k-step
   // kk, fragment columns 2*c4, 2*c4+1, 2*c4+8, 2*c4+9 map to d = base,
   // base + 1, base + 2, base + 3 with base = c4*D/4 + 4kk (the two 16-bit
-  // halves of the word holding d = base..base+3).
+  // halves of the word holding d = base..base+3).  There the f16 MMAs take q
+  // in f16: each head's row is first scaled by the power of two sc that puts
+  // its largest magnitude in [2^7, 2^8), so no bf16 value leaves f16's range
+  // (exact down to 2^-21 of the row maximum), and its scores are scaled back
+  // by 1 / sc with the score scale.
   unsigned qb[D / 16][NT][2];
+  float sl2h[NT][2];  // score scale of the lane's head columns 2*c4, 2*c4 + 1
   {
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
                                 (static_cast<int64_t>(t0) * p.H + g * G) * D;
+    if constexpr (FP8) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
+      for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + quad;
+        // this lane's D/4 values of the head's row: d = c4*D/4 + 8i .. + 7 in w[i]
+        uint4 w[D / 32];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int i = 0; i < D / 32; ++i)
+          w[i] = (head < G) ? *reinterpret_cast<const uint4*>(qrow + head * D + c4 * (D / 4) + 8 * i)
+                            : make_uint4(0, 0, 0, 0);
+        // the row's largest magnitude over its four lanes (bf16 magnitudes
+        // compare as unsigned integers once the sign bit is cleared)
+        unsigned m = 0;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int head = nt * 8 + quad;
-          unsigned v = 0;
-          if (head < G) {
-            if constexpr (FP8) {
-              // d = base + 2e and base + 2e + 1, base = c4*D/4 + 4kk
-              const __nv_bfloat16* qd = qrow + head * D + c4 * (D / 4) + 4 * kk + 2 * e;
-              v = pack2<true>(__bfloat162float(qd[0]), __bfloat162float(qd[1]));
-            } else {
-              const int d = kk * 16 + 2 * c4 + e * 8;
-              v = *reinterpret_cast<const unsigned*>(qrow + head * D + d);
-            }
-          }
-          qb[kk][nt][e] = v;
+        for (int i = 0; i < D / 32; ++i) {
+          const unsigned v[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m = max(m, max(v[e] & 0x7fffu, (v[e] >> 16) & 0x7fffu));
         }
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        float sc, inv;
+        split_scale(static_cast<int>(m >> 7), sc, inv);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            // d = base + 2e and base + 2e + 1 (word 2kk + e of the lane's range)
+            const uint4& wi = w[(2 * kk + e) >> 2];
+            const int c = (2 * kk + e) & 3;
+            const unsigned x = c == 0 ? wi.x : c == 1 ? wi.y : c == 2 ? wi.z : wi.w;
+            qb[kk][nt][e] = pack2<true>(__uint_as_float(x << 16) * sc,
+                                        __uint_as_float(x & 0xffff0000u) * sc);
+          }
+        // the scales of the lane's output head columns (kept normal, so that
+        // a masked score still maps to -inf)
+        const float i0 = __shfl_sync(0xffffffffu, inv, (2 * c4) * 4);
+        const float i1 = __shfl_sync(0xffffffffu, inv, (2 * c4 + 1) * 4);
+        sl2h[nt][0] = fmaxf(sl2 * i0, 1e-37f);
+        sl2h[nt][1] = fmaxf(sl2 * i1, 1e-37f);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int head = nt * 8 + quad;
+            const int d = kk * 16 + 2 * c4 + e * 8;
+            qb[kk][nt][e] = (head < G) ? *reinterpret_cast<const unsigned*>(qrow + head * D + d) : 0u;
+          }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sl2h[nt][0] = sl2h[nt][1] = sl2;
+    }
   }
   float o[D / 16][NT][4];
 #pragma unroll
@@ -501,7 +541,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8, NT, HG, WPH>::THREADS, WPH >
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float v = sc[u][0][nt][e] + sc[u][1][nt][e];
-          x[u][nt][e] = ((e < 2) ? va : vb) ? v * sl2 : -INFINITY;
+          x[u][nt][e] = ((e < 2) ? va : vb) ? v * sl2h[nt][e & 1] : -INFINITY;
           grow |= x[u][nt][e] > m_run[nt][e & 1] + RESCALE_LOG2;
         }
     }

@@ -170,14 +170,6 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float b, float c) {
       : "f"(b), "f"(c));
 }
 
-// Two e4m3 codes (the low 16 bits of v) -> f16x2, exactly (the hardware pair
-// conversion; every e4m3 value is an f16 value).
-__device__ __forceinline__ unsigned e4m3x2_to_f16x2(unsigned v) {
-  unsigned r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(v)));
-  return r;
-}
-
 // Widens rows [row0, row1) of an e4m3 tile, stored as rows of D bytes
 // in the last BLOCK_N x D bytes of a K or V stage, in place into the stage's
 // f16 tile in the 128-byte-swizzled layout: code c of row r goes to d half
@@ -275,27 +267,6 @@ __device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w) {
   return *reinterpret_cast<const unsigned*>(&h);
 }
 
-// f16x2 -> two e4m3 codes (low half -> low byte), round to nearest, saturating.
-__device__ __forceinline__ unsigned f16x2_to_e4m3x2(unsigned h) {
-  unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
-  return r;
-}
-
-// A bf16 pair (w), times sc = 2^k, as e4m3 hi and lo codes with hi + lo equal
-// to the scaled pair: hi rounds the 8-bit significand to 4 bits, and the
-// remainder (at most 4 significant bits, exact in f16) is lo.  Exact while the
-// scaled value's remainder is no finer than e4m3's smallest step (2^-9).
-__device__ __forceinline__ void split_pair(unsigned w, float sc, unsigned& hi, unsigned& lo) {
-  const __half2 y = __floats2half2_rn(__uint_as_float(w << 16) * sc,
-                                      __uint_as_float(w & 0xffff0000u) * sc);
-  const unsigned yb = *reinterpret_cast<const unsigned*>(&y);
-  hi = f16x2_to_e4m3x2(yb);
-  const unsigned hb = e4m3x2_to_f16x2(hi);
-  const __half2 r = __hsub2(y, *reinterpret_cast<const __half2*>(&hb));
-  lo = f16x2_to_e4m3x2(*reinterpret_cast<const unsigned*>(&r));
-}
-
 // An e4m3 call at d 128 computes the scores with 8-bit MMAs straight from the
 // cache's K codes.  Q (bf16, as TMA loaded it: two 128-byte-swizzled d halves)
 // is split in place, once its copy has landed (q_full at `parity`), into two
@@ -331,9 +302,8 @@ __device__ __forceinline__ bool split_q_tile(unsigned char* q, uint64_t* q_full,
     }
   }
   const int eb = static_cast<int>(max(m_lo, m_hi >> 16) >> 7);  // exponent field of the max
-  const int k = min(126, max(-126, 134 - eb));  // max * 2^k in [2^7, 2^8)
-  const float sc = __int_as_float((k + 127) << 23);
-  inv = __int_as_float((127 - k) << 23);
+  float sc;
+  split_scale(eb, sc, inv);  // max * sc in [2^7, 2^8)
   // code chunk c (elements 16c ... 16c + 15) comes from bf16 chunks 2(c % 4)
   // and 2(c % 4) + 1 of d half c / 4
 #pragma unroll

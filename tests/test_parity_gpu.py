@@ -61,6 +61,27 @@ def test_decode_fp8(splits):
     check_case(make(spec), num_splits=splits)
 
 
+@pytest.mark.parametrize("G,D", [(8, 128), (16, 64), (4, 128)])
+def test_decode_fp8_query_heads_of_very_different_magnitudes(G, D):
+    # The e4m3 decode scores are 8-bit MMAs on the K codes against each head's
+    # q split into e4m3 hi + lo codes after a power-of-two scaling; heads
+    # scaled from 2^-40 to 2^8 (and heads with one large entry among small
+    # ones) must still match the definition.
+    spec = small_spec(640 + G + D, H=2 * G, Hkv=2, d=D, bs=16, n_req=6, max_s=900,
+                      kv_dtype=W.KV_FP8_E4M3, kinds=("decode",))
+    case = make(spec)
+    T, H, _ = case.q.shape
+    g = torch.Generator().manual_seed(640 + G)
+    e = torch.randint(-40, 9, (T, H, 1), generator=g).float()
+    q = case.q.float() * torch.pow(2.0, e).to(DEV)
+    spike = torch.rand(T, H, generator=g).to(DEV) < 0.25
+    col = torch.randint(0, D, (T, H), generator=g).to(DEV)
+    q[spike] = q[spike] * 1e-4
+    q[spike, col[spike]] = 300.0 * torch.sign(torch.randn(int(spike.sum()), device=DEV))
+    case.q.copy_(q.to(case.q.dtype))
+    check_case(case)
+
+
 @pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_FP8_E4M3])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("Hkv", [1, 2, 4, 8])
