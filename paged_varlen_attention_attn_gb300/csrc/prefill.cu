@@ -230,41 +230,50 @@ __device__ __forceinline__ void widen_e4m3_in_place(unsigned char* stage, int ro
   }
 }
 
-// bf16x2 -> f16x2 (exact for bf16 values in f16's range; q of an e4m3 call)
-__device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w);
-
-// Converts a Q tile (bf16, as TMA loaded it) to f16 in place for the f16
-// MMAs of an e4m3 call, once its copy has landed (q_full at `parity`): an
-// elementwise change, so the swizzled layout stays.  Thread t of the
-// 128-thread softmax warpgroup converts the 16-byte pieces t + 128 i, eight
-// loads ahead; each warp then arrives on q_conv (four arrivals complete it).
-template <int TILE>
+// Converts a Q tile (bf16, as TMA loaded it: DH 128-byte-swizzled d halves)
+// to f16 in place for the f16 MMAs of an e4m3 call at d 64, once its copy has
+// landed (q_full at `parity`): an elementwise change, so the layout stays.
+// Thread t of the softmax warpgroup takes row t (the row whose scores it
+// owns) and scales it by the power of two sc that puts its largest magnitude
+// in [2^7, 2^8), so no bf16 value leaves f16's range (exact down to 2^-21 of
+// the row maximum); `inv` returns 1 / sc, by which the row's scores are
+// scaled back.  Each warp then arrives on q_conv.
+template <int DH>
 __device__ __forceinline__ bool convert_q_tile(unsigned char* q, uint64_t* q_full,
                                                uint64_t* q_conv, unsigned parity, int t,
-                                               unsigned* status, volatile int* abort_flag) {
+                                               unsigned* status, volatile int* abort_flag,
+                                               float& inv) {
   if (!__all_sync(0xffffffffu, mbar_wait(q_full, parity, status, abort_flag))) return false;
-  constexpr int PER = TILE / 16 / 128;
-  static_assert(PER % 8 == 0, "whole batches of eight pieces");
-  uint4* q4 = reinterpret_cast<uint4*>(q) + t;
-  for (int b = 0; b < PER; b += 8) {
-    uint4 w[8];
+  constexpr int HALF = BLOCK_M * 128;
+  unsigned char* row = q + t * 128;
+  const int sw = t & 7;
+  // two passes over the row's 16-byte pieces (the maximum, then the
+  // conversion, each piece written where it was read)
+  unsigned m = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = q4[128 * (b + i)];
+  for (int i = 0; i < 8 * DH; ++i) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + (i >> 3) * HALF + (((i & 7) ^ sw) << 4));
+    const unsigned v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      q4[128 * (b + i)] = make_uint4(bf16x2_to_f16x2(w[i].x), bf16x2_to_f16x2(w[i].y),
-                                     bf16x2_to_f16x2(w[i].z), bf16x2_to_f16x2(w[i].w));
+    for (int e = 0; e < 4; ++e) m = max(m, max(v[e] & 0x7fffu, (v[e] >> 16) & 0x7fffu));
+  }
+  float sc;
+  split_scale(static_cast<int>(m >> 7), sc, inv);
+#pragma unroll
+  for (int i = 0; i < 8 * DH; ++i) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + (i >> 3) * HALF + (((i & 7) ^ sw) << 4));
+    const unsigned v[4] = {w.x, w.y, w.z, w.w};
+    unsigned h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      h[e] = pack2<true>(__uint_as_float(v[e] << 16) * sc, __uint_as_float(v[e] & 0xffff0000u) * sc);
+    *reinterpret_cast<uint4*>(row + (i >> 3) * HALF + (((i & 7) ^ sw) << 4)) =
+        make_uint4(h[0], h[1], h[2], h[3]);
   }
   fence_proxy_async_smem();
   __syncwarp();
   if ((t & 31) == 0) mbar_arrive(q_conv);
   return true;
-}
-
-// bf16x2 -> f16x2 (exact for bf16 values in f16's range; q of an e4m3 call)
-__device__ __forceinline__ unsigned bf16x2_to_f16x2(unsigned w) {
-  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-  return *reinterpret_cast<const unsigned*>(&h);
 }
 
 // An e4m3 call at d 128 computes the scores with 8-bit MMAs straight from the
@@ -1074,9 +1083,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           float inv = 1.f;
           if (!(NK ? split_q_tile(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X], qn & 1,
                                   row, status, abort_flag, inv)
-                   : convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X],
-                                             &bars->q_conv[X], qn & 1, row, status,
-                                             abort_flag))) {
+                   : convert_q_tile<C::DH>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
+                                           qn & 1, row, status, abort_flag, inv))) {
             ok = false;
             break;
           }
@@ -1233,9 +1241,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           float inv = 1.f;
           if (!(NK ? split_q_tile(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X], qn & 1,
                                   row, status, abort_flag, inv)
-                   : convert_q_tile<C::TILE>(sQ + X * C::TILE, &bars->q_full[X],
-                                             &bars->q_conv[X], qn & 1, row, status,
-                                             abort_flag))) {
+                   : convert_q_tile<C::DH>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
+                                           qn & 1, row, status, abort_flag, inv))) {
             ok = false;
           } else {
             sl2r = fmaxf(sl2 * inv, 1e-37f);

@@ -7,7 +7,8 @@ float64 oracle at the e4m3 tolerance: head sizes 64 and 128, even and odd GQA
 ratios, a sliding window, block sizes 64, 128 and 256 (pages of a key tile or
 more), attention sinks, a batch of chunked prefills beside many decodes, a
 prefill request whose query is longer than its sequence (reported, rows zero,
-others exact), and query rows whose magnitudes span 2^-40 to 2^8."""
+others exact), and query rows whose magnitudes span 2^-40 to 2^8 (both head
+sizes)."""
 import numpy as np
 import pytest
 import torch
@@ -105,14 +106,16 @@ def test_query_longer_than_its_sequence():
             assert_close(out[x:y].float().cpu().numpy(), ref[x:y], W.KV_FP8_E4M3)
 
 
-def test_query_rows_of_very_different_magnitudes():
+@pytest.mark.parametrize("d", [128, 64])
+def test_query_rows_of_very_different_magnitudes(d):
     # At head size 128 the scores are 8-bit MMAs on the K codes against a Q
-    # split per row into e4m3 hi + lo codes after a power-of-two scaling; rows
-    # scaled from 2^-40 to 2^8 (and rows with one large entry among small
-    # ones) must still match the definition.  (Larger rows would give scores
-    # whose log2-domain magnitude, above ~2^20, an fp32 softmax cannot resolve
-    # to a unit: a limit of every path, not of the split.)
-    sp = small_spec(1880, H=8, Hkv=2, d=128, bs=16, n_req=4, max_s=400, kinds=("prefill",),
+    # split per row into e4m3 hi + lo codes after a power-of-two scaling; at
+    # 64 Q rows are scaled by a power of two into f16's range for the f16
+    # MMAs.  Rows scaled from 2^-40 to 2^8 (and rows with one large entry
+    # among small ones) must still match the definition.  (Larger rows would
+    # give scores whose log2-domain magnitude, above ~2^20, an fp32 softmax
+    # cannot resolve to a unit: a limit of every path, not of the scaling.)
+    sp = small_spec(1880 + d, H=8, Hkv=2, d=d, bs=16, n_req=4, max_s=400, kinds=("prefill",),
                     kv_dtype=W.KV_FP8_E4M3)
     case = W.make_case(sp, device=DEV)
     T, H, D = case.q.shape
