@@ -1038,13 +1038,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     unsigned ph = 0;
     bool ok = true;
     int qn = 0;             // Q tiles of this sub-tile converted so far (FP8)
-    bool q_ahead = false;   // this item's Q tile was converted during the previous item
-    // Score scale of this row: sl2, over a split Q (NK) times the row's 1 / sc,
+    // Score scale of this row: sl2, over an e4m3 cache times the row's 1 / sc,
     // kept normal so that a masked score (-inf) still maps to -inf.  Set when
-    // the item's Q tile is split (the previous item no longer needs it then).
+    // the item's Q tile is converted (the previous item no longer needs it).
     float sl2r = sl2;
-    Item it = load_item(p, item_at(0), n_items, NP, KC);
-    for (int k = 0; ok && k * GS < n_items; ++k) {
+    // An e4m3 call converts each item's Q tile at the end of the previous
+    // item (below), so its loop starts one step early, on an empty item, to
+    // convert the first one there too: one copy of that long code.
+    Item it = load_item(p, FP8 ? n_items : item_at(0), n_items, NP, KC);
+    for (int k = FP8 ? -1 : 0; ok && k * GS < n_items; ++k) {
       const Sub u = make_sub(p, it, head_pairs, X);
       const Sub subA = X ? make_sub(p, it, head_pairs, 0) : u;
       const Sub subB = X ? u : make_sub(p, it, head_pairs, 1);
@@ -1076,23 +1078,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const int chunk = it.chunk;
       float m_run = -INFINITY, l_run = 0.f;
       const int nt = u.x1 - u.x0;
-      if constexpr (FP8) {
-        // an e4m3 call's Q tile is split (d 128) or becomes f16 (d 64) before
-        // its first scores
-        if (nt > 0 && !q_ahead) {
-          float inv = 1.f;
-          if (!(NK ? split_q_tile(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X], qn & 1,
-                                  row, status, abort_flag, inv)
-                   : convert_q_tile<C::DH>(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X],
-                                           qn & 1, row, status, abort_flag, inv))) {
-            ok = false;
-            break;
-          }
-          sl2r = fmaxf(sl2 * inv, 1e-37f);
-          ++qn;
-        }
-        q_ahead = false;
-      }
       for (int c = 0; c < nt; ++c) {
         const int kt = u.x0 + c;
         const int key0 = kt * BLOCK_N;
@@ -1235,8 +1220,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const Item nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
       if constexpr (FP8) {
         // The next item's Q tile of this sub-tile is loaded once this item's
-        // last S MMA is done: convert it now, while the last P V runs, so
-        // the next item's first scores need not wait for the epilogue.
+        // last S MMA is done: split it (d 128) or convert it to f16 (d 64)
+        // now, while the last P V runs, so the next item's first scores need
+        // not wait for the epilogue.
         if (ok && make_sub(p, nxt, head_pairs, X).x1 > make_sub(p, nxt, head_pairs, X).x0) {
           float inv = 1.f;
           if (!(NK ? split_q_tile(sQ + X * C::TILE, &bars->q_full[X], &bars->q_conv[X], qn & 1,
@@ -1247,7 +1233,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           } else {
             sl2r = fmaxf(sl2 * inv, 1e-37f);
             ++qn;
-            q_ahead = true;
           }
         }
       }
