@@ -148,8 +148,13 @@ typedef struct {
  *   causal          1: k <= p; 0: every key < seq_len (then window must be <= 0)
  *   kv_dtype        a pattn_kv_dtype_t.  With e4m3, decode rows run on the
  *                   bandwidth-bound decode kernel and prefill rows on the
- *                   tensor-core prefill kernel, which widens K and V tiles to
- *                   f16 (exactly) and rounds q to f16 for its f16 MMAs
+ *                   tensor-core prefill kernel.  At head_size 128 its score
+ *                   MMAs take the K codes as they are, against each q row
+ *                   split exactly into two e4m3 codes per value after a
+ *                   power-of-two scaling, and V tiles are widened to f16
+ *                   (exactly) for f16 P V MMAs; at 64 K and V are widened and
+ *                   q is scaled per row into f16 (the decode kernel likewise
+ *                   per head)
  *   kv_scale        host float[2] {k_scale, v_scale}; required for e4m3, ignored
  *                   for bf16 (may be NULL)
  *   ext             host sizes, workspace and stream (see pattn_ext_t)
