@@ -269,3 +269,22 @@ def test_full_size_workload_sampled_rows(cfg):
     assert torch.isfinite(out.float()).all()
     del case, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_full_size_workload_over_an_e4m3_cache_sampled_rows(cfg):
+    # the varlen prefill and the mixed workload (co-scheduled kernels) with
+    # their caches quantised to e4m3: the prefill rows take the 8-bit score
+    # MMAs against the split q, the decode rows the widening decode kernel
+    import dataclasses
+    case = make(dataclasses.replace(W.config_spec(cfg), kv_dtype=W.KV_FP8_E4M3))
+    out = run_gpu(case)
+    rows = _sample_rows(case, seed=10 + cfg)
+    ref, _ = oracle_sampled(case, rows)
+    t = torch.tensor([r[0] for r in rows], device=DEV)
+    h = torch.tensor([r[1] for r in rows], device=DEV)
+    got = out[t, h].float().cpu().numpy()
+    assert_close(got, ref, W.KV_FP8_E4M3)
+    assert torch.isfinite(out.float()).all()
+    del case, out
+    torch.cuda.empty_cache()
