@@ -20,11 +20,13 @@
 //   warps 4-7  softmax + epilogue of sub-tile B, likewise
 //   warp  8    TMA producer of both Q tiles of each item and the K tiles, page by
 //              page through block_table into a 3-stage ring, one lane per
-//              page copy (over an e4m3 cache at d 64 it also widens each K tile)
+//              page copy (over an e4m3 cache it also widens each K tile at d
+//              64, and rows 80-127 of each V tile at d 128)
 //   warp  9    MMA issuer (one thread): sub-tile A's MMAs (both sub-tiles'
 //              over an e4m3 cache at d 64)
-//   warp 10    TMA producer of the V tiles (2-stage ring), one page per copy
-//              (over an e4m3 cache it also widens each V tile to f16)
+//   warp 10    TMA producer of the V tiles (2-stage ring; 3 over an e4m3 cache
+//              at d 128), one page per copy (over an e4m3 cache it also widens
+//              each V tile to f16, rows 0-79 of it at d 128)
 //   warp 11    MMA issuer of sub-tile B (the two issuers take turns); idle
 //              over an e4m3 cache at d 64
 // Over an e4m3 cache at d 128 the scores are 8-bit MMAs (kind::f8f6f4) on the
@@ -428,10 +430,12 @@ __device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) 
 }
 
 // HALF: q, the cache and out are f16 (else bf16).  FP8: an e4m3 cache with
-// bf16 q and out; K and V tiles are widened to f16 in shared memory (exact:
-// every e4m3 value is an f16 value), each softmax warpgroup converts its Q
-// tile to f16 in place, and the MMAs and P run in f16; the K scale is in sl2
-// and the V scale is out_scale.
+// bf16 q and out.  V tiles are widened to f16 in shared memory (exact: every
+// e4m3 value is an f16 value) and P V runs in f16.  At d 128 the score MMAs
+// take the K codes as they are against each Q tile split in place into e4m3
+// hi and lo codes; at d 64 K tiles are widened too and each Q tile is scaled
+// and converted to f16 in place.  The per-row scale of Q, the K scale and
+// sl2 make the row's score scale; the V scale is out_scale.
 //
 // Persistent: the grid holds at most one CTA per SM and CTA b takes items
 // b, 2G-1-b, 2G+b, ... of the LPT-ordered list (G = grid size; the order
@@ -781,14 +785,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // A tcgen05.mma occupies its issuing thread for about as long as the
     // tensor core takes to run it, so everything else that thread does (barrier
     // waits, commits, bookkeeping) leaves the tensor core idle.  With TWO
-    // (a 16-bit cache) two threads issue: warp 9 sub-tile
+    // (a 16-bit cache, or e4m3 at d 128) two threads issue: warp 9 sub-tile
     // A's MMAs, warp 11 sub-tile B's.  They take turns, A then B for each key
     // tile, handing a token over through tok[] (A's turn t waits for B's turn
     // t - 1, B's turn t for A's turn t), and each waits for its operands and
     // commits while the other one issues.  Each commits its own release of
     // every K and V stage and of the Q tiles (those barriers then count one
-    // arrival per issuer).  Otherwise warp 9 issues both sub-tiles' MMAs in
-    // the same order (over an e4m3 cache warp 11 widens tiles).
+    // arrival per issuer).  Otherwise (an e4m3 cache at d 64) warp 9 issues
+    // both sub-tiles' MMAs in the same order.
     if (lane == 0) {
       constexpr unsigned idesc_s = make_idesc_f16(BLOCK_M, BLOCK_N, !MMA_F16, false);
       // e4m3 x e4m3 (type fields 0), fp32 accumulation, both K-major
@@ -1354,8 +1358,8 @@ cudaError_t launch_prefill(const Problem& p, const CUtensorMap& q_map, const CUt
   if (p.kv_dtype == PATTN_KV_F16)
     return p.D == 128 ? launch_prefill_t<128, true, false, true>(p, q_map, k_map, v_map, g)
                       : launch_prefill_t<64, true, false, true>(p, q_map, k_map, v_map, g);
-  // An e4m3 cache at d 128 takes two as well (its score MMAs read the K codes
-  // directly, so warp 11 no longer widens); at d 64 one.
+  // An e4m3 cache at d 128 takes two as well (no warp widens K tiles there:
+  // the score MMAs read the codes as they are); at d 64 one.
   if (p.kv_dtype == PATTN_KV_FP8_E4M3)
     return p.D == 128 ? launch_prefill_t<128, false, true, true>(p, q_map, k_map, v_map, g)
                       : launch_prefill_t<64, false, true, false>(p, q_map, k_map, v_map, g);
