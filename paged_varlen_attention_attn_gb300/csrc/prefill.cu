@@ -315,6 +315,10 @@ __device__ __forceinline__ bool split_q_tile(unsigned char* q, uint64_t* q_full,
   const int eb = static_cast<int>(max(m_lo, m_hi >> 16) >> 7);  // exponent field of the max
   float sc;
   split_scale(eb, sc, inv);  // max * sc in [2^7, 2^8)
+  // A row holding an inf or a NaN (exponent field 255) gets NaN codes, so its
+  // scores and output are NaN as the definition gives (the saturating
+  // conversion would turn an inf into a finite code).
+  const unsigned nan_row = (eb == 255) ? 0x7f7f7f7fu : 0u;
   // code chunk c (elements 16c ... 16c + 15) comes from bf16 chunks 2(c % 4)
   // and 2(c % 4) + 1 of d half c / 4
 #pragma unroll
@@ -326,8 +330,8 @@ __device__ __forceinline__ bool split_q_tile(unsigned char* q, uint64_t* q_full,
     for (int e = 0; e < 8; ++e) split_pair(v[e], sc, hi[e], lo[e]);
     const int pos = (c ^ sw) << 4;
     *reinterpret_cast<uint4*>(row + pos) =
-        make_uint4(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16),
-                   hi[6] | (hi[7] << 16));
+        make_uint4(hi[0] | (hi[1] << 16) | nan_row, hi[2] | (hi[3] << 16) | nan_row,
+                   hi[4] | (hi[5] << 16) | nan_row, hi[6] | (hi[7] << 16) | nan_row);
     *reinterpret_cast<uint4*>(row + HALF + pos) =
         make_uint4(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16), lo[4] | (lo[5] << 16),
                    lo[6] | (lo[7] << 16));

@@ -288,3 +288,35 @@ def test_full_size_workload_over_an_e4m3_cache_sampled_rows(cfg):
     assert torch.isfinite(out.float()).all()
     del case, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_FP8_E4M3])
+@pytest.mark.parametrize("D", [128, 64])
+def test_query_row_with_a_nan_gives_nan_there_only(kv_dtype, D):
+    # The definition makes a (row, head) whose q holds a NaN all NaN (every
+    # score is NaN); every path must give NaN there, whatever its operand
+    # handling (f16 q, the e4m3 split into hi + lo codes), and leave the other
+    # rows exact.
+    spec = small_spec(1400 + D + kv_dtype, H=8, Hkv=2, d=D, bs=16, n_req=6, max_s=500,
+                      kv_dtype=kv_dtype)
+    case = make(spec)
+    T = case.q.shape[0]
+    g = torch.Generator().manual_seed(1400 + D)
+    bad = [(int(t), int(h)) for t, h in zip(torch.randint(0, T, (6,), generator=g),
+                                            torch.randint(0, 8, (6,), generator=g))]
+    qsl = case.query_start_loc.cpu().numpy()
+    bad.append((int(qsl[-1]) - 1, 3))  # the last request's last row
+    for t, h in bad:
+        case.q[t, h, (t * 7 + h) % D] = float("nan")
+    out = run_gpu(case).float().cpu().numpy()
+    ref, _ = oracle_all(case)
+    a, b = valid_rows(case)
+    keep = np.zeros(out.shape[:2], dtype=bool)
+    keep[a:b] = True
+    for t, h in bad:
+        if a <= t < b:
+            assert np.isnan(out[t, h]).all(), (t, h)
+            assert np.isnan(ref[t, h]).all(), (t, h)
+        keep[t, h] = False
+    assert np.isfinite(ref[keep]).all()
+    assert_close(out[keep], ref[keep], kv_dtype)
