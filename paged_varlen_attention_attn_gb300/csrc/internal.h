@@ -19,7 +19,9 @@ struct WsHeader {
   int prefill_ctas;       // written by the plan kernel: CTAs of the prefill grid
                           // that run (0: all); the decode grid takes the SMs of
                           // the others while prefill runs
-  int pad[61];
+  unsigned next_item;     // zeroed by the plan kernel: prefill items claimed past
+                          // each CTA's first
+  int pad[60];
 };
 
 struct Problem {

@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
     s_dec_blocks = 0ull;
   }
   if (tid == 0 && p.clear_status) p.hdr->status = 0u;
+  if (tid == 0) p.hdr->next_item = 0u;
   for (int i = tid; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) decode_prep_kernel(const Problem
     p.hdr->status = 0u;
     p.hdr->num_prefill_tiles = 0;
     p.hdr->prefill_ctas = 0;
+    p.hdr->next_item = 0u;
     s_dec_blocks = 0ull;
   }
   for (int i = threadIdx.x; i < p.B * p.Hkv; i += PLAN_THREADS) p.counters[i] = 0u;

@@ -90,6 +90,10 @@ static_assert(2 * 128 * softmax_regs(true) + 128 * other_regs(true) == SPLIT_REG
 constexpr int PF_KST = 3;
 constexpr int PF_VST = 2;
 constexpr int PF_VST_MAX = 3;
+// Item ring: the indices of this CTA's next items, claimed one ahead by warp 8
+constexpr int PF_RING = 4;
+// Rounds of the item list at its end that CTAs claim as they get free
+constexpr int DYN_ROUNDS = 4;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 // 2^RESCALE_THRESHOLD: if any of a row's weights against an unmoved
 // reference exceeds it, so does their sum; a sum above this sends the tile
@@ -144,9 +148,14 @@ struct Bars {
   uint64_t q_empty;     // every S MMA of an item issued and done: Q may be replaced
   uint64_t drain;       // every MMA issued, before TMEM is released
   uint64_t tok[2];      // issuer X may take its turn (two MMA issuers)
+  uint64_t ring_full[PF_RING];   // slot i holds the index of this CTA's next item
+  uint64_t ring_empty[PF_RING];  // every role has taken slot i
+  int ring[PF_RING];
   unsigned tmem_base;
   int abort_flag;
 };
+
+static_assert(sizeof(Bars) <= 512, "the barriers fit the space kept for them");
 
 struct Sub {
   int h, i0, i_last, x0, x1;
@@ -483,9 +492,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   // The decode kernel of the same call reads nothing this kernel writes.
   if (p.pdl_trigger && threadIdx.x == 0) grid_dep_trigger();
   if (static_cast<int>(blockIdx.x) >= n_items || static_cast<int>(blockIdx.x) >= GS) return;
-  auto item_at = [&](int k) {
-    return k * GS + ((k & 1) ? GS - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
-  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -514,6 +520,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     mbar_init(&bars->q_conv[0], 4);  // one arrival per warp of the softmax warpgroup
     mbar_init(&bars->q_conv[1], 4);
     mbar_init(&bars->drain, TWO ? 2 : 1);
+    // the item ring: posted by warp 8; taken by warp 10, each MMA issuer and
+    // each softmax warp
+    for (int i = 0; i < PF_RING; ++i) {
+      mbar_init(&bars->ring_full[i], 1);
+      mbar_init(&bars->ring_empty[i], 1 + (TWO ? 2 : 1) + 8);
+    }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -526,6 +538,38 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   tc_fence_after();
   const unsigned tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
+
+  // The CTA's k-th item, from the longest-first list.  The first rounds
+  // follow a fixed order: CTA b takes items b, 2G-1-b, 2G+b, ... (G = GS; the
+  // order snakes so that no CTA draws the heaviest item of every round).  The
+  // last DYN_ROUNDS rounds' worth of items go to whichever CTA asks first:
+  // warp 8 claims each with an atomic on the workspace counter (the plan
+  // kernel zeroes it), so CTAs that ran ahead take more of the tail.  Warp 8
+  // claims one item ahead and posts the index in the item ring, where the
+  // other roles take it.  An index of n_items or more ends the CTA's
+  // sequence.  A wait that gives up returns -1.
+  const int rounds = (n_items + GS - 1) / GS;
+  const int fixed_rounds = max(0, rounds - DYN_ROUNDS);
+  auto claim = [&](int k) -> int {  // warp 8, one thread
+    int idx = (k < fixed_rounds)
+                  ? k * GS + ((k & 1) ? GS - 1 - static_cast<int>(blockIdx.x)
+                                      : static_cast<int>(blockIdx.x))
+                  : fixed_rounds * GS + static_cast<int>(atomicAdd(&p.hdr->next_item, 1u));
+    idx = min(idx, n_items);
+    const int slot = k % PF_RING;
+    if (k >= PF_RING &&
+        !mbar_wait(&bars->ring_empty[slot], ((k / PF_RING) - 1) & 1, status, abort_flag))
+      return -1;
+    bars->ring[slot] = idx;
+    mbar_arrive(&bars->ring_full[slot]);
+    return idx;
+  };
+  auto take = [&](int k) -> int {  // every other role: one thread, or all lanes of a warp
+    const int slot = k % PF_RING;
+    if (!mbar_wait(&bars->ring_full[slot], (k / PF_RING) & 1, status, abort_flag)) return -1;
+    return *reinterpret_cast<volatile int*>(&bars->ring[slot]);
+  };
+  auto release = [&](int k) { mbar_arrive(&bars->ring_empty[k % PF_RING]); };
 
   unsigned char* sQ = smem + C::Q_OFF;
   unsigned char* sK = smem + C::K_OFF;
@@ -572,10 +616,32 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #else
     constexpr int skip_pos = -1;
 #endif
-    Item nxt = load_item(p, item_at(0), n_items, NP, KC);
-    for (int k = 0; k * GS < n_items; ++k) {
+    // Warp 8 claims the next item as it starts the current one (its metadata
+    // then loads in the shadow of this item); warp 10 takes the items from the
+    // ring, one ahead as well.
+    auto next_index = [&](int k) {
+      int idx = 0;
+      if (lane == 0) {
+        if (kv == 0) {
+          idx = claim(k);
+        } else {
+          idx = take(k);
+          if (idx >= 0) release(k);
+        }
+      }
+      return __shfl_sync(FULL, idx, 0);
+    };
+    int idx_next = next_index(0);
+    if (idx_next < 0) gave_up = true;
+    Item nxt = load_item(p, gave_up ? n_items : idx_next, n_items, NP, KC);
+    for (int k = 0; !gave_up && nxt.live; ++k) {
       const Item it = nxt;
-      nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
+      idx_next = next_index(k + 1);
+      if (idx_next < 0) {
+        gave_up = true;
+        break;
+      }
+      nxt = load_item(p, idx_next, n_items, NP, KC);
       const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
       int u0;
       const int n_union = union_tiles(subA, subB, u0);
@@ -817,8 +883,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         int q_tot = 0;      // Q tiles of sub-tile X so far (q_full phase)
         unsigned turn = 0;  // turns taken so far
         bool ok = true;
-        for (int k = 0; ok && k * GS < n_items; ++k) {
-          const Item it = load_item(p, item_at(k), n_items, NP, KC);
+        for (int k = 0; ok; ++k) {
+          const int idx = take(k);
+          if (idx < 0) {
+            ok = false;
+            break;
+          }
+          release(k);
+          const Item it = load_item(p, idx, n_items, NP, KC);
+          if (!it.live) break;
           const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
           int u0;
           const int n_union = union_tiles(subA, subB, u0);
@@ -925,8 +998,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         int pv_tot0 = 0, pv_tot1 = 0;  // P V of sub-tile X so far (p_full phase)
         int q_tot0 = 0, q_tot1 = 0;    // Q tiles of sub-tile X so far (q_full phase)
         bool issued = false, ok = true;
-        for (int k = 0; ok && k * GS < n_items; ++k) {
-          const Item it = load_item(p, item_at(k), n_items, NP, KC);
+        for (int k = 0; ok; ++k) {
+          const int idx = take(k);
+          if (idx < 0) {
+            ok = false;
+            break;
+          }
+          release(k);
+          const Item it = load_item(p, idx, n_items, NP, KC);
+          if (!it.live) break;
           const Sub subA = make_sub(p, it, head_pairs, 0), subB = make_sub(p, it, head_pairs, 1);
           int u0;
           const int n_union = union_tiles(subA, subB, u0);
@@ -1053,8 +1133,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // An e4m3 call converts each item's Q tile at the end of the previous
     // item (below), so its loop starts one step early, on an empty item, to
     // convert the first one there too: one copy of that long code.
-    Item it = load_item(p, FP8 ? n_items : item_at(0), n_items, NP, KC);
-    for (int k = FP8 ? -1 : 0; ok && k * GS < n_items; ++k) {
+    // Each softmax warp takes every item index from the ring (all lanes wait,
+    // one arrival per warp).
+    auto take_warp = [&](int k) {
+      const int idx = take(k);
+      const bool got = __all_sync(FULL, idx >= 0);
+      if (got && lane == 0) release(k);
+      return got ? idx : -1;
+    };
+    Item it = load_item(p, n_items, n_items, NP, KC);  // none yet
+    if (!FP8) {
+      const int idx0 = take_warp(0);
+      if (idx0 < 0) ok = false;
+      else it = load_item(p, idx0, n_items, NP, KC);
+    }
+    for (int k = FP8 ? -1 : 0; ok && (k < 0 || it.live); ++k) {
       const Sub u = make_sub(p, it, head_pairs, X);
       const Sub subA = X ? make_sub(p, it, head_pairs, 0) : u;
       const Sub subB = X ? u : make_sub(p, it, head_pairs, 1);
@@ -1225,7 +1318,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       ph = ((ph ^ (nt & 1)) & 3) | ((((ph >> 2) + static_cast<unsigned>(n_union)) % VPOS) << 2);
       // The next item's metadata is fetched here, where the score registers
       // are dead, and lands while the epilogue runs.
-      const Item nxt = load_item(p, item_at(k + 1), n_items, NP, KC);
+      const int idx_next = ok ? take_warp(k + 1) : -1;
+      if (idx_next < 0) ok = false;
+      const Item nxt = load_item(p, ok ? idx_next : n_items, n_items, NP, KC);
       if constexpr (FP8) {
         // The next item's Q tile of this sub-tile is loaded once this item's
         // last S MMA is done: split it (d 128) or convert it to f16 (d 64)
