@@ -450,9 +450,10 @@ __device__ __forceinline__ int union_tiles(const Sub& a, const Sub& b, int& u0) 
 // and converted to f16 in place.  The per-row scale of Q, the K scale and
 // sl2 make the row's score scale; the V scale is out_scale.
 //
-// Persistent: the grid holds at most one CTA per SM and CTA b takes items
-// b, 2G-1-b, 2G+b, ... of the LPT-ordered list (G = grid size; the order
-// snakes so that no CTA draws the heaviest item of every round).  Every role
+// Persistent: the grid holds at most one CTA per SM; its items come from the
+// LPT-ordered list, in a fixed order for the first rounds and claimed as
+// CTAs get free for the last ones (warp 8 posts them in the item ring, see
+// claim below).  Every role
 // walks the same item sequence and keeps its ring stages and barrier phases as
 // running counts across items, so the next item's Q, K and first scores go out
 // while the last P V and the epilogue of the current one run.  Two orderings
