@@ -94,25 +94,48 @@ __device__ int scan_descending(int* hist, int* warp_sums) {
   return total;
 }
 
+// Adds n to hist[key] for every lane in `lanes` (the calling lanes, which
+// all execute this) and returns each lane's old value plus its rank among the
+// lanes with the same key: one shared-memory atomic per distinct key in the
+// warp (decode batches often share one cost, whose lane-by-lane atomics
+// would serialise).
+__device__ __forceinline__ int hist_add_warp(int* hist, int key, unsigned lanes) {
+  const int lane = threadIdx.x & 31;
+  const unsigned peers = __match_any_sync(lanes, key);
+  const int leader = __ffs(peers) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(&hist[key], __popc(peers));
+  base = __shfl_sync(peers, base, leader);
+  return base + __popc(peers & ((1u << lane) - 1u));
+}
+
 // Writes p.decode_order: every request, by decreasing decode cost (a counting
 // sort; the order within one cost is whatever the atomics give).  cost0 is
 // the decode cost of the thread's first request (request tid), which the
 // caller read; a larger batch reads the rest here.  Adds the visible KV
-// blocks of every decode row to *blocks.
+// blocks of every decode row to *blocks.  The whole warp walks the requests
+// together (its lanes past the batch take no part), so that its atomics can
+// be combined.
 __device__ void order_decodes(const Problem& p, int* hist, int* warp_sums,
                               unsigned long long* blocks, int cost0) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   for (int b = tid; b < NBUCKET; b += PLAN_THREADS) hist[b] = 0;
   __syncthreads();
-  for (int r = tid; r < p.B; r += PLAN_THREADS) {
-    const int c = r == tid ? cost0 : decode_cost(p, r);
-    atomicAdd(&hist[c], 1);
-    atomicAdd(blocks, static_cast<unsigned long long>(c));
+  for (int r = tid; r - lane < p.B; r += PLAN_THREADS) {
+    const bool in = r < p.B;
+    const unsigned lanes = __ballot_sync(0xffffffffu, in);
+    const int c = !in ? 0 : (r == tid ? cost0 : decode_cost(p, r));
+    if (in) hist_add_warp(hist, c, lanes);
+    const unsigned sum = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(c));
+    if (lane == 0) atomicAdd(blocks, static_cast<unsigned long long>(sum));
   }
   __syncthreads();
   scan_descending(hist, warp_sums);
-  for (int r = tid; r < p.B; r += PLAN_THREADS)
-    p.decode_order[atomicAdd(&hist[r == tid ? cost0 : decode_cost(p, r)], 1)] = r;
+  for (int r = tid; r - lane < p.B; r += PLAN_THREADS) {
+    const bool in = r < p.B;
+    const unsigned lanes = __ballot_sync(0xffffffffu, in);
+    if (in) p.decode_order[hist_add_warp(hist, r == tid ? cost0 : decode_cost(p, r), lanes)] = r;
+  }
 }
 
 // Estimated time (us) of a mixed batch whose prefill keeps `gs` SMs and
@@ -122,19 +145,19 @@ __device__ void order_decodes(const Problem& p, int* hist, int* warp_sums,
 // item, and never less than the total work over gs SMs.  Decode: m SMs
 // stream at dec_bytes_per_us each, capped by the HBM bandwidth beside prefill.
 // cost[t]: the key tiles of sorted tile t (kept in shared memory by pass 2).
+// (fp32 throughout: an estimate, and GB300's fp64 is slow)
 __device__ float co_schedule_estimate(const Problem& p, const unsigned short* cost, int gs,
-                                      int n_items, int np, unsigned long long work_items,
-                                      double dec_bytes) {
+                                      int n_items, int np, float work_items, float dec_bytes) {
   float rounds = 0.f;
   for (int x = 0; x < n_items; x += gs) rounds += static_cast<float>(cost[x / np]);
-  const float t_pre = p.pf_us_per_tile * fmaxf(rounds, static_cast<float>(work_items) / gs);
+  const float t_pre = p.pf_us_per_tile * fmaxf(rounds, work_items / gs);
   const int m = p.num_sms - gs;
   const float full_rate = fminf(p.num_sms * p.dec_bytes_per_us, p.hbm_bytes_per_us);
-  if (m <= 0) return t_pre + static_cast<float>(dec_bytes / full_rate);
+  if (m <= 0) return t_pre + dec_bytes / full_rate;
   const float rate = fminf(m * p.dec_bytes_per_us, p.hbm_bytes_per_us);
-  const float t_dec = static_cast<float>(dec_bytes / rate);
+  const float t_dec = dec_bytes / rate;
   if (t_dec <= t_pre) return t_pre;
-  return t_pre + static_cast<float>((dec_bytes - static_cast<double>(rate) * t_pre) / full_rate);
+  return t_pre + (dec_bytes - rate * t_pre) / full_rate;
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
@@ -229,14 +252,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
   }
   const int np = ((p.G % 2) == 0 ? p.H / 2 : p.H) * p.kv_chunks;
   const int n_items = min(p.hdr->num_prefill_tiles, p.max_tiles) * np;
-  const double dec_bytes = static_cast<double>(s_dec_blocks) * p.bs * p.Hkv * 2.0 * p.D *
-                           (p.kv_dtype == PATTN_KV_FP8_E4M3 ? 1.0 : 2.0);
-  const unsigned long long work_items = s_tile_work * static_cast<unsigned long long>(np);
+  const float dec_bytes = static_cast<float>(s_dec_blocks) * static_cast<float>(p.bs * p.Hkv) *
+                          2.f * p.D * (p.kv_dtype == PATTN_KV_FP8_E4M3 ? 1.f : 2.f);
+  const float work_items = static_cast<float>(s_tile_work) * np;
   float best = INFINITY;
   int best_gs = p.num_sms;
   // (the tile costs are kept for the first NBUCKET sorted tiles; a batch with
   // more keeps every SM for its prefill)
-  if (n_items > 0 && dec_bytes > 0.0 && n_items / np <= NBUCKET) {
+  if (n_items > 0 && dec_bytes > 0.f && n_items / np <= NBUCKET) {
     for (int gs = p.num_sms - tid; gs >= max(1, p.num_sms / 2); gs -= PLAN_THREADS) {
       const float e = co_schedule_estimate(p, s_cost, gs, n_items, np, work_items, dec_bytes);
       if (e < best || (e == best && gs > best_gs)) {
