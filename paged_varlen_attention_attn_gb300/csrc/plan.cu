@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const Problem p) {
     return;
   }
   const int np = ((p.G % 2) == 0 ? p.H / 2 : p.H) * p.kv_chunks;
-  const int n_items = min(p.hdr->num_prefill_tiles, p.max_tiles) * np;
+  const int n_items = min(run, p.max_tiles) * np;  // (run: every thread has it)
   const float dec_bytes = static_cast<float>(s_dec_blocks) * static_cast<float>(p.bs * p.Hkv) *
                           2.f * p.D * (p.kv_dtype == PATTN_KV_FP8_E4M3 ? 1.f : 2.f);
   const float work_items = static_cast<float>(s_tile_work) * np;
