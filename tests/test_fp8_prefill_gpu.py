@@ -64,7 +64,8 @@ def _check(case, out, sinks=None, skip=()):
 
 @pytest.mark.parametrize("H,Hkv,d,bs,window", [(8, 2, 128, 16, 0), (6, 2, 64, 16, 0),
                                                (4, 4, 128, 64, 0), (16, 2, 128, 16, 90),
-                                               (12, 4, 128, 256, 0), (8, 8, 64, 128, 0)])
+                                               (12, 4, 128, 256, 0), (8, 8, 64, 128, 0),
+                                               (8, 2, 64, 16, 50), (6, 2, 128, 32, 130)])
 def test_mixed_batches(H, Hkv, d, bs, window):
     sp = small_spec(1800 + H + d + bs + window, H=H, Hkv=Hkv, d=d, bs=bs, n_req=6, max_s=600,
                     window=window, kv_dtype=W.KV_FP8_E4M3)
