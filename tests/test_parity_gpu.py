@@ -320,3 +320,27 @@ def test_query_row_with_a_nan_gives_nan_there_only(kv_dtype, D):
         keep[t, h] = False
     assert np.isfinite(ref[keep]).all()
     assert_close(out[keep], ref[keep], kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_FP8_E4M3])
+def test_one_long_prefill_and_a_long_chunk_sampled_rows(kv_dtype):
+    # a 32,768-token prefill (256 key tiles for its last row tiles) and a
+    # 4,096-token chunk on 28,672 cached tokens beside two decodes: long items
+    # that cross many ring stages, and few enough items that CTAs claim most
+    # of them at run time; rows sampled at tile edges against the oracle
+    q_lens = [32768, 4096, 1, 1]
+    seq = [32768, 32768, 32768, 9000]
+    spec = W.CaseSpec("long_prefill", q_lens, seq, 8, 2, 128, 16, kv_dtype=kv_dtype,
+                      pool_blocks=sum((s + 15) // 16 for s in seq) + 8, seed=1500 + kv_dtype)
+    case = make(spec)
+    out = run_gpu(case)
+    rows = _sample_rows(case, n_per_req=4, seed=1500)
+    qsl = case.query_start_loc.cpu().numpy()
+    rows += [(int(qsl[0]) + 32767, 5), (int(qsl[1]) + 4095, 2)]  # the longest rows
+    ref, _ = oracle_sampled(case, rows)
+    t = torch.tensor([r[0] for r in rows], device=DEV)
+    h = torch.tensor([r[1] for r in rows], device=DEV)
+    assert_close(out[t, h].float().cpu().numpy(), ref, kv_dtype)
+    assert torch.isfinite(out.float()).all()
+    del case, out
+    torch.cuda.empty_cache()
