@@ -933,7 +933,9 @@ def kernel_roofline(kind, counts, ms, pk, pk_src, spec):
         peak = pk["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "kernel": "prefill_kernel" + (" (e4m3 tiles widened to f16 in shared memory)"
+                "kernel": "prefill_kernel" + ((" (e4m3: 8-bit score MMAs on the K codes, V "
+                                               "widened to f16)" if spec.head_size == 128 else
+                                               " (e4m3 tiles widened to f16)")
                                               if spec.kv_dtype == 1 else ""),
                 "work_per_launch": f"{counts['flops_prefill']:.6g} FLOP (4 d per visible "
                                    f"(row, key, head))"}
